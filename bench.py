@@ -1,0 +1,362 @@
+"""Benchmark: NVFP4 row-scaled quantize-transpose of linear-layer operands.
+
+One step = the whole hot path over one batch: for the activation X (16384 x 8192
+BF16) and the gradient dY (16384 x 28672 BF16), the fused exact row+column amax
+pass followed by the encode pass that writes rowwise and columnwise E2M1 codes
+and E4M3 scales (row-scaled: rows use the row amax, columns the column amax).
+
+The step is issued as nvfp4_amax + nvfp4_quantize_both(amax_in = that amax) per
+operand -- the same three kernels nvfp4_quantize_both launches on its own --
+so that CUDA events on the launching stream can time the encode kernel alone
+for the roofline figure.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("NVFP4 quantize-transpose GB/s (BF16 in + codes/scales out) and % of GB300 HBM peak")
+ROWS, K_X, K_DY = 16384, 8192, 28672
+WORKLOAD = ("linear-layer operands: X 16384x8192 and dY 16384x28672 BF16, N(0,0.02) x per-row "
+            "LogNormal(0,1); row-scaled NVFP4 quantize, fused row+col amax, rowwise+columnwise "
+            "1x16 E2M1/E4M3 outputs, bound 448")
+
+
+def bytes_io(rows, cols):
+    """BF16 in once + codes + scales (both directions) + amax out."""
+    codes = rows * ((cols + 1) // 2) + cols * ((rows + 1) // 2)
+    scales = rows * ((cols + 15) // 16) + cols * ((rows + 15) // 16)
+    return 2 * rows * cols + codes + scales + 4 * (rows + cols)
+
+
+def bytes_min(rows, cols):
+    """B_io plus the second read of x that a global amax forces (x exceeds on-chip storage)."""
+    return bytes_io(rows, cols) + 2 * rows * cols
+
+
+def encode_bytes(rows, cols):
+    """Algorithmic bytes of one encode-kernel launch: x once, codes+scales out, amax in."""
+    return bytes_io(rows, cols)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "of measured"
+    return 6800.0, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(sample_rows: int, seed: int = 2):
+    """Time the oracle on the first `sample_rows` rows of X and dY (drawn from the
+    same distribution on the CPU), both directions, row-scaled."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads
+    g = workloads.generator(seed, "cpu")
+    xs = [workloads.row_lognormal(sample_rows, k, g, "cpu") for k in (K_X, K_DY)]
+    bits = [x.view(torch.int16).numpy().view(np.uint16) for x in xs]
+    t0 = time.perf_counter()
+    for b in bits:
+        oracle.quantize(b, "bf16", mode=oracle.ROW_SCALED, bound=448.0)
+    dt = time.perf_counter() - t0
+    nbytes = sum(bytes_io(sample_rows, k) for k in (K_X, K_DY))
+    return nbytes / dt / 1e9, dt, f"first {sample_rows} rows of X and dY, both directions"
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    sample_rows = args.oracle_rows or 128
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(sample_rows)
+    t_all = []
+    for _ in range(args.steps):
+        v, dt, what = oracle_sample(sample_rows)
+        vals.append(v)
+        t_all.append(dt)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(t_all), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": what},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": what},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args):
+    import torch
+
+    import nvfp4_precision_quantization_gb300 as nv
+    import workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    nv.load_library()
+
+    x, dy = workloads.linear(dev, rows=args.rows)
+    ops = [x, dy]
+    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+    outs = []
+    for t in ops:
+        r, c = t.shape
+        row = nv.alloc_out(r, c, r, dev)
+        col = nv.alloc_out(c, r, c, dev)
+        row.amax_in, col.amax_in = row.amax, col.amax
+        outs.append((row, col))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > 129 MB L2
+
+    def step(ev=None):
+        for i, (t, (row, col)) in enumerate(zip(ops, outs)):
+            nv.nvfp4_amax(t, row.amax, col.amax, None, stream=stream)
+            if ev is not None:
+                ev[2 * i].record(stream)
+            nv.nvfp4_quantize_both(t, cfg, row, col, stream=stream)
+            if ev is not None:
+                ev[2 * i + 1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mid = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    for k in range(K):
+        flush.zero_()
+        starts[k].record(stream)
+        step(mid[k])
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    t_total = sum(step_ms) / 1e3
+    t_total = max_over_ranks(t_total, world, dev)
+    ms_per_step = 1e3 * t_total / K
+    # encode-kernel durations (between the event after amax and after quantize)
+    enc_x = [mid[k][0].elapsed_time(mid[k][1]) for k in range(K)]
+    enc_dy = [(mid[k][2].elapsed_time(mid[k][3])) for k in range(K)]
+    amax_x = [starts[k].elapsed_time(mid[k][0]) for k in range(K)]
+    amax_dy = [mid[k][1].elapsed_time(mid[k][2]) for k in range(K)]
+
+    shapes = [t.shape for t in ops]
+    bio = sum(bytes_io(r, c) for r, c in shapes)
+    bmin = sum(bytes_min(r, c) for r, c in shapes)
+    elems = sum(r * c for r, c in shapes)
+    value = world * bio * K / t_total / 1e9
+    peak, peak_src = measured_peaks()
+    enc_bytes = sum(encode_bytes(r, c) for r, c in shapes) / 2  # per launch (mean of the two)
+    enc_dur = (statistics.mean(enc_x) + statistics.mean(enc_dy)) / 2 / 1e3
+    achieved = enc_bytes / enc_dur / 1e9
+
+    e2e = None if args.no_e2e else measure_e2e(nv, ops, outs, cfg, stream, dev, max(2, min(K, 5)))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, what = oracle_sample(args.oracle_rows or 768)
+        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": what,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "pct_of_hbm_peak": 100.0 * value / world / peak,
+            "config": {
+                "workload": WORKLOAD,
+                "l2": "inputs larger than L2 (268 MB, 940 MB) and a 256 MB L2 flush before each step",
+                "bytes_io_per_step": bio, "bytes_min_per_step": bmin,
+                "elements_per_step": elems,
+                "gbps_bytes_min": world * bmin * K / t_total / 1e9,
+                "pct_of_hbm_peak_bytes_min": 100.0 * bmin * K / t_total / 1e9 / peak,
+                "elements_per_s": world * elems * K / t_total,
+                "peak_gbs": peak, "peak_source": peak_src,
+                "ms_amax_x": statistics.mean(amax_x), "ms_encode_x": statistics.mean(enc_x),
+                "ms_amax_dy": statistics.mean(amax_dy), "ms_encode_dy": statistics.mean(enc_dy),
+            },
+            "roofline": {"kernel": "k_quantize (encode pass)", "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 6 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(nv, ops, outs, cfg, stream, dev, steps):
+    """Same metric through the C ABI with host buffers: pinned H2D of X and dY,
+    the quantize, D2H of codes, scales and amax, all inside the timed region."""
+    import torch
+    host_in = [t.cpu().pin_memory() for t in ops]
+    host_out = []
+    for row, col in outs:
+        host_out.append([torch.empty_like(a, device="cpu").pin_memory()
+                         for a in (row.codes, row.scales, row.amax, col.codes, col.scales,
+                                   col.amax)])
+    dev_in = [torch.empty_like(t) for t in ops]
+    e2e_outs = []
+    for t in ops:
+        r, c = t.shape
+        e2e_outs.append((nv.alloc_out(r, c, r, dev), nv.alloc_out(c, r, c, dev)))
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(a.numel() * a.element_size() for lst in host_out for a in lst)
+    times = []
+    for _ in range(steps + 1):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for hi, di, (row, col), ho in zip(host_in, dev_in, e2e_outs, host_out):
+            di.copy_(hi, non_blocking=True)
+            nv.nvfp4_quantize_both(di, cfg, row, col, stream=stream)
+            for dst, src in zip(ho, (row.codes, row.scales, row.amax, col.codes, col.scales,
+                                     col.amax)):
+                dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times[1:])
+    bio = sum(bytes_io(*t_.shape) for t_ in ops)
+    return {"value": bio / t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * t}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--oracle-rows", type=int, default=None,
+                    help="rows of X and dY in the oracle sample (default 768 for the CPU "
+                         "baseline, 128 per step for --impl reference)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rows", type=int, default=ROWS,
+                    help="rows of X and dY (default 16384; smaller only for profiling captures)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4: NVFP4 quantize / dequantize on one GB300 GPU.
+ *
+ * What the library computes (web pages; titles and sections):
+ *   [TE-3206] TransformerEngine PR #3206 "NVFP4: enable row-scaled transpose
+ *             quantization for backward": a row-scaled NVFP4 quantize that emits
+ *             both the rowwise (fprop) and the columnwise / transposed (wgrad)
+ *             output in one pass, after a per-row and per-column amax pre-pass
+ *             (sequence diagram; description).
+ *   [TE-3454] TransformerEngine PR #3454 "row-scaled nvfp4 path: fuse row/col
+ *             amax into a single TMA-tiled kernel": one kernel for the row and
+ *             column amax, byte-identical to two separate reductions; a noop flag
+ *             that must leave the amax buffers untouched (description; flowchart;
+ *             review comment on compute_fused_amax).
+ *   [AO-9]    torchao PR #9 "Add NVFP4 four-over-six grouped GEMM for MoE
+ *             training": per-block four-over-six choice with bound 448 or 256;
+ *             grouped quantize whose per-group amax is expanded to a per-row
+ *             vector over contiguous token groups given by group-end offsets
+ *             (description).
+ *   [AO-8]    torchao PR #8 "Add backward overrides and 1x16 weights to NVFP4
+ *             four-over-six": dequantize = code * ((scale * amax) * factor_inv)
+ *             with a correctly rounded FP32 reciprocal; 1x16 or 16x16 weight
+ *             blocks; BF16 or FP32 output (description).
+ *
+ * Encode recipe (the pages fix the formats and the dequantize formula but print
+ * no encode formula; this is the plain reading the library implements, FP32 with
+ * round-to-nearest-even, one operation at a time):
+ *   F  = bound * 6                          (6 = largest E2M1 magnitude)
+ *   S  = F / a (a = amax of the line or tensor; S = 1 if a == 0; FLT_MAX if F/a
+ *        overflows)
+ *   per 16-element block (or 16x16 tile) with max |x| = b, for T = 6 (and T = 4
+ *   when four-over-six is on):
+ *     s8 = E4M3_satfinite((b / T) * S)      block scale byte
+ *     e  = S / decode(s8)  (0 if decode(s8) == 0)
+ *     c  = E2M1_satfinite(x * e)            4-bit code, sign kept
+ *   four-over-six keeps T = 4 only if its squared error, summed in element order
+ *   after dequantizing with the formula above, is strictly smaller.
+ *
+ * Layouts (all row-major, compact):
+ *   x            [rows][cols] BF16 or FP32, row stride = cols elements.
+ *   rowwise      codes  [rows][ceil(cols/2)]  two codes per byte, low nibble = even column
+ *                scales [rows][ceil(cols/16)] one E4M3 byte per 1x16 block
+ *                amax   [rows] (row-scaled) or [1] (per-tensor)
+ *   columnwise   the rowwise layout of x^T: codes [cols][ceil(rows/2)],
+ *                scales [cols][ceil(rows/16)], amax [cols] or [1].
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers on the current CUDA device; the
+ *     caller allocates and owns every buffer.  The library allocates nothing,
+ *     never synchronizes and never reads device memory on the host, so a call
+ *     can be captured in a CUDA graph (after the first call on a device, which
+ *     loads the kernels).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) on the current device.
+ *   - noop: optional device float; if non-NULL and *noop == 1.0f at run time,
+ *     the call writes nothing at all (no amax, codes or scales).
+ *   - Return value: NVFP4_OK once the work is enqueued.  NVFP4_ERR_INVALID for
+ *     bad arguments (NULL required pointer, negative size, bound not 448/256,
+ *     16x16 blocks with row-scaled mode, unknown dtype); nothing is enqueued
+ *     then.  NVFP4_ERR_CUDA if a launch failed.  The reason is available from
+ *     nvfp4_last_error() (per host thread).
+ *   - Problems found on the device (invalid group ends, a wait that gave up)
+ *     set bits in the library's device status word, read with
+ *     nvfp4_device_status().
+ *   - rows == 0 or cols == 0 is valid: amax buffers of the non-empty extent are
+ *     written with 0 and no code or scale byte exists.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID = 1,
+    NVFP4_ERR_UNSUPPORTED = 2,
+    NVFP4_ERR_CUDA = 3,
+    NVFP4_ERR_TIMEOUT = 4
+} nvfp4_status;
+
+typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_FP32 = 1 } nvfp4_in_dtype;
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_out_dtype;
+
+/* PER_TENSOR: one amax for the whole tensor (both directions use it).
+ * ROW_SCALED: rowwise output uses the per-row amax, columnwise output uses the
+ * per-column amax [TE-3206]. */
+typedef enum { NVFP4_PER_TENSOR = 0, NVFP4_ROW_SCALED = 1 } nvfp4_amax_mode;
+
+/* Device status bits (nvfp4_device_status). */
+#define NVFP4_DEVICE_TIMEOUT 1    /* a kernel gave up a bounded wait */
+#define NVFP4_DEVICE_BAD_GROUPS 2 /* group ends not non-decreasing / last != rows */
+
+typedef struct {
+    int32_t mode;          /* nvfp4_amax_mode */
+    float bound;           /* E4M3 bound of the global scale: 448 or 256 [AO-9] */
+    int32_t four_over_six; /* 0: T = 6 only; 1: per-block choice of T = 4 or 6 by MSE */
+    int32_t block_2d;      /* 0: 1x16 blocks; 1: 16x16 blocks (PER_TENSOR only) [AO-8] */
+} nvfp4_config;
+
+/* One output direction. */
+typedef struct {
+    uint8_t *codes;        /* [lines][ceil(n/2)] */
+    uint8_t *scales;       /* [lines][ceil(n/16)] */
+    float *amax;           /* [lines] or [1]: receives the amax the codes were made with */
+    const float *amax_in;  /* NULL: compute amax from x; else [lines] or [1] to use (may equal amax) */
+} nvfp4_out;
+
+/*
+ * nvfp4_amax -- exact amax of x, rows and columns in one pass over x [TE-3454].
+ *   row_amax [rows], col_amax [cols], tensor_amax [1]: each may be NULL (at least
+ *   one must be given).  Values are max |x| (an empty line gives 0); the result
+ *   does not depend on the order of reduction.
+ */
+NVFP4_API nvfp4_status nvfp4_amax(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
+                        float *row_amax, float *col_amax, float *tensor_amax,
+                        const float *noop, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_quantize_rowwise / _columnwise / _both -- NVFP4 quantize of x [TE-3206].
+ *   cfg: see nvfp4_config.  row / col: the output direction(s); amax length is
+ *   rows / cols for ROW_SCALED and 1 for PER_TENSOR.  The _both variant reads x
+ *   for the amax pass and once more for the encode pass (a global amax must be
+ *   known before the first code), in one stream-ordered sequence of kernels.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_rowwise(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                    const nvfp4_config *cfg, const nvfp4_out *row,
+                                    const float *noop, nvfp4_stream_t stream);
+NVFP4_API nvfp4_status nvfp4_quantize_columnwise(const void *x, int32_t in_dtype, int64_t rows,
+                                       int64_t cols, const nvfp4_config *cfg,
+                                       const nvfp4_out *col, const float *noop,
+                                       nvfp4_stream_t stream);
+NVFP4_API nvfp4_status nvfp4_quantize_both(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                 const nvfp4_config *cfg, const nvfp4_out *row,
+                                 const nvfp4_out *col, const float *noop, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_dequantize -- value = code * ((decode(scale) * amax) * fl(1/(bound*6)))
+ * [AO-8], written as FP32 or rounded to nearest-even BF16.
+ *   codes [rows][ceil(cols/2)], scales [rows][ceil(cols/16)], amax [rows]
+ *   (ROW_SCALED) or [1] (PER_TENSOR); out [rows][cols].  For a columnwise output
+ *   pass rows = original cols, cols = original rows.
+ */
+NVFP4_API nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *amax,
+                              int32_t mode, int64_t rows, int64_t cols, float bound, void *out,
+                              int32_t out_dtype, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_grouped_amax -- per-group amax over contiguous row groups [AO-9].
+ *   group_ends: device int64 [num_groups], cumulative row ends, non-decreasing,
+ *   last == rows (an empty group is allowed and gets amax 0).
+ *   group_amax [num_groups] (required); row_amax_expanded [rows] (optional)
+ *   receives each row's group amax.  Invalid ends set NVFP4_DEVICE_BAD_GROUPS and
+ *   nothing is written.  num_groups <= 4096.
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_amax(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                const int64_t *group_ends, int32_t num_groups, float *group_amax,
+                                float *row_amax_expanded, const float *noop,
+                                nvfp4_stream_t stream);
+
+/*
+ * nvfp4_grouped_quantize_rowwise -- rowwise quantize of grouped tokens [AO-9].
+ *   cfg->mode PER_TENSOR: each group uses its own amax (the group amax expanded
+ *   to every row), bit-identical to quantizing each group separately;
+ *   cfg->mode ROW_SCALED: per-row amax (groups do not change the result).
+ *   row->amax [rows] receives the per-row amax used; row->amax_in must be NULL.
+ *   group_amax [num_groups] (optional with ROW_SCALED, required otherwise).
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_quantize_rowwise(const void *x, int32_t in_dtype, int64_t rows,
+                                            int64_t cols, const int64_t *group_ends,
+                                            int32_t num_groups, const nvfp4_config *cfg,
+                                            const nvfp4_out *row, float *group_amax,
+                                            const float *noop, nvfp4_stream_t stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+NVFP4_API const char *nvfp4_last_error(void);
+
+/*
+ * nvfp4_device_status -- read (and if reset != 0, clear) the device status word
+ * of the current device.  Synchronizes the device; not for use inside graph
+ * capture.  *status receives NVFP4_DEVICE_* bits (0 = nothing happened).
+ */
+NVFP4_API nvfp4_status nvfp4_device_status(int32_t *status, int32_t reset);
+
+/*
+ * nvfp4_selftest_convert -- diagnostic: run the device conversions used by the
+ * kernels over n FP32 inputs: e2m1_out[i] = E2M1 code of in[i] (one code per
+ * byte) and e4m3_out[i] = E4M3 byte of in[i] (either output may be NULL).  Lets
+ * a test compare the hardware conversions with the oracle on every bit pattern.
+ */
+NVFP4_API nvfp4_status nvfp4_selftest_convert(const float *in, int64_t n, uint8_t *e2m1_out,
+                                    uint8_t *e4m3_out, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

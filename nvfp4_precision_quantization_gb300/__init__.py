@@ -1,0 +1,247 @@
+"""NVFP4 quantize / dequantize on GB300 (sm_103a) -- Python binding of libnvfp4.
+
+Thin ctypes layer over the C ABI declared in ``include/nvfp4.h``: the functions
+keep the C names and only marshal arguments (torch tensors -> device pointers,
+the current torch stream -> cudaStream_t).  Every step of the computation runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
+importing a function without the compiled library raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import platform
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "NVFP4_OK", "NVFP4_IN_BF16", "NVFP4_IN_FP32", "NVFP4_OUT_BF16", "NVFP4_OUT_FP32",
+    "NVFP4_PER_TENSOR", "NVFP4_ROW_SCALED", "NVFP4_DEVICE_TIMEOUT", "NVFP4_DEVICE_BAD_GROUPS",
+    "Config", "Out", "NVFP4Error", "load_library", "library_path",
+    "nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise", "nvfp4_quantize_both",
+    "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
+    "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
+    "alloc_out", "EXPORTED_SYMBOLS",
+]
+
+NVFP4_OK = 0
+NVFP4_ERR_INVALID = 1
+NVFP4_ERR_UNSUPPORTED = 2
+NVFP4_ERR_CUDA = 3
+NVFP4_ERR_TIMEOUT = 4
+NVFP4_IN_BF16 = 0
+NVFP4_IN_FP32 = 1
+NVFP4_OUT_BF16 = 0
+NVFP4_OUT_FP32 = 1
+NVFP4_PER_TENSOR = 0
+NVFP4_ROW_SCALED = 1
+NVFP4_DEVICE_TIMEOUT = 1
+NVFP4_DEVICE_BAD_GROUPS = 2
+
+EXPORTED_SYMBOLS = (
+    "nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise", "nvfp4_quantize_both",
+    "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
+    "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"nvfp4 status {status}: {message}")
+        self.status = status
+
+
+class Config(C.Structure):
+    """nvfp4_config: mode (PER_TENSOR / ROW_SCALED), bound (448 or 256),
+    four_over_six (0/1), block_2d (0: 1x16, 1: 16x16)."""
+    _fields_ = [("mode", C.c_int32), ("bound", C.c_float), ("four_over_six", C.c_int32),
+                ("block_2d", C.c_int32)]
+
+
+class _COut(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("amax", C.c_void_p),
+                ("amax_in", C.c_void_p)]
+
+
+@dataclass
+class Out:
+    """One output direction: codes [lines][ceil(n/2)] uint8, scales
+    [lines][ceil(n/16)] uint8, amax [lines] or [1] float32, optional amax_in."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    amax: torch.Tensor
+    amax_in: Optional[torch.Tensor] = None
+
+    def _c(self) -> _COut:
+        return _COut(_ptr(self.codes), _ptr(self.scales), _ptr(self.amax), _ptr(self.amax_in))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, f"libnvfp4_{platform.machine()}.so")
+
+
+_lib = None
+
+
+def load_library():
+    """Load libnvfp4 (raises if it has not been built: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libnvfp4 is not built ({path} missing); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = C.CDLL(path)
+    vp, i32, i64, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_float
+    sig = {
+        "nvfp4_amax": [vp, i32, i64, i64, vp, vp, vp, vp, vp],
+        "nvfp4_quantize_rowwise": [vp, i32, i64, i64, vp, vp, vp, vp],
+        "nvfp4_quantize_columnwise": [vp, i32, i64, i64, vp, vp, vp, vp],
+        "nvfp4_quantize_both": [vp, i32, i64, i64, vp, vp, vp, vp, vp],
+        "nvfp4_dequantize": [vp, vp, vp, i32, i64, i64, f32, vp, i32, vp],
+        "nvfp4_grouped_amax": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp],
+        "nvfp4_grouped_quantize_rowwise": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp, vp],
+        "nvfp4_device_status": [C.POINTER(C.c_int32), i32],
+        "nvfp4_selftest_convert": [vp, i64, vp, vp, vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = C.c_int
+    L.nvfp4_last_error.argtypes = []
+    L.nvfp4_last_error.restype = C.c_char_p
+    _lib = L
+    return L
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != NVFP4_OK:
+        raise NVFP4Error(status, nvfp4_last_error())
+
+
+def _in_dtype(x: torch.Tensor) -> int:
+    if x.dtype == torch.bfloat16:
+        return NVFP4_IN_BF16
+    if x.dtype == torch.float32:
+        return NVFP4_IN_FP32
+    raise TypeError(f"x must be bfloat16 or float32, got {x.dtype}")
+
+
+def _matrix(x: torch.Tensor):
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    return x.shape[0], x.shape[1]
+
+
+def nvfp4_last_error() -> str:
+    return load_library().nvfp4_last_error().decode()
+
+
+def nvfp4_amax(x: torch.Tensor, row_amax=None, col_amax=None, tensor_amax=None, noop=None,
+               stream=None) -> None:
+    rows, cols = _matrix(x)
+    _check(load_library().nvfp4_amax(_ptr(x), _in_dtype(x), rows, cols, _ptr(row_amax),
+                                     _ptr(col_amax), _ptr(tensor_amax), _ptr(noop),
+                                     _stream(stream)))
+
+
+def nvfp4_quantize_rowwise(x: torch.Tensor, cfg: Config, row: Out, noop=None, stream=None):
+    rows, cols = _matrix(x)
+    r = row._c()
+    _check(load_library().nvfp4_quantize_rowwise(_ptr(x), _in_dtype(x), rows, cols,
+                                                 C.byref(cfg), C.byref(r), _ptr(noop),
+                                                 _stream(stream)))
+
+
+def nvfp4_quantize_columnwise(x: torch.Tensor, cfg: Config, col: Out, noop=None, stream=None):
+    rows, cols = _matrix(x)
+    c = col._c()
+    _check(load_library().nvfp4_quantize_columnwise(_ptr(x), _in_dtype(x), rows, cols,
+                                                    C.byref(cfg), C.byref(c), _ptr(noop),
+                                                    _stream(stream)))
+
+
+def nvfp4_quantize_both(x: torch.Tensor, cfg: Config, row: Out, col: Out, noop=None,
+                        stream=None):
+    rows, cols = _matrix(x)
+    r, c = row._c(), col._c()
+    _check(load_library().nvfp4_quantize_both(_ptr(x), _in_dtype(x), rows, cols, C.byref(cfg),
+                                              C.byref(r), C.byref(c), _ptr(noop),
+                                              _stream(stream)))
+
+
+def nvfp4_dequantize(codes, scales, amax, mode: int, rows: int, cols: int, bound: float,
+                     out: torch.Tensor, stream=None) -> None:
+    if out.dtype == torch.bfloat16:
+        od = NVFP4_OUT_BF16
+    elif out.dtype == torch.float32:
+        od = NVFP4_OUT_FP32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    _check(load_library().nvfp4_dequantize(_ptr(codes), _ptr(scales), _ptr(amax), mode, rows,
+                                           cols, bound, _ptr(out), od, _stream(stream)))
+
+
+def nvfp4_grouped_amax(x: torch.Tensor, group_ends: torch.Tensor, group_amax: torch.Tensor,
+                       row_amax_expanded=None, noop=None, stream=None) -> None:
+    rows, cols = _matrix(x)
+    _check(load_library().nvfp4_grouped_amax(_ptr(x), _in_dtype(x), rows, cols,
+                                             _ptr(group_ends), int(group_ends.numel()),
+                                             _ptr(group_amax), _ptr(row_amax_expanded),
+                                             _ptr(noop), _stream(stream)))
+
+
+def nvfp4_grouped_quantize_rowwise(x: torch.Tensor, group_ends: torch.Tensor, cfg: Config,
+                                   row: Out, group_amax=None, noop=None, stream=None) -> None:
+    rows, cols = _matrix(x)
+    r = row._c()
+    _check(load_library().nvfp4_grouped_quantize_rowwise(
+        _ptr(x), _in_dtype(x), rows, cols, _ptr(group_ends), int(group_ends.numel()),
+        C.byref(cfg), C.byref(r), _ptr(group_amax), _ptr(noop), _stream(stream)))
+
+
+def nvfp4_device_status(reset: bool = False) -> int:
+    v = C.c_int32(0)
+    _check(load_library().nvfp4_device_status(C.byref(v), int(reset)))
+    return v.value
+
+
+def nvfp4_selftest_convert(x: torch.Tensor, e2m1_out=None, e4m3_out=None, stream=None) -> None:
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise TypeError("x must be contiguous float32")
+    _check(load_library().nvfp4_selftest_convert(_ptr(x), x.numel(), _ptr(e2m1_out),
+                                                 _ptr(e4m3_out), _stream(stream)))
+
+
+def alloc_out(lines: int, n: int, amax_len: int, device="cuda", fill=None) -> Out:
+    """Allocate one output direction with torch (codes, scales, amax)."""
+    codes = torch.empty(lines, (n + 1) // 2, dtype=torch.uint8, device=device)
+    scales = torch.empty(lines, (n + 15) // 16, dtype=torch.uint8, device=device)
+    amax = torch.empty(amax_len, dtype=torch.float32, device=device)
+    if fill is not None:
+        codes.fill_(fill)
+        scales.fill_(fill)
+    return Out(codes, scales, amax)

@@ -1,0 +1,476 @@
+// api.cu -- the C ABI of libnvfp4 (declared in include/nvfp4.h).
+//
+// Host side only: argument validation with a per-thread message (in the style of
+// the checks quoted in "NVFP4: enable row-scaled transpose quantization for
+// backward", TransformerEngine PR #3206, review of the grouped GEMM draft, and
+// "row-scaled nvfp4 path: fuse row/col amax into a single TMA-tiled kernel",
+// PR #3454, review of compute_fused_amax), the per-device cache (SM count and the
+// status word, for the *current* device -- the draft reviewed in PR #3206
+// hard-coded device 0), and the stream-ordered launch sequences.  Nothing here
+// allocates device memory, synchronizes, or reads device data, except
+// nvfp4_device_status, which exists to do exactly that.
+//
+// Unlike the wrapper reviewed in PR #3454, amax buffers are never cleared by a
+// host-side memset: clearing happens in a kernel that first checks the noop
+// flag, so a skipped call leaves existing amax metadata untouched.
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/nvfp4.h"
+#include "internal.h"
+
+namespace nvfp4 {
+
+// The library's one piece of device state: sticky error bits that kernels set
+// when they find invalid device-resident input or give up a bounded wait.
+__device__ int g_status_word;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+nvfp4_status fail(nvfp4_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+nvfp4_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(NVFP4_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DevCacheEntry {
+  bool ready = false;
+  int num_sms = 0;
+  int* status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DevCacheEntry g_dev[kMaxDevices];
+
+nvfp4_status current_device(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_UNSUPPORTED, "device index too large");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevCacheEntry& c = g_dev[dev];
+  if (!c.ready) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    c.num_sms = sms;
+    c.status = static_cast<int*>(p);
+    c.ready = true;
+  }
+  out->device = dev;
+  out->num_sms = c.num_sms;
+  out->status = c.status;
+  return NVFP4_OK;
+}
+
+bool valid_in_dtype(int32_t d) { return d == NVFP4_IN_BF16 || d == NVFP4_IN_FP32; }
+
+nvfp4_status check_sizes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return fail(NVFP4_ERR_INVALID, "rows and cols must be >= 0");
+  if (rows >= (1LL << 31) || cols >= (1LL << 31))
+    return fail(NVFP4_ERR_INVALID, "rows and cols must be < 2^31");
+  return NVFP4_OK;
+}
+
+nvfp4_status check_config(const nvfp4_config* cfg) {
+  if (cfg == nullptr) return fail(NVFP4_ERR_INVALID, "cfg is NULL");
+  if (cfg->mode != NVFP4_PER_TENSOR && cfg->mode != NVFP4_ROW_SCALED)
+    return fail(NVFP4_ERR_INVALID, "cfg->mode must be NVFP4_PER_TENSOR or NVFP4_ROW_SCALED");
+  if (!(cfg->bound == 448.0f || cfg->bound == 256.0f))
+    return fail(NVFP4_ERR_INVALID, "cfg->bound must be 448 or 256");
+  if (cfg->four_over_six != 0 && cfg->four_over_six != 1)
+    return fail(NVFP4_ERR_INVALID, "cfg->four_over_six must be 0 or 1");
+  if (cfg->block_2d != 0 && cfg->block_2d != 1)
+    return fail(NVFP4_ERR_INVALID, "cfg->block_2d must be 0 or 1");
+  if (cfg->block_2d && cfg->mode == NVFP4_ROW_SCALED)
+    return fail(NVFP4_ERR_INVALID, "16x16 blocks are per-tensor only");
+  return NVFP4_OK;
+}
+
+nvfp4_status check_out(const nvfp4_out* o, const char* name, int64_t lines, int64_t n,
+                       int64_t amax_len) {
+  if (o == nullptr) return fail(NVFP4_ERR_INVALID, std::string(name) + " is NULL");
+  if (o->amax == nullptr && amax_len > 0)
+    return fail(NVFP4_ERR_INVALID, std::string(name) + "->amax is NULL");
+  if (lines * n > 0 && (o->codes == nullptr || o->scales == nullptr))
+    return fail(NVFP4_ERR_INVALID, std::string(name) + "->codes / ->scales is NULL");
+  return NVFP4_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// One sequence of launches for any quantize direction set (row and/or col may be NULL).
+nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                           const nvfp4_config* cfg, const nvfp4_out* row, const nvfp4_out* col,
+                           const float* noop, cudaStream_t stream,
+                           const int64_t* group_ends = nullptr, int num_groups = 0) {
+  nvfp4_status st;
+  if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
+  if ((st = check_sizes(rows, cols)) != NVFP4_OK) return st;
+  if ((st = check_config(cfg)) != NVFP4_OK) return st;
+  const bool rs_mode = cfg->mode == NVFP4_ROW_SCALED;
+  if (row && (st = check_out(row, "row", rows, cols, rs_mode ? rows : 1)) != NVFP4_OK) return st;
+  if (col && (st = check_out(col, "col", cols, rows, rs_mode ? cols : 1)) != NVFP4_OK) return st;
+  if (x == nullptr && rows * cols > 0) return fail(NVFP4_ERR_INVALID, "x is NULL");
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+
+  const bool rs = cfg->mode == NVFP4_ROW_SCALED;
+  const bool need_r = row && row->amax_in == nullptr;
+  const bool need_c = col && col->amax_in == nullptr;
+  const InType in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+
+  PrepArgs prep{};
+  AmaxArgs am{};
+  am.x = x;
+  am.in = in;
+  am.M = rows;
+  am.K = cols;
+  am.noop = noop;
+  am.group_ends = group_ends;
+  am.num_groups = num_groups;
+  QuantArgs q{};
+  q.x = x;
+  q.in = in;
+  q.M = rows;
+  q.K = cols;
+  q.row_scaled = rs;
+  q.four_over_six = cfg->four_over_six != 0;
+  q.block_2d = cfg->block_2d != 0;
+  q.bound = cfg->bound;
+  q.noop = noop;
+  q.group_ends = group_ends;
+  q.num_groups = num_groups;
+  if (row) {
+    q.row_codes = row->codes;
+    q.row_scales = row->scales;
+    q.row_amax = row->amax;
+  }
+  if (col) {
+    q.col_codes = col->codes;
+    q.col_scales = col->scales;
+    q.col_amax = col->amax;
+  }
+  int nz = 0, nc = 0;
+  auto add_zero = [&](float* p, int64_t n) {
+    prep.zero_ptr[nz] = p;
+    prep.zero_n[nz++] = n;
+  };
+  auto add_copy = [&](float* d, const float* s, int64_t n) {
+    if (d == s) return;
+    prep.copy_dst[nc] = d;
+    prep.copy_src[nc] = s;
+    prep.copy_n[nc++] = n;
+  };
+  if (rs) {
+    if (need_r) {
+      add_zero(row->amax, rows);
+      am.row_amax = row->amax;
+    } else if (row) {
+      add_copy(row->amax, row->amax_in, rows);
+    }
+    if (need_c) {
+      add_zero(col->amax, cols);
+      am.col_amax = col->amax;
+    } else if (col) {
+      add_copy(col->amax, col->amax_in, cols);
+    }
+  } else {
+    float* target = need_r ? row->amax : (need_c ? col->amax : nullptr);
+    if (target) {
+      add_zero(target, 1);
+      am.tensor_amax = target;
+    }
+    if (row && !need_r) add_copy(row->amax, row->amax_in, 1);
+    if (col && !need_c) add_copy(col->amax, col->amax_in, 1);
+    if (need_r && need_c) {
+      // both directions use the one tensor amax computed into row->amax; the
+      // quantize kernel copies it to col->amax (zeroed here for empty inputs)
+      add_zero(col->amax, 1);
+      q.col_amax = row->amax;
+      q.copy_dst = col->amax;
+      q.copy_src = row->amax;
+    }
+  }
+  cudaError_t e;
+  prep.noop = noop;
+  if (nz + nc > 0) {
+    if (group_ends) {
+      // grouped calls: the prep step must also refuse invalid group ends
+      GroupCheckArgs g{};
+      g.M = rows;
+      g.group_ends = group_ends;
+      g.num_groups = num_groups;
+      g.noop = noop;
+      g.prep = prep;
+      if ((e = launch_group_check(g, dev, stream, false)) != cudaSuccess)
+        return cuda_fail(e, "group check launch");
+    } else if ((e = launch_prep(prep, dev, stream)) != cudaSuccess) {
+      return cuda_fail(e, "prep launch");
+    }
+  }
+  if (am.row_amax || am.col_amax || am.tensor_amax) {
+    if ((e = launch_amax(am, dev, stream)) != cudaSuccess) return cuda_fail(e, "amax launch");
+  }
+  if (q.block_2d && row && col && q.row_amax != q.col_amax) {
+    // 16x16 tiles share one scale per tile; with two different per-tensor amax
+    // sources the directions are encoded by two launches
+    QuantArgs qr = q, qc = q;
+    qr.col_codes = nullptr;
+    qc.row_codes = nullptr;
+    qc.copy_dst = nullptr;
+    if ((e = launch_quantize(qr, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize");
+    if ((e = launch_quantize(qc, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize");
+  } else if ((e = launch_quantize(q, dev, stream)) != cudaSuccess) {
+    return cuda_fail(e, "quantize launch");
+  }
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+bool make_tile_map(CUtensorMap* map, const void* base, InType in, int64_t rows, int64_t cols,
+                   int box_cols, int box_rows) {
+  const int elem = in == InType::BF16 ? 2 : 4;
+  if (rows <= 0 || cols <= 0) return false;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return false;
+  if ((cols * elem) % 16 != 0) return false;
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(cols * elem)};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r =
+      fn(map, in == InType::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+         2, const_cast<void*>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                        float* row_amax, float* col_amax, float* tensor_amax, const float* noop,
+                        nvfp4_stream_t stream) {
+  nvfp4_status st;
+  if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
+  if ((st = check_sizes(rows, cols)) != NVFP4_OK) return st;
+  if (!row_amax && !col_amax && !tensor_amax)
+    return fail(NVFP4_ERR_INVALID, "no amax output given");
+  if (x == nullptr && rows * cols > 0) return fail(NVFP4_ERR_INVALID, "x is NULL");
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+  PrepArgs prep{};
+  int nz = 0;
+  if (row_amax) { prep.zero_ptr[nz] = row_amax; prep.zero_n[nz++] = rows; }
+  if (col_amax) { prep.zero_ptr[nz] = col_amax; prep.zero_n[nz++] = cols; }
+  if (tensor_amax) { prep.zero_ptr[nz] = tensor_amax; prep.zero_n[nz++] = 1; }
+  prep.noop = noop;
+  cudaError_t e = launch_prep(prep, dev, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+  AmaxArgs am{};
+  am.x = x;
+  am.in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+  am.M = rows;
+  am.K = cols;
+  am.row_amax = row_amax;
+  am.col_amax = col_amax;
+  am.tensor_amax = tensor_amax;
+  am.noop = noop;
+  if ((e = launch_amax(am, dev, stream)) != cudaSuccess) return cuda_fail(e, "amax launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize_rowwise(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                    const nvfp4_config* cfg, const nvfp4_out* row,
+                                    const float* noop, nvfp4_stream_t stream) {
+  if (row == nullptr) return fail(NVFP4_ERR_INVALID, "row is NULL");
+  return quantize_impl(x, in_dtype, rows, cols, cfg, row, nullptr, noop, stream);
+}
+
+nvfp4_status nvfp4_quantize_columnwise(const void* x, int32_t in_dtype, int64_t rows,
+                                       int64_t cols, const nvfp4_config* cfg,
+                                       const nvfp4_out* col, const float* noop,
+                                       nvfp4_stream_t stream) {
+  if (col == nullptr) return fail(NVFP4_ERR_INVALID, "col is NULL");
+  return quantize_impl(x, in_dtype, rows, cols, cfg, nullptr, col, noop, stream);
+}
+
+nvfp4_status nvfp4_quantize_both(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                 const nvfp4_config* cfg, const nvfp4_out* row,
+                                 const nvfp4_out* col, const float* noop, nvfp4_stream_t stream) {
+  if (row == nullptr || col == nullptr) return fail(NVFP4_ERR_INVALID, "row or col is NULL");
+  return quantize_impl(x, in_dtype, rows, cols, cfg, row, col, noop, stream);
+}
+
+nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const float* amax,
+                              int32_t mode, int64_t rows, int64_t cols, float bound, void* out,
+                              int32_t out_dtype, nvfp4_stream_t stream) {
+  nvfp4_status st;
+  if ((st = check_sizes(rows, cols)) != NVFP4_OK) return st;
+  if (mode != NVFP4_PER_TENSOR && mode != NVFP4_ROW_SCALED)
+    return fail(NVFP4_ERR_INVALID, "mode must be NVFP4_PER_TENSOR or NVFP4_ROW_SCALED");
+  if (!(bound == 448.0f || bound == 256.0f)) return fail(NVFP4_ERR_INVALID, "bound must be 448 or 256");
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+    return fail(NVFP4_ERR_INVALID, "unknown out_dtype");
+  if (rows * cols > 0 && (!codes || !scales || !amax || !out))
+    return fail(NVFP4_ERR_INVALID, "codes, scales, amax and out must be non-NULL");
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+  DequantArgs d{};
+  d.codes = codes;
+  d.scales = scales;
+  d.amax = amax;
+  d.row_scaled = mode == NVFP4_ROW_SCALED;
+  d.rows = rows;
+  d.cols = cols;
+  d.bound = bound;
+  d.out = out;
+  d.out_bf16 = out_dtype == NVFP4_OUT_BF16;
+  cudaError_t e = launch_dequantize(d, dev, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_grouped_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                const int64_t* group_ends, int32_t num_groups, float* group_amax,
+                                float* row_amax_expanded, const float* noop,
+                                nvfp4_stream_t stream) {
+  nvfp4_status st;
+  if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
+  if ((st = check_sizes(rows, cols)) != NVFP4_OK) return st;
+  if (num_groups < 1 || num_groups > 4096)
+    return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
+  if (group_ends == nullptr || group_amax == nullptr)
+    return fail(NVFP4_ERR_INVALID, "group_ends and group_amax must be non-NULL");
+  if (x == nullptr && rows * cols > 0) return fail(NVFP4_ERR_INVALID, "x is NULL");
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+  GroupCheckArgs g{};
+  g.M = rows;
+  g.group_ends = group_ends;
+  g.num_groups = num_groups;
+  g.noop = noop;
+  g.prep.zero_ptr[0] = group_amax;
+  g.prep.zero_n[0] = num_groups;
+  g.prep.noop = noop;
+  cudaError_t e = launch_group_check(g, dev, stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "group check launch");
+  GroupedAmaxArgs a{};
+  a.x = x;
+  a.in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+  a.M = rows;
+  a.K = cols;
+  a.group_ends = group_ends;
+  a.num_groups = num_groups;
+  a.group_amax = group_amax;
+  a.noop = noop;
+  if ((e = launch_grouped_amax(a, dev, stream)) != cudaSuccess)
+    return cuda_fail(e, "grouped amax launch");
+  if (row_amax_expanded) {
+    g.prep = PrepArgs{};
+    g.group_amax = group_amax;
+    g.expand = row_amax_expanded;
+    if ((e = launch_group_check(g, dev, stream, true)) != cudaSuccess)
+      return cuda_fail(e, "group expand launch");
+  }
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_grouped_quantize_rowwise(const void* x, int32_t in_dtype, int64_t rows,
+                                            int64_t cols, const int64_t* group_ends,
+                                            int32_t num_groups, const nvfp4_config* cfg,
+                                            const nvfp4_out* row, float* group_amax,
+                                            const float* noop, nvfp4_stream_t stream) {
+  nvfp4_status st;
+  if ((st = check_config(cfg)) != NVFP4_OK) return st;
+  if (cfg->block_2d) return fail(NVFP4_ERR_INVALID, "grouped quantize uses 1x16 blocks");
+  if (row == nullptr) return fail(NVFP4_ERR_INVALID, "row is NULL");
+  if (row->amax_in != nullptr)
+    return fail(NVFP4_ERR_INVALID, "grouped quantize computes its amax: row->amax_in must be NULL");
+  if (num_groups < 1 || num_groups > 4096)
+    return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
+  if (group_ends == nullptr) return fail(NVFP4_ERR_INVALID, "group_ends is NULL");
+  if (cfg->mode == NVFP4_PER_TENSOR && group_amax == nullptr)
+    return fail(NVFP4_ERR_INVALID, "group_amax is required with NVFP4_PER_TENSOR");
+  nvfp4_config rcfg = *cfg;
+  rcfg.mode = NVFP4_ROW_SCALED;
+  if (cfg->mode == NVFP4_ROW_SCALED) {
+    if (group_amax) {
+      st = nvfp4_grouped_amax(x, in_dtype, rows, cols, group_ends, num_groups, group_amax,
+                              nullptr, noop, stream);
+      if (st != NVFP4_OK) return st;
+    }
+    return quantize_impl(x, in_dtype, rows, cols, &rcfg, row, nullptr, noop, stream, group_ends,
+                         num_groups);
+  }
+  st = nvfp4_grouped_amax(x, in_dtype, rows, cols, group_ends, num_groups, group_amax, row->amax,
+                          noop, stream);
+  if (st != NVFP4_OK) return st;
+  nvfp4_out r = *row;
+  r.amax_in = row->amax;  // the expanded per-row amax is already in place
+  return quantize_impl(x, in_dtype, rows, cols, &rcfg, &r, nullptr, noop, stream, group_ends,
+                       num_groups);
+}
+
+const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
+
+nvfp4_status nvfp4_device_status(int32_t* status, int32_t reset) {
+  if (status == nullptr) return fail(NVFP4_ERR_INVALID, "status is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int v = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int))) != cudaSuccess)
+    return cuda_fail(e, "read status word");
+  *status = v;
+  if (reset) {
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int))) != cudaSuccess)
+      return cuda_fail(e, "reset status word");
+  }
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_selftest_convert(const float* in, int64_t n, uint8_t* e2m1_out,
+                                    uint8_t* e4m3_out, nvfp4_stream_t stream) {
+  if (n < 0) return fail(NVFP4_ERR_INVALID, "n must be >= 0");
+  if (n > 0 && (in == nullptr || (e2m1_out == nullptr && e4m3_out == nullptr)))
+    return fail(NVFP4_ERR_INVALID, "in and one output must be non-NULL");
+  cudaError_t e = launch_selftest_convert(in, n, e2m1_out, e4m3_out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  return NVFP4_OK;
+}
+
+}  // extern "C"

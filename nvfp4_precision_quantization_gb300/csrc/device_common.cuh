@@ -1,0 +1,331 @@
+// device_common.cuh -- device helpers shared by the NVFP4 kernels (sm_103a).
+//
+// Number formats and the encode recipe follow the pages listed in
+// include/nvfp4.h: E2M1 codes and E4M3 block scales ("NVFP4: enable row-scaled
+// transpose quantization for backward", TransformerEngine PR #3206), the
+// four-over-six choice with bound 448/256 ("Add NVFP4 four-over-six grouped GEMM
+// for MoE training", torchao PR #9) and the dequantize formula ("Add backward
+// overrides and 1x16 weights to NVFP4 four-over-six", torchao PR #8).
+//
+// Every floating-point step of the recipe is one explicitly rounded FP32
+// operation (__fmul_rn / __fdiv_rn / __fadd_rn / __fsub_rn) so that nothing is
+// contracted into an FMA; the conversions use the sm_100-family cvt
+// instructions (RNE, satfinite).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+constexpr int kStatusTimeout = 1;    // NVFP4_DEVICE_TIMEOUT
+constexpr int kStatusBadGroups = 2;  // NVFP4_DEVICE_BAD_GROUPS
+
+// ---------------------------------------------------------------- flags / status
+
+__device__ __forceinline__ bool noop_set(const float* noop) {
+  return noop != nullptr && *noop == 1.0f;
+}
+
+__device__ __forceinline__ void raise_status(int* status, int bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+// Group ends are valid when non-decreasing, within [0, M], and the last equals M.
+// Must be called by every thread of the block.
+__device__ __forceinline__ bool groups_valid(const int64_t* ends, int G, int64_t M) {
+  int bad = 0;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const int64_t e = ends[g];
+    const int64_t p = g ? ends[g - 1] : 0;
+    if (e < p || e > M || (g == G - 1 && e != M)) bad = 1;
+  }
+  return !__syncthreads_or(bad);
+}
+
+// ---------------------------------------------------------------- BF16 helpers
+
+// The two BF16 halves of a packed pair, widened exactly to FP32.
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Lane-wise max of |a|, |b| over packed BF16 pairs.  The sign bits of the
+// result are meaningless (xorsign); callers mask them off.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// max of the two magnitudes held in a packed pair, as FP32 (exact).
+__device__ __forceinline__ float bf16x2_hmax_f32(uint32_t v) {
+  uint32_t m = v & 0x7fff7fffu;
+  uint32_t lo = m << 16, hi = m & 0xffff0000u;
+  return __uint_as_float(lo > hi ? lo : hi);
+}
+
+// ---------------------------------------------------------------- conversions
+
+// Eight FP32 values -> eight E2M1 codes packed in 32 bits; value k lands in
+// nibble k (low nibble of byte 0 = value 0).  RNE, saturating at +-6, sign kept.
+// cvt...e2m1x2 puts its first source in the high nibble, so each pair is
+// passed high-then-low.
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4,
+                                           float v5, float v6, float v7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return r;
+}
+
+// FP16 bit pattern -> FP32 (exact).
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((uint16_t)(h & 0xffffu)));
+  return f;
+}
+
+// FP32 -> E4M3 byte (RNE, satfinite: anything beyond 448, inf included, gives 448).
+__device__ __forceinline__ uint32_t e4m3_byte(float s) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(s));
+  return r & 0xffu;
+}
+
+// E4M3 byte -> FP32 (exact; every E4M3 value is an FP16 value).
+__device__ __forceinline__ float e4m3_value(uint32_t s8) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)s8;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return f16_bits_to_f32(h2);
+}
+
+// Two E2M1 codes (one byte, low nibble first) -> their FP32 values (exact).
+__device__ __forceinline__ void e2m1x2_values(uint32_t byte, float& lo, float& hi) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)(byte & 0xffu);
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "h"(in));
+  lo = f16_bits_to_f32(h2);
+  hi = f16_bits_to_f32(h2 >> 16);
+}
+
+// ---------------------------------------------------------------- recipe steps
+
+// Global encode scale S = F / a (1 if a == 0, FLT_MAX if the quotient overflows).
+__device__ __forceinline__ float global_scale(float a, float F) {
+  if (a == 0.0f) return 1.0f;
+  float S = __fdiv_rn(F, a);
+  return S > 3.402823466e38f ? 3.402823466e38f : S;
+}
+
+// Block scale byte and encode factor for block max b and target T (6 or 4).
+struct BlockEnc {
+  uint32_t s8;  // E4M3 byte
+  float sd;     // its value
+  float e;      // S / sd, or 0
+};
+
+template <int T>
+__device__ __forceinline__ BlockEnc block_encode(float b, float S) {
+  float q = (T == 4) ? __fmul_rn(b, 0.25f) : __fdiv_rn(b, (float)T);  // b/4 == b*0.25 exactly
+  float s32 = __fmul_rn(q, S);
+  BlockEnc r;
+  r.s8 = e4m3_byte(s32);
+  r.sd = e4m3_value(r.s8);
+  r.e = (r.sd == 0.0f) ? 0.0f : __fdiv_rn(S, r.sd);
+  return r;
+}
+
+// Dequantize factor (decode(s8) * a) * F_inv of a block.
+__device__ __forceinline__ float dequant_factor(float sd, float a, float F_inv) {
+  return __fmul_rn(__fmul_rn(sd, a), F_inv);
+}
+
+// Running squared error over 8 values and their 8 codes (packed), in order.
+__device__ __forceinline__ float sse8(float err, const float* x, uint32_t codes, float D) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float v0, v1;
+    e2m1x2_values(codes >> (8 * k), v0, v1);
+    float d0 = __fsub_rn(x[2 * k], __fmul_rn(v0, D));
+    err = __fadd_rn(err, __fmul_rn(d0, d0));
+    float d1 = __fsub_rn(x[2 * k + 1], __fmul_rn(v1, D));
+    err = __fadd_rn(err, __fmul_rn(d1, d1));
+  }
+  return err;
+}
+
+// Quantize 16 FP32 values of one block: writes the two code words and returns
+// the scale byte.  FOS: four-over-six (needs line amax a and F_inv).
+template <bool FOS>
+__device__ __forceinline__ uint32_t quantize16(const float* x, float S, float a, float F_inv,
+                                               uint32_t& c0, uint32_t& c1) {
+  float b = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(x[i]));
+  BlockEnc e6 = block_encode<6>(b, S);
+  c0 = e2m1x8(__fmul_rn(x[0], e6.e), __fmul_rn(x[1], e6.e), __fmul_rn(x[2], e6.e),
+              __fmul_rn(x[3], e6.e), __fmul_rn(x[4], e6.e), __fmul_rn(x[5], e6.e),
+              __fmul_rn(x[6], e6.e), __fmul_rn(x[7], e6.e));
+  c1 = e2m1x8(__fmul_rn(x[8], e6.e), __fmul_rn(x[9], e6.e), __fmul_rn(x[10], e6.e),
+              __fmul_rn(x[11], e6.e), __fmul_rn(x[12], e6.e), __fmul_rn(x[13], e6.e),
+              __fmul_rn(x[14], e6.e), __fmul_rn(x[15], e6.e));
+  if constexpr (!FOS) {
+    return e6.s8;
+  } else {
+    BlockEnc e4 = block_encode<4>(b, S);
+    uint32_t d0 = e2m1x8(__fmul_rn(x[0], e4.e), __fmul_rn(x[1], e4.e), __fmul_rn(x[2], e4.e),
+                         __fmul_rn(x[3], e4.e), __fmul_rn(x[4], e4.e), __fmul_rn(x[5], e4.e),
+                         __fmul_rn(x[6], e4.e), __fmul_rn(x[7], e4.e));
+    uint32_t d1 = e2m1x8(__fmul_rn(x[8], e4.e), __fmul_rn(x[9], e4.e), __fmul_rn(x[10], e4.e),
+                         __fmul_rn(x[11], e4.e), __fmul_rn(x[12], e4.e), __fmul_rn(x[13], e4.e),
+                         __fmul_rn(x[14], e4.e), __fmul_rn(x[15], e4.e));
+    float D6 = dequant_factor(e6.sd, a, F_inv);
+    float D4 = dequant_factor(e4.sd, a, F_inv);
+    float err6 = sse8(sse8(0.0f, x, c0, D6), x + 8, c1, D6);
+    float err4 = sse8(sse8(0.0f, x, d0, D4), x + 8, d1, D4);
+    if (err4 < err6) {
+      c0 = d0;
+      c1 = d1;
+      return e4.s8;
+    }
+    return e6.s8;
+  }
+}
+
+// ---------------------------------------------------------------- mbarrier / TMA
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~2 s (or 2^28 polls) and
+// returns false; the caller then records a timeout and leaves.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0; it < (1u << 28); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u && global_timer_ns() - t0 > 2000000000ull) break;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2D tiled TMA load global -> shared, completing on `bar`; x = innermost (column)
+// coordinate, y = row coordinate.  policy: an L2 cache policy from createpolicy.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16-byte global load with an L2 cache policy (read-only data).
+__device__ __forceinline__ uint4 ldg_v4_policy(const void* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
+// Streaming stores for outputs that are not read again by this kernel.
+__device__ __forceinline__ void stg_v4_cs(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void stg_v2_cs(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void stg_u32_cs(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+__device__ __forceinline__ void stg_u16_cs(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"((uint16_t)a) : "memory");
+}
+
+// Write n bytes (n <= 16) of the little-endian words w[] to p, with the widest
+// stores the alignment of p and n allow.
+__device__ __forceinline__ void store_bytes(uint8_t* p, const uint32_t* w, int n) {
+  if (n == 16 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+    stg_v4_cs(p, make_uint4(w[0], w[1], w[2], w[3]));
+    return;
+  }
+  if (n == 8 && (reinterpret_cast<uintptr_t>(p) & 7u) == 0) {
+    stg_v2_cs(p, w[0], w[1]);
+    return;
+  }
+  if ((n & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 3u) == 0) {
+    for (int i = 0; i < n / 4; ++i) stg_u32_cs(p + 4 * i, w[i]);
+    return;
+  }
+  for (int i = 0; i < n; ++i) p[i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,119 @@
+// internal.h -- host-side launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+enum class InType : int { BF16 = 0, FP32 = 1 };
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int* status;  // device address of the library status word
+};
+
+// Zero up to four float arrays and copy up to two (dst <- src), unless noop.
+struct PrepArgs {
+  float* zero_ptr[4];
+  int64_t zero_n[4];
+  float* copy_dst[2];
+  const float* copy_src[2];
+  int64_t copy_n[2];
+  const float* noop;
+};
+cudaError_t launch_prep(const PrepArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// Fused exact amax over x [M][K].  Outputs must be zeroed first (launch_prep)
+// unless they are NULL.  Maxima are published with atomicMax on the FP32 bit
+// pattern (valid for non-negative values).
+struct AmaxArgs {
+  const void* x;
+  InType in;
+  int64_t M, K;
+  float* row_amax;     // [M] or NULL
+  float* col_amax;     // [K] or NULL
+  float* tensor_amax;  // [1] or NULL
+  const float* noop;
+  const int64_t* group_ends;  // optional: do nothing unless these group ends are valid
+  int num_groups;
+};
+cudaError_t launch_amax(const AmaxArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// Grouped amax: group_amax[g] = max over rows of group g (must be zeroed first).
+struct GroupedAmaxArgs {
+  const void* x;
+  InType in;
+  int64_t M, K;
+  const int64_t* group_ends;
+  int num_groups;
+  float* group_amax;
+  const float* noop;
+};
+cudaError_t launch_grouped_amax(const GroupedAmaxArgs& a, const DeviceInfo& dev,
+                                cudaStream_t stream);
+
+// Validates group ends (sets the status word and returns early if invalid),
+// then performs `prep` (zero / copy) and, in the expand pass, writes
+// expand[r] = group_amax[group of r].
+struct GroupCheckArgs {
+  int64_t M;
+  const int64_t* group_ends;
+  int num_groups;
+  const float* group_amax;
+  float* expand;
+  const float* noop;
+  PrepArgs prep;
+};
+cudaError_t launch_group_check(const GroupCheckArgs& a, const DeviceInfo& dev,
+                               cudaStream_t stream, bool expand_pass);
+
+// Tile quantize of x [M][K] into the rowwise and/or columnwise outputs.
+struct QuantArgs {
+  const void* x;
+  InType in;
+  int64_t M, K;
+  bool row_scaled;
+  bool four_over_six;
+  bool block_2d;
+  float bound;
+  // rowwise output (codes == NULL to skip)
+  uint8_t* row_codes;
+  uint8_t* row_scales;
+  const float* row_amax;  // [M] or [1] (read)
+  // columnwise output (codes == NULL to skip)
+  uint8_t* col_codes;
+  uint8_t* col_scales;
+  const float* col_amax;  // [K] or [1] (read)
+  // per-tensor: copy *copy_src to *copy_dst once (the second direction's amax)
+  float* copy_dst;
+  const float* copy_src;
+  const float* noop;
+  const int64_t* group_ends;  // optional: do nothing unless these group ends are valid
+  int num_groups;
+};
+cudaError_t launch_quantize(const QuantArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+struct DequantArgs {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* amax;
+  bool row_scaled;
+  int64_t rows, cols;
+  float bound;
+  void* out;
+  bool out_bf16;
+};
+cudaError_t launch_dequantize(const DequantArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+cudaError_t launch_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3,
+                                    cudaStream_t stream);
+
+// Host helper (api.cu): encode a 2D tiled tensor map; false if TMA cannot be used.
+bool make_tile_map(CUtensorMap* map, const void* base, InType in, int64_t rows, int64_t cols,
+                   int box_cols, int box_rows);
+
+}  // namespace nvfp4

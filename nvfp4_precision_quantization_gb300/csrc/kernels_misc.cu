@@ -1,0 +1,149 @@
+// kernels_misc.cu -- NVFP4 dequantize and the conversion self-test.
+//
+// Dequantize follows "Add backward overrides and 1x16 weights to NVFP4
+// four-over-six" (torchao PR #8, description): value = code * ((scale * amax) *
+// factor_inv), factor_inv a correctly rounded FP32 reciprocal of bound * 6, with
+// BF16 output rounded to nearest even from the FP32 value.
+//
+// The kernel is write-bound (0.5625 bytes in, 2 or 4 bytes out per element): a
+// thread expands one 16-element block (8 code bytes + 1 scale byte) into 32 or
+// 64 contiguous output bytes, so a warp writes 1 or 2 KB contiguous.
+#include <algorithm>
+
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+namespace {
+
+struct DequantKernelArgs {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* amax;
+  int row_scaled;
+  int64_t rows, cols, nblk;
+  int64_t cpitch, spitch;
+  float F_inv;
+  void* out;
+};
+
+template <bool BF16, bool VEC>
+__global__ void __launch_bounds__(256) k_dequantize(DequantKernelArgs a) {
+  const int64_t total = a.rows * a.nblk;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / a.nblk, j = i % a.nblk;
+    const int64_t c0 = j * 16;
+    const int n = (a.cols - c0) < 16 ? (int)(a.cols - c0) : 16;
+    const float amax = a.amax[a.row_scaled ? r : 0];
+    const float D = dequant_factor(e4m3_value(a.scales[r * a.spitch + j]), amax, a.F_inv);
+    const uint8_t* cp = a.codes + r * a.cpitch + c0 / 2;
+    uint32_t w[2];
+    if (VEC && n == 16) {
+      const uint2 u = *reinterpret_cast<const uint2*>(cp);
+      w[0] = u.x;
+      w[1] = u.y;
+    } else {
+      w[0] = w[1] = 0;
+      for (int b = 0; b < (n + 1) / 2; ++b) w[b >> 2] |= (uint32_t)cp[b] << (8 * (b & 3));
+    }
+    float v[16];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      float lo, hi;
+      e2m1x2_values(w[b >> 2] >> (8 * (b & 3)), lo, hi);
+      v[2 * b] = __fmul_rn(lo, D);
+      v[2 * b + 1] = __fmul_rn(hi, D);
+    }
+    if constexpr (BF16) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + r * a.cols + c0;
+      if (VEC && n == 16) {
+        uint32_t p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+          p[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        stg_v4_cs(o, make_uint4(p[0], p[1], p[2], p[3]));
+        stg_v4_cs(o + 8, make_uint4(p[4], p[5], p[6], p[7]));
+      } else {
+        for (int k = 0; k < n; ++k) o[k] = __float2bfloat16_rn(v[k]);
+      }
+    } else {
+      float* o = static_cast<float*>(a.out) + r * a.cols + c0;
+      if (VEC && n == 16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          stg_v4_cs(o + 4 * k, make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                                          __float_as_uint(v[4 * k + 2]),
+                                          __float_as_uint(v[4 * k + 3])));
+      } else {
+        for (int k = 0; k < n; ++k) o[k] = v[k];
+      }
+    }
+  }
+}
+
+// One code (and one scale byte) per input value, through the same conversion
+// helpers the kernels use: 8 inputs are packed by e2m1x8 and split again, so
+// a wrong nibble order shows up as permuted codes.
+__global__ void k_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3) {
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g * 8 < n;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = (g * 8 + k < n) ? in[g * 8 + k] : 0.0f;
+    const uint32_t w = e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int64_t i = g * 8 + k;
+      if (i < n) {
+        if (e2m1 != nullptr) e2m1[i] = (uint8_t)((w >> (4 * k)) & 15u);
+        if (e4m3 != nullptr) e4m3[i] = (uint8_t)e4m3_byte(v[k]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dequantize(const DequantArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
+  DequantKernelArgs a{};
+  a.codes = q.codes;
+  a.scales = q.scales;
+  a.amax = q.amax;
+  a.row_scaled = q.row_scaled ? 1 : 0;
+  a.rows = q.rows;
+  a.cols = q.cols;
+  a.nblk = (q.cols + 15) / 16;
+  a.cpitch = (q.cols + 1) / 2;
+  a.spitch = (q.cols + 15) / 16;
+  a.F_inv = 1.0f / (q.bound * 6.0f);
+  a.out = q.out;
+  const int64_t total = a.rows * a.nblk;
+  if (total == 0) return cudaSuccess;
+  const int elem = q.out_bf16 ? 2 : 4;
+  const bool vec = (a.cpitch % 8 == 0) && ((q.cols * elem) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(q.codes) % 8 == 0) &&
+                   (reinterpret_cast<uintptr_t>(q.out) % 16 == 0);
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 8LL * dev.num_sms);
+  void (*fn)(DequantKernelArgs);
+  if (q.out_bf16) fn = vec ? k_dequantize<true, true> : k_dequantize<true, false>;
+  else fn = vec ? k_dequantize<false, true> : k_dequantize<false, false>;
+  fn<<<(unsigned)blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3,
+                                    cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t groups = (n + 7) / 8;
+  const int64_t blocks = std::min<int64_t>((groups + 255) / 256, 4096);
+  k_selftest_convert<<<(unsigned)blocks, 256, 0, stream>>>(in, n, e2m1, e4m3);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

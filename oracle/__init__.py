@@ -11,6 +11,7 @@ at a time.  BF16 arrays are passed around as their uint16 bit patterns.
 from __future__ import annotations
 
 import ctypes as C
+import os
 
 import numpy as np
 
@@ -25,7 +26,8 @@ ROW_SCALED = 1
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # NVFP4_ORACLE_LIBRARY lets the mutation tests load a deliberately broken copy
+        path = os.environ.get("NVFP4_ORACLE_LIBRARY") or _build.build()
         L = C.CDLL(path)
         f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
         u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")

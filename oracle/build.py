@@ -40,5 +40,17 @@ def build(force: bool = False) -> str:
     return out
 
 
+def build_variant(source_text: str, out_path: str) -> str:
+    """Compile a modified copy of the oracle source (used by the mutation tests,
+    which plant a mistake and check that the pins catch it)."""
+    d = os.path.dirname(out_path)
+    src = os.path.join(d, "variant.c")
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", *[f for f in CFLAGS if f != "-Werror"], src, "-o", out_path, "-lm"],
+                   check=True)
+    return out_path
+
+
 if __name__ == "__main__":
     print(build(force=True))

@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads, and exports every entry point that
+include/nvfp4.h declares (CPU only: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from nvfp4_precision_quantization_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise",
+                 "nvfp4_quantize_both", "nvfp4_dequantize", "nvfp4_grouped_amax",
+                 "nvfp4_grouped_quantize_rowwise", "nvfp4_last_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib_path):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {n for n in exported if n.startswith("nvfp4_")}
+    assert ours == set(declared_functions())
+
+
+def test_binding_wraps_every_symbol(lib_path):
+    import nvfp4_precision_quantization_gb300 as nv
+    assert set(nv.EXPORTED_SYMBOLS) == set(declared_functions())
+    nv.load_library()
+    for name in declared_functions():
+        assert callable(getattr(nv, name))
+
+
+def test_host_validation_without_gpu(lib_path):
+    """Argument checks run before any CUDA call, so they work on a CPU host."""
+    import nvfp4_precision_quantization_gb300 as nv
+    L = nv.load_library()
+    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 300.0, 0, 0)  # bad bound
+    out = nv._COut(1, 1, 1, None)
+    st = L.nvfp4_quantize_rowwise(16, nv.NVFP4_IN_BF16, 4, 4, ctypes.byref(cfg),
+                                  ctypes.byref(out), None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "bound" in nv.nvfp4_last_error()
+    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 1)  # 16x16 with row-scaled
+    st = L.nvfp4_quantize_rowwise(16, nv.NVFP4_IN_BF16, 4, 4, ctypes.byref(cfg),
+                                  ctypes.byref(out), None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "16x16" in nv.nvfp4_last_error()
+    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+    st = L.nvfp4_quantize_rowwise(16, 7, 4, 4, ctypes.byref(cfg), ctypes.byref(out), None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "dtype" in nv.nvfp4_last_error()
+    st = L.nvfp4_quantize_rowwise(16, nv.NVFP4_IN_BF16, -1, 4, ctypes.byref(cfg),
+                                  ctypes.byref(out), None, None)
+    assert st == nv.NVFP4_ERR_INVALID
+    st = L.nvfp4_quantize_rowwise(None, nv.NVFP4_IN_BF16, 4, 4, ctypes.byref(cfg),
+                                  ctypes.byref(out), None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "x is NULL" in nv.nvfp4_last_error()
+    st = L.nvfp4_dequantize(1, 1, 1, nv.NVFP4_ROW_SCALED, 4, 4, 448.0, 1, 9, None)
+    assert st == nv.NVFP4_ERR_INVALID
+    st = L.nvfp4_grouped_amax(1, nv.NVFP4_IN_BF16, 4, 4, 1, 0, 1, None, None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "num_groups" in nv.nvfp4_last_error()
+    st = L.nvfp4_amax(1, nv.NVFP4_IN_BF16, 4, 4, None, None, None, None, None)
+    assert st == nv.NVFP4_ERR_INVALID
