@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 SOURCES = ["api.cu", "kernels_amax.cu", "kernels_quantize.cu", "kernels_misc.cu"]
-HEADERS = ["device_common.cuh", "internal.h"]
+HEADERS = ["device_common.cuh", "internal.h", "tile_pipeline.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC",

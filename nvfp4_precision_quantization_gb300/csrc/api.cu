@@ -275,6 +275,24 @@ bool make_tile_map(CUtensorMap* map, const void* base, InType in, int64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+bool make_byte_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pitch,
+                   int box_bytes, int box_rows) {
+  if (rows <= 0 || pitch <= 0) return false;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || pitch % 16 != 0) return false;
+  if (rows >= (1LL << 31) || pitch >= (1LL << 31)) return false;
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)pitch};
+  const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;

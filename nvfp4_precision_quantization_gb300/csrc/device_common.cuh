@@ -164,14 +164,12 @@ __device__ __forceinline__ float sse8(float err, const float* x, uint32_t codes,
   return err;
 }
 
-// Quantize 16 FP32 values of one block: writes the two code words and returns
-// the scale byte.  FOS: four-over-six (needs line amax a and F_inv).
+// Quantize 16 FP32 values of one block whose max |x| is b: writes the two code
+// words (value k in nibble k) and returns the scale byte.  FOS: four-over-six
+// (needs the line amax a and F_inv for the error of each candidate).
 template <bool FOS>
-__device__ __forceinline__ uint32_t quantize16(const float* x, float S, float a, float F_inv,
-                                               uint32_t& c0, uint32_t& c1) {
-  float b = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(x[i]));
+__device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S, float a,
+                                               float F_inv, uint32_t& c0, uint32_t& c1) {
   BlockEnc e6 = block_encode<6>(b, S);
   c0 = e2m1x8(__fmul_rn(x[0], e6.e), __fmul_rn(x[1], e6.e), __fmul_rn(x[2], e6.e),
               __fmul_rn(x[3], e6.e), __fmul_rn(x[4], e6.e), __fmul_rn(x[5], e6.e),
@@ -200,6 +198,14 @@ __device__ __forceinline__ uint32_t quantize16(const float* x, float S, float a,
     }
     return e6.s8;
   }
+}
+
+// Codes of 16 values with a given encode factor (16x16 blocks: the tile's scale).
+__device__ __forceinline__ void codes16(const float* x, float e, uint32_t& c0, uint32_t& c1) {
+  c0 = e2m1x8(__fmul_rn(x[0], e), __fmul_rn(x[1], e), __fmul_rn(x[2], e), __fmul_rn(x[3], e),
+              __fmul_rn(x[4], e), __fmul_rn(x[5], e), __fmul_rn(x[6], e), __fmul_rn(x[7], e));
+  c1 = e2m1x8(__fmul_rn(x[8], e), __fmul_rn(x[9], e), __fmul_rn(x[10], e), __fmul_rn(x[11], e),
+              __fmul_rn(x[12], e), __fmul_rn(x[13], e), __fmul_rn(x[14], e), __fmul_rn(x[15], e));
 }
 
 // ---------------------------------------------------------------- mbarrier / TMA
@@ -267,6 +273,32 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 2D tiled TMA store shared -> global (bulk-group completion).  Elements outside
+// the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(smem_addr(src)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until the committed bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// wait until the committed bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// make generic-proxy shared-memory writes visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -298,6 +330,28 @@ __device__ __forceinline__ uint4 ldg_v4_policy(const void* p, uint64_t policy) {
 __device__ __forceinline__ void stg_v4_cs(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void sts_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void sts_v2(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_addr(p)), "r"(a), "r"(b) : "memory");
+}
+// Stores that should stay in L2 until their 32-byte sector is complete (scale
+// bytes written in pieces by consecutive tiles).
+__device__ __forceinline__ void stg_v2_keep(void* p, uint32_t a, uint32_t b, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(a), "r"(b),
+               "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void stg_u32_keep(void* p, uint32_t a, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(a), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void stg_u16_keep(void* p, uint32_t a, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u16 [%0], %1, %2;" ::"l"(p), "h"((uint16_t)a), "l"(pol)
                : "memory");
 }
 __device__ __forceinline__ void stg_v2_cs(void* p, uint32_t a, uint32_t b) {

@@ -112,8 +112,14 @@ cudaError_t launch_dequantize(const DequantArgs& a, const DeviceInfo& dev, cudaS
 cudaError_t launch_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3,
                                     cudaStream_t stream);
 
-// Host helper (api.cu): encode a 2D tiled tensor map; false if TMA cannot be used.
+// Grid size shared by the TMA amax and encode kernels (same tile -> CTA mapping).
+int pipe_grid_size(int64_t num_tiles, int num_sms);
+
+// Host helpers (api.cu): encode 2D tiled tensor maps; false if TMA cannot be used.
 bool make_tile_map(CUtensorMap* map, const void* base, InType in, int64_t rows, int64_t cols,
                    int box_cols, int box_rows);
+// byte matrix [rows][pitch] (an output of codes), box of box_bytes x box_rows
+bool make_byte_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pitch,
+                   int box_bytes, int box_rows);
 
 }  // namespace nvfp4

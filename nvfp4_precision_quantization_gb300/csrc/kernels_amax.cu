@@ -15,9 +15,11 @@
 // Publishing uses atomicMax on the FP32 bit pattern, valid because every value
 // is >= 0, and exact and order-independent.
 #include <algorithm>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "tile_pipeline.cuh"
 
 namespace nvfp4 {
 
@@ -346,6 +348,267 @@ AmaxFn pick_amax(InType in, bool vec, bool row, bool col, bool ten) {
   }
 }
 
+// ---------------------------------------------------------------- TMA amax kernel
+
+// The same tiles, tile order and grid size as the encode kernel (see
+// tile_pipeline.cuh): CTA j walks its chunk in the direction opposite to the
+// encode kernel's CTA j, so that kernel finds the tail of the walk in L2 (the
+// last tiles of each walk are loaded with an L2 evict_last policy).
+//
+// Consumer warp w reads box (w & 1), rows 32 * (w >> 1) .. +32; lane l owns the
+// 16-byte column chunk (l & 7) of rows (l >> 3) + 4 i.  Column maxima of the
+// super-strip's kGroup tile columns stay in registers while the CTA walks down
+// the super-strip and are published when it moves to another one; row maxima are
+// reduced over the 8 lanes that share a row with a transposing shuffle reduction
+// and published per tile.
+struct AmaxTmaArgs {
+  int64_t M, K;
+  TileGrid grid;
+  float* row_amax;
+  float* col_amax;
+  float* tensor_amax;
+  const float* noop;
+  const int64_t* ends;
+  int G;
+  int keep_tiles;  // the last keep_tiles tiles of a chunk are loaded with evict_last
+  int* status;
+};
+
+template <typename T, bool ROW, bool COL, bool TEN>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+    k_amax_tma(const __grid_constant__ CUtensorMap tmap, AmaxTmaArgs a) {
+  using Geo = TileGeo<T>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ __align__(8) uint64_t empty[kStages];
+  __shared__ volatile int abort_flag;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  if (noop_set(a.noop)) return;
+  if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int begin, end;
+  a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
+  const int count = end - begin;
+  const bool fwd = (blockIdx.x & 1) == 0;  // the encode kernel walks this chunk the other way
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (count <= 0) return;
+
+  if (warp == kConsumerWarps) {
+    if (lane != 0) return;
+    prefetch_tmap(&tmap);
+    const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
+    int issued = 0;
+    for (int k = 0; k < count; ++k) {
+      const int s = k % kStages;
+      if (k >= kStages &&
+          !mbar_wait_bounded(&empty[s], (uint32_t)(((k / kStages) - 1) & 1))) {
+        abort_flag = 1;
+        raise_status(a.status, kStatusTimeout);
+        break;
+      }
+      if (abort_flag) break;
+      int tm, tn;
+      a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+      issue_tile<T>(smem + s * kTileBytes, &tmap, &full[s], tm, tn,
+                    k >= count - a.keep_tiles ? pol_last : pol_first);
+      issued = k + 1;
+    }
+    if (abort_flag)
+      for (int k = issued - kStages > 0 ? issued - kStages : 0; k < issued; ++k)
+        (void)mbar_wait_bounded(&full[k % kStages], (uint32_t)((k / kStages) & 1));
+    return;
+  }
+
+  // consumers: the preceding kernel zeroes the outputs
+  pdl_wait();
+  const int box = warp & 1, rg = warp >> 1;
+  const int c = lane & 7, ro = lane >> 3;
+  const uint32_t offA = box * kBoxBytes + ((c ^ (ro & 7)) << 4);
+  const uint32_t offB = box * kBoxBytes + ((c ^ ((ro + 4) & 7)) << 4);
+  constexpr bool BF16 = sizeof(T) == 2;
+  constexpr int NG = TileGrid::kGroup;
+  using Acc = typename std::conditional<BF16, uint32_t, float>::type;
+  Acc cm[NG][4];
+#pragma unroll
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cm[g][j] = 0;
+  Acc tmx = 0;
+  int cur_ss = -1;
+
+  auto flush_cols = [&](int ss) {
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const int tn = ss * NG + g;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if constexpr (BF16) {
+          cm[g][j] = absmax_bf16x2(cm[g][j], __shfl_xor_sync(0xffffffffu, cm[g][j], 8));
+          cm[g][j] = absmax_bf16x2(cm[g][j], __shfl_xor_sync(0xffffffffu, cm[g][j], 16));
+        } else {
+          cm[g][j] = fmaxf(cm[g][j], __shfl_xor_sync(0xffffffffu, cm[g][j], 8));
+          cm[g][j] = fmaxf(cm[g][j], __shfl_xor_sync(0xffffffffu, cm[g][j], 16));
+        }
+      }
+      if (ro == 0 && tn < a.grid.tiles_n) {
+        const int64_t col0 = (int64_t)tn * Geo::TILEC + box * Geo::BOXC + c * (16 / (int)sizeof(T));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if constexpr (BF16) {
+            const uint32_t mv = cm[g][j] & 0x7fff7fffu;
+            if (col0 + 2 * j < a.K)
+              atomic_max_nonneg(&a.col_amax[col0 + 2 * j], __uint_as_float(mv << 16));
+            if (col0 + 2 * j + 1 < a.K)
+              atomic_max_nonneg(&a.col_amax[col0 + 2 * j + 1], __uint_as_float(mv & 0xffff0000u));
+          } else {
+            if (col0 + j < a.K) atomic_max_nonneg(&a.col_amax[col0 + j], cm[g][j]);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cm[g][j] = 0;
+    }
+  };
+
+  for (int k = 0; k < count; ++k) {
+    const int s = k % kStages;
+    int tm, tn;
+    a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+    const int ss = tn / NG, gsel = tn - ss * NG;
+    if (COL && ss != cur_ss) {
+      if (cur_ss >= 0) flush_cols(cur_ss);
+      cur_ss = ss;
+    }
+    if (!mbar_wait_bounded(&full[s], (uint32_t)((k / kStages) & 1))) {
+      abort_flag = 1;
+      if (lane == 0) raise_status(a.status, kStatusTimeout);
+      break;
+    }
+    if (abort_flag) break;
+    const uint8_t* stage = smem + s * kTileBytes + (rg * 32 + ro) * 128;
+    Acc rp[8], ct[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(stage + i * 4 * 128 + ((i & 1) ? offB : offA));
+      if constexpr (BF16) {
+        if (COL) {
+          ct[0] = absmax_bf16x2(ct[0], v.x);
+          ct[1] = absmax_bf16x2(ct[1], v.y);
+          ct[2] = absmax_bf16x2(ct[2], v.z);
+          ct[3] = absmax_bf16x2(ct[3], v.w);
+        }
+        rp[i] = absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w));
+      } else {
+        const float e0 = fabsf(__uint_as_float(v.x)), e1 = fabsf(__uint_as_float(v.y));
+        const float e2 = fabsf(__uint_as_float(v.z)), e3 = fabsf(__uint_as_float(v.w));
+        if (COL) {
+          ct[0] = fmaxf(ct[0], e0);
+          ct[1] = fmaxf(ct[1], e1);
+          ct[2] = fmaxf(ct[2], e2);
+          ct[3] = fmaxf(ct[3], e3);
+        }
+        rp[i] = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the tile is in registers now
+    if (COL) {
+      // merge into the partials of this tile's column strip (register arrays
+      // cannot be indexed at run time: select)
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          Acc mv;
+          if constexpr (BF16) mv = absmax_bf16x2(cm[g][j], ct[j]);
+          else mv = fmaxf(cm[g][j], ct[j]);
+          cm[g][j] = (g == gsel) ? mv : cm[g][j];
+        }
+      }
+    }
+    if (TEN) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if constexpr (BF16) tmx = absmax_bf16x2(tmx, rp[i]);
+        else tmx = fmaxf(tmx, rp[i]);
+      }
+    }
+    if (ROW) {
+      const int64_t row0 = (int64_t)tm * kTileRows + rg * 32 + ro;
+      if constexpr (BF16) {
+        // fold each pair, pack two rows per word, reduce over the 8 lanes of the row
+        uint32_t P[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t f0 = absmax_bf16x2(rp[2 * j], __byte_perm(rp[2 * j], 0, 0x1032));
+          const uint32_t f1 = absmax_bf16x2(rp[2 * j + 1], __byte_perm(rp[2 * j + 1], 0, 0x1032));
+          P[j] = __byte_perm(f0, f1, 0x7610);
+        }
+        const bool u4 = lane & 4, u2 = lane & 2;
+        uint32_t q0 = absmax_bf16x2(u4 ? P[2] : P[0], __shfl_xor_sync(0xffffffffu, u4 ? P[0] : P[2], 4));
+        uint32_t q1 = absmax_bf16x2(u4 ? P[3] : P[1], __shfl_xor_sync(0xffffffffu, u4 ? P[1] : P[3], 4));
+        uint32_t rr = absmax_bf16x2(u2 ? q1 : q0, __shfl_xor_sync(0xffffffffu, u2 ? q0 : q1, 2));
+        rr = absmax_bf16x2(rr, __shfl_xor_sync(0xffffffffu, rr, 1)) & 0x7fff7fffu;
+        if ((lane & 1) == 0) {
+          const int i0 = (u4 ? 4 : 0) + (u2 ? 2 : 0);
+          const int64_t r0 = row0 + 4 * i0, r1 = r0 + 4;
+          if (r0 < a.M) atomic_max_nonneg(&a.row_amax[r0], __uint_as_float(rr << 16));
+          if (r1 < a.M) atomic_max_nonneg(&a.row_amax[r1], __uint_as_float(rr & 0xffff0000u));
+        }
+      } else {
+        const bool u4 = lane & 4, u2 = lane & 2, u1 = lane & 1;
+        float q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          q[j] = fmaxf(u4 ? rp[4 + j] : rp[j], __shfl_xor_sync(0xffffffffu, u4 ? rp[j] : rp[4 + j], 4));
+        float h[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          h[j] = fmaxf(u2 ? q[2 + j] : q[j], __shfl_xor_sync(0xffffffffu, u2 ? q[j] : q[2 + j], 2));
+        const float g = fmaxf(u1 ? h[1] : h[0], __shfl_xor_sync(0xffffffffu, u1 ? h[0] : h[1], 1));
+        const int i0 = (u4 ? 4 : 0) + (u2 ? 2 : 0) + (u1 ? 1 : 0);
+        const int64_t r0 = row0 + 4 * i0;
+        if (r0 < a.M) atomic_max_nonneg(&a.row_amax[r0], g);
+      }
+    }
+  }
+  if (COL && cur_ss >= 0 && !abort_flag) flush_cols(cur_ss);
+  if (TEN) {
+    float m;
+    if constexpr (BF16) m = bf16x2_hmax_f32(tmx);
+    else m = tmx;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) atomic_max_nonneg(a.tensor_amax, m);
+  }
+}
+
+using AmaxTmaFn = void (*)(const CUtensorMap, AmaxTmaArgs);
+
+template <typename T>
+AmaxTmaFn pick_amax_tma(bool row, bool col, bool ten) {
+  const int key = (row ? 4 : 0) | (col ? 2 : 0) | (ten ? 1 : 0);
+  switch (key) {
+    case 1: return k_amax_tma<T, false, false, true>;
+    case 2: return k_amax_tma<T, false, true, false>;
+    case 3: return k_amax_tma<T, false, true, true>;
+    case 4: return k_amax_tma<T, true, false, false>;
+    case 5: return k_amax_tma<T, true, false, true>;
+    case 6: return k_amax_tma<T, true, true, false>;
+    case 7: return k_amax_tma<T, true, true, true>;
+    default: return nullptr;
+  }
+}
+
 // ---------------------------------------------------------------- grouped
 
 constexpr int kMaxGroups = 4096;
@@ -486,6 +749,47 @@ cudaError_t launch_prep(const PrepArgs& a, const DeviceInfo& dev, cudaStream_t s
 
 cudaError_t launch_amax(const AmaxArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   if (a.M == 0 || a.K == 0) return cudaSuccess;
+  {
+    const bool bf16 = a.in == InType::BF16;
+    const int box_cols = bf16 ? TileGeo<uint16_t>::BOXC : TileGeo<float>::BOXC;
+    CUtensorMap map;
+    if (make_tile_map(&map, a.x, a.in, a.M, a.K, box_cols, kTileRows)) {
+      AmaxTmaArgs k{};
+      k.M = a.M;
+      k.K = a.K;
+      k.grid.tiles_m = (int)((a.M + kTileRows - 1) / kTileRows);
+      k.grid.tiles_n = (int)((a.K + 2 * box_cols - 1) / (2 * box_cols));
+      k.grid.num_tiles = k.grid.tiles_m * k.grid.tiles_n;
+      k.row_amax = a.row_amax;
+      k.col_amax = a.col_amax;
+      k.tensor_amax = a.tensor_amax;
+      k.noop = a.noop;
+      k.ends = a.group_ends;
+      k.G = a.num_groups;
+      k.status = dev.status;
+      const int grid = pipe_grid_size(k.grid.num_tiles, dev.num_sms);
+      // keep about 80 MB of the tail of the walk in L2 for the encode pass
+      k.keep_tiles = (int)std::max<int64_t>(1, (80LL << 20) / ((int64_t)grid * kTileBytes));
+      AmaxTmaFn fn = bf16 ? pick_amax_tma<uint16_t>(a.row_amax, a.col_amax, a.tensor_amax)
+                          : pick_amax_tma<float>(a.row_amax, a.col_amax, a.tensor_amax);
+      if (fn == nullptr) return cudaSuccess;
+      constexpr int smem = kStages * kTileBytes + 1024;
+      cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (err != cudaSuccess) return err;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)grid);
+      cfg.blockDim = dim3(kPipeThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, fn, map, k);
+    }
+  }
+  // x rows not 16-byte aligned: plain 128-bit (or scalar) loads
   const int elem = a.in == InType::BF16 ? 2 : 4;
   const int VE = 16 / elem;
   const int CW = kColWarps * 32 * VE;

@@ -8,61 +8,33 @@
 // four-over-six grouped GEMM for MoE training" (torchao PR #9) and "Add
 // backward overrides and 1x16 weights to NVFP4 four-over-six" (torchao PR #8).
 //
-// Design (sm_103a): a persistent grid of 2 CTAs per SM walks 128-row tiles of x
-// (128 BF16 or 64 FP32 columns = two 128-byte TMA boxes with the 128-byte
-// swizzle) through a 3-stage shared-memory ring filled by cp.async.bulk.tensor
-// and tracked by mbarriers.  Rowwise blocks are read as 16-byte rows of a box;
-// columnwise blocks are read down a column pair; both access patterns are
-// bank-conflict free under the swizzle.  Tiles are visited in reverse order so
-// that the tail of x, which the amax pass read last, is re-read from L2.
+// Design (sm_103a): a persistent grid of 2 CTAs per SM; each CTA walks its chunk
+// of the strip-major tile order backwards (see tile_pipeline.cuh).  Warp 8 is the
+// producer: lane 0 issues the two TMA boxes of a tile into a 3-stage ring, then
+// the warp stages the tile's per-row and per-column amax and global scale
+// S = F / amax in shared memory (one division per row / column instead of one per
+// thread).  Warps 0-7 consume: with both directions, warps 0-3 encode rows (a
+// thread = one row, 128 bytes of each box) and warps 4-7 encode columns (a thread
+// = a column pair over 64 rows).  Each consumer warp releases a stage through an
+// "empty" mbarrier, so warps never wait for each other.  Shared-memory reads are
+// bank-conflict free under the swizzle; stores are 16-byte streaming stores of
+// full 32-byte sectors on interior tiles.
 #include <algorithm>
+#include <cstring>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "tile_pipeline.cuh"
 
 namespace nvfp4 {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTileRows = 128;
-constexpr int kStages = 3;
-constexpr int kBoxBytes = 128 * 128;       // 128 rows x 128 bytes
-constexpr int kStageBytes = 2 * kBoxBytes;  // two boxes per tile
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 
-template <typename T>
-struct Geo {
-  static constexpr int ELEM = sizeof(T);
-  static constexpr int BOXC = 128 / ELEM;  // columns per box (64 BF16 / 32 FP32)
-  static constexpr int TILEC = 2 * BOXC;   // columns per tile
-  static constexpr int NB_R = BOXC / 16;   // rowwise blocks per thread
-  static constexpr int NP = TILEC / 2;     // column pairs per tile
-  static constexpr int NQ = kThreads / NP; // row groups of the columnwise threads
-  static constexpr int RQ = kTileRows / NQ;// rows per columnwise thread
-  static constexpr int NB_C = RQ / 16;     // columnwise blocks per column per thread
-  static constexpr int SUBC = TILEC / 16;  // 16x16 sub-tiles across a tile
-  static constexpr int NSUB = (kTileRows / 16) * SUBC;
-};
-
-// Byte offset of element (r, c) of a tile in its stage buffer (128-byte swizzle:
-// the 16-byte chunk index inside each 128-byte row is XORed with r mod 8).
-template <typename T>
-__device__ __forceinline__ uint32_t soff(int r, int c) {
-  constexpr int BOXC = Geo<T>::BOXC;
-  const int box = c / BOXC;
-  const int byte = (c % BOXC) * (int)sizeof(T);
-  return box * kBoxBytes + r * 128 + ((((byte >> 4) ^ (r & 7))) << 4) + (byte & 15);
-}
-
-__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
-  return *reinterpret_cast<const uint4*>(p);
-}
-
-struct QuantKernelArgs {
+struct EncodeArgs {
   const void* x;
   int64_t M, K;
-  int64_t tiles_n, num_tiles;
+  TileGrid grid;
   uint8_t* row_codes;
   uint8_t* row_scales;
   const float* row_amax;
@@ -78,346 +50,671 @@ struct QuantKernelArgs {
   int* status;
   const int64_t* ends;
   int G;
+  int full_m, full_n;  // tiles with tm < full_m and tn < full_n lie entirely inside x
+  int vec_ok;          // output pitches / bases allow the 16-byte stores
 };
 
-// ---------------------------------------------------------------- per-thread work
+struct StageMeta {
+  float rowS[kTileRows], rowA[kTileRows];
+  float colS[128], colA[128];
+  uint32_t s2d[64];
+  float e2d[64];
+};
 
-// Unpack 16 values of a rowwise block from two 16-byte chunks.
-template <typename T>
-__device__ __forceinline__ void unpack16(const uint4& v0, const uint4& v1, const uint4& v2,
-                                         const uint4& v3, float* x) {
-  if constexpr (sizeof(T) == 2) {
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// max |.| over 8 packed BF16 pairs, as FP32
+__device__ __forceinline__ float absmax8_bf16(const uint4& v0, const uint4& v1) {
+  uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(v0.x, v0.y), absmax_bf16x2(v0.z, v0.w)),
+                             absmax_bf16x2(absmax_bf16x2(v1.x, v1.y), absmax_bf16x2(v1.z, v1.w)));
+  return bf16x2_hmax_f32(m);
+}
+
+__device__ __forceinline__ float absmax16_f32(const float* x) {
+  float b = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[2 * i] = bf16_lo(w[i]);
-      x[2 * i + 1] = bf16_hi(w[i]);
-    }
-  } else {
-    const uint32_t w[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
-                            v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(w[i]);
+  for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(x[i]));
+  return b;
+}
+
+// Edge tiles: write the first n (<= 32) bytes of the little-endian words w0..w7,
+// one byte at a time (bounds and alignment of the destination are arbitrary).
+// The words are passed by value so that the fast path keeps them in registers.
+__device__ __noinline__ void store_tail(uint8_t* p, int n, uint32_t w0, uint32_t w1, uint32_t w2,
+                                        uint32_t w3, uint32_t w4, uint32_t w5, uint32_t w6,
+                                        uint32_t w7) {
+  for (int i = 0; i < n; ++i) {
+    const int k = i >> 2;
+    const uint32_t w = k == 0 ? w0 : k == 1 ? w1 : k == 2 ? w2 : k == 3 ? w3
+                     : k == 4 ? w4 : k == 5 ? w5 : k == 6 ? w6 : w7;
+    p[i] = (uint8_t)(w >> (8 * (i & 3)));
   }
 }
 
-template <typename T, bool B2D>
-__device__ __forceinline__ uint32_t encode_block(const float* x, float S, float a, float F_inv,
-                                                 bool fos, uint32_t s2d, float e2d, uint32_t& c0,
-                                                 uint32_t& c1) {
+template <int NW>
+__device__ __forceinline__ void store_tail_words(uint8_t* p, const uint32_t (&w)[NW], int n) {
+  store_tail(p, n, w[0], NW > 1 ? w[1 < NW ? 1 : 0] : 0u, NW > 2 ? w[2 < NW ? 2 : 0] : 0u,
+             NW > 3 ? w[3 < NW ? 3 : 0] : 0u, NW > 4 ? w[4 < NW ? 4 : 0] : 0u,
+             NW > 5 ? w[5 < NW ? 5 : 0] : 0u, NW > 6 ? w[6 < NW ? 6 : 0] : 0u,
+             NW > 7 ? w[7 < NW ? 7 : 0] : 0u);
+}
+
+template <bool FOS, bool B2D>
+__device__ __forceinline__ uint32_t encode_block(const float* x, float b, float S, float a,
+                                                 float F_inv, uint32_t s2d, float e2d,
+                                                 uint32_t& c0, uint32_t& c1) {
   if constexpr (B2D) {
-    c0 = e2m1x8(__fmul_rn(x[0], e2d), __fmul_rn(x[1], e2d), __fmul_rn(x[2], e2d),
-                __fmul_rn(x[3], e2d), __fmul_rn(x[4], e2d), __fmul_rn(x[5], e2d),
-                __fmul_rn(x[6], e2d), __fmul_rn(x[7], e2d));
-    c1 = e2m1x8(__fmul_rn(x[8], e2d), __fmul_rn(x[9], e2d), __fmul_rn(x[10], e2d),
-                __fmul_rn(x[11], e2d), __fmul_rn(x[12], e2d), __fmul_rn(x[13], e2d),
-                __fmul_rn(x[14], e2d), __fmul_rn(x[15], e2d));
+    codes16(x, e2d, c0, c1);
     return s2d;
   } else {
-    if (fos) return quantize16<true>(x, S, a, F_inv, c0, c1);
-    return quantize16<false>(x, S, a, F_inv, c0, c1);
+    return quantize16<FOS>(x, b, S, a, F_inv, c0, c1);
   }
 }
 
-// Rowwise: thread = one row of one box (NB_R blocks of 16).
-template <typename T, bool FOS, bool B2D>
-__device__ __forceinline__ void rowwise_tile(const uint8_t* stage, const QuantKernelArgs& a,
-                                             int64_t tm, int64_t tn, float S_tensor,
-                                             const uint32_t* s2d_s8, const float* s2d_e) {
-  using G = Geo<T>;
-  const int tid = threadIdx.x;
-  const int r = tid & (kTileRows - 1), box = tid >> 7;
-  const int64_t gr = tm * kTileRows + r;
-  const int64_t gc0 = tn * G::TILEC + box * G::BOXC;
-  if (gr >= a.M || gc0 >= a.K) return;
-  const float amax = a.row_amax[a.row_scaled ? gr : 0];
-  const float S = a.row_scaled ? global_scale(amax, a.F) : S_tensor;
-  uint32_t w[2 * G::NB_R];
-  uint32_t sc = 0;
-  const uint8_t* rowp = stage + box * kBoxBytes + r * 128;
-#pragma unroll
-  for (int j = 0; j < G::NB_R; ++j) {
-    float x[16];
-    constexpr int CH = 16 * (int)sizeof(T) / 16;  // 16-byte chunks per block (2 or 4)
-    uint4 v[4];
-#pragma unroll
-    for (int k = 0; k < CH; ++k) v[k] = lds128(rowp + ((((CH * j + k) ^ (r & 7))) << 4));
-    unpack16<T>(v[0], v[1], CH > 2 ? v[2] : v[0], CH > 2 ? v[3] : v[0], x);
-    uint32_t s8s = 0;
-    float e2 = 0.f;
-    if constexpr (B2D) {
-      const int sub = (r >> 4) * G::SUBC + (box * G::BOXC) / 16 + j;
-      s8s = s2d_s8[sub];
-      e2 = s2d_e[sub];
-    }
-    const uint32_t s8 = encode_block<T, B2D>(x, S, amax, a.F_inv, FOS, s8s, e2, w[2 * j],
-                                             w[2 * j + 1]);
-    sc |= s8 << (8 * j);
-  }
-  const int64_t rem_c = a.K - gc0;
-  const int ncols = rem_c < G::BOXC ? (int)rem_c : G::BOXC;
-  const int nbytes = (int)((ncols + 1) / 2);
-  const int nsc = (int)((ncols + 15) / 16);
-  uint8_t* cp = a.row_codes + gr * a.row_cpitch + gc0 / 2;
-  store_bytes(cp, w, nbytes < 16 ? nbytes : 16);
-  if (nbytes > 16) store_bytes(cp + 16, w + 4, nbytes - 16);
-  store_bytes(a.row_scales + gr * a.row_spitch + gc0 / 16, &sc, nsc);
-}
+// ---------------------------------------------------------------- rowwise
 
-// Columnwise: thread = a column pair over RQ rows (NB_C blocks per column).
-template <typename T, bool FOS, bool B2D>
-__device__ __forceinline__ void colwise_tile(const uint8_t* stage, const QuantKernelArgs& a,
-                                             int64_t tm, int64_t tn, float S_tensor,
-                                             const uint32_t* s2d_s8, const float* s2d_e) {
-  using G = Geo<T>;
-  const int tid = threadIdx.x;
-  const int p = tid % G::NP, q = tid / G::NP;
-  const int cl = 2 * p;
-  const int64_t gc = tn * G::TILEC + cl;
-  const int64_t gr0 = tm * kTileRows + q * G::RQ;
-  if (gc >= a.K || gr0 >= a.M) return;
-  const bool has1 = gc + 1 < a.K;
-  const float a0 = a.row_scaled ? a.col_amax[gc] : a.col_amax[0];
-  const float a1 = has1 ? (a.row_scaled ? a.col_amax[gc + 1] : a.col_amax[0]) : 0.0f;
-  const float S0 = a.row_scaled ? global_scale(a0, a.F) : S_tensor;
-  const float S1 = a.row_scaled ? global_scale(a1, a.F) : S_tensor;
-  uint32_t w0[2 * G::NB_C], w1[2 * G::NB_C];
-  uint32_t sc0 = 0, sc1 = 0;
+// Codes and scales of row r of boxes [b0, b0 + NBOX): w[box][word], sc[box].
+// Rows / columns outside x were zero-filled by the load, so they encode to 0;
+// the caller decides what is stored.
+template <typename T, int NBOX, bool FOS, bool B2D>
+__device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const StageMeta& m,
+                                                const EncodeArgs& a, int r, int b0, float S_t,
+                                                float A_t,
+                                                uint32_t (&w)[NBOX][TileGeo<T>::BOXC / 8],
+                                                uint32_t (&sc)[NBOX]) {
+  using G = TileGeo<T>;
+  constexpr int NB = G::BOXC / 16;  // blocks per box row
+  const float S = a.row_scaled ? m.rowS[r] : S_t;
+  const float A = a.row_scaled ? m.rowA[r] : A_t;
+  const int sw = r & 7;
 #pragma unroll
-  for (int jb = 0; jb < G::NB_C; ++jb) {
-    const int rb = q * G::RQ + 16 * jb;
-    float x0[16], x1[16];
+  for (int bi = 0; bi < NBOX; ++bi) {
+    const int box = b0 + bi;
+    const uint8_t* rowp = stage + box * kBoxBytes + r * 128;
+    sc[bi] = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int j = 0; j < NB; ++j) {
+      float x[16];
+      float b;
       if constexpr (sizeof(T) == 2) {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(stage + soff<T>(rb + i, cl));
-        x0[i] = bf16_lo(v);
-        x1[i] = bf16_hi(v);
+        const uint4 v0 = lds128(rowp + (((2 * j) ^ sw) << 4));
+        const uint4 v1 = lds128(rowp + (((2 * j + 1) ^ sw) << 4));
+        const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[2 * i] = bf16_lo(u[i]);
+          x[2 * i + 1] = bf16_hi(u[i]);
+        }
+        b = B2D ? 0.0f : absmax8_bf16(v0, v1);
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(stage + soff<T>(rb + i, cl));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = lds128(rowp + (((4 * j + k) ^ sw) << 4));
+          x[4 * k] = __uint_as_float(v.x);
+          x[4 * k + 1] = __uint_as_float(v.y);
+          x[4 * k + 2] = __uint_as_float(v.z);
+          x[4 * k + 3] = __uint_as_float(v.w);
+        }
+        b = B2D ? 0.0f : absmax16_f32(x);
+      }
+      uint32_t s2 = 0;
+      float e2 = 0.0f;
+      if constexpr (B2D) {
+        const int sub = (r >> 4) * (G::TILEC / 16) + box * NB + j;
+        s2 = m.s2d[sub];
+        e2 = m.e2d[sub];
+      }
+      sc[bi] |= encode_block<FOS, B2D>(x, b, S, A, a.F_inv, s2, e2, w[bi][2 * j], w[bi][2 * j + 1])
+                << (8 * j);
+    }
+  }
+}
+
+// Direct stores of one row's codes and scales (no TMA for the outputs).
+template <typename T, int NBOX>
+__device__ __forceinline__ void rowwise_store(const EncodeArgs& a, int r, int b0, int tm, int tn,
+                                              const uint32_t (&w)[NBOX][TileGeo<T>::BOXC / 8],
+                                              const uint32_t (&sc)[NBOX], bool fast) {
+  using G = TileGeo<T>;
+  constexpr int NB = G::BOXC / 16;
+  const int64_t gr = (int64_t)tm * kTileRows + r;
+  if (gr >= a.M) return;
+#pragma unroll
+  for (int bi = 0; bi < NBOX; ++bi) {
+    const int64_t gc0 = (int64_t)tn * G::TILEC + (b0 + bi) * G::BOXC;
+    if (gc0 >= a.K) return;
+    uint8_t* cp = a.row_codes + gr * a.row_cpitch + gc0 / 2;
+    uint8_t* sp = a.row_scales + gr * a.row_spitch + gc0 / 16;
+    if (fast) {
+#pragma unroll
+      for (int q = 0; q < NB / 2; ++q)
+        stg_v4_cs(cp + 16 * q, make_uint4(w[bi][4 * q], w[bi][4 * q + 1], w[bi][4 * q + 2],
+                                          w[bi][4 * q + 3]));
+      if constexpr (NB == 4) stg_u32_keep(sp, sc[bi], policy_evict_last());
+      else stg_u16_keep(sp, sc[bi], policy_evict_last());
+    } else {
+      const int64_t rem = a.K - gc0;
+      const int ncols = rem < G::BOXC ? (int)rem : G::BOXC;
+      store_tail_words<2 * NB>(cp, w[bi], (ncols + 1) / 2);
+      store_tail(sp, (ncols + 15) / 16, sc[bi], 0, 0, 0, 0, 0, 0, 0);
+    }
+  }
+}
+
+// Scales only (the codes went out through the TMA store).
+template <typename T, int NBOX>
+__device__ __forceinline__ void rowwise_store_scales(const EncodeArgs& a, int r, int b0, int tm,
+                                                     int tn, const uint32_t (&sc)[NBOX],
+                                                     bool fast) {
+  using G = TileGeo<T>;
+  constexpr int NB = G::BOXC / 16;
+  const int64_t gr = (int64_t)tm * kTileRows + r;
+  if (gr >= a.M) return;
+  const int64_t gc0 = (int64_t)tn * G::TILEC + b0 * G::BOXC;
+  uint8_t* sp = a.row_scales + gr * a.row_spitch + gc0 / 16;
+  if (fast) {
+    const uint64_t keep = policy_evict_last();
+    if constexpr (NBOX == 2 && NB == 4) stg_v2_keep(sp, sc[0], sc[1], keep);
+    else if constexpr (NBOX == 1 && NB == 4) stg_u32_keep(sp, sc[0], keep);
+    else {
+#pragma unroll
+      for (int bi = 0; bi < NBOX; ++bi) stg_u16_keep(sp + 2 * bi, sc[bi], keep);
+    }
+  } else {
+#pragma unroll
+    for (int bi = 0; bi < NBOX; ++bi) {
+      const int64_t rem = a.K - (gc0 + bi * G::BOXC);
+      if (rem <= 0) return;
+      const int ncols = rem < G::BOXC ? (int)rem : G::BOXC;
+      store_tail(sp + bi * NB, (ncols + 15) / 16, sc[bi], 0, 0, 0, 0, 0, 0, 0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- columnwise
+
+// Codes and scales of column pair (cl, cl + 1) over rows [rb0, rb0 + RG).
+template <typename T, int RG, bool FOS, bool B2D>
+__device__ __forceinline__ void colwise_compute(const uint8_t* stage, const StageMeta& m,
+                                                const EncodeArgs& a, int cl, int rb0,
+                                                const uint32_t (&coff)[8], float S_t, float A_t,
+                                                uint32_t (&w0)[RG / 8], uint32_t (&w1)[RG / 8],
+                                                uint32_t& sc0, uint32_t& sc1) {
+  using G = TileGeo<T>;
+  constexpr int NB = RG / 16;
+  const float S0 = a.row_scaled ? m.colS[cl] : S_t;
+  const float S1 = a.row_scaled ? m.colS[cl + 1] : S_t;
+  const float A0 = a.row_scaled ? m.colA[cl] : A_t;
+  const float A1 = a.row_scaled ? m.colA[cl + 1] : A_t;
+  sc0 = sc1 = 0;
+#pragma unroll
+  for (int jb = 0; jb < NB; ++jb) {
+    const uint8_t* base = stage + (rb0 + 16 * jb) * 128;
+    float x0[16], x1[16];
+    float b0 = 0.0f, b1 = 0.0f;
+    if constexpr (sizeof(T) == 2) {
+      uint32_t v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = *reinterpret_cast<const uint32_t*>(base + i * 128 + coff[i & 7]);
+      if constexpr (!B2D) {
+        uint32_t t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = absmax_bf16x2(v[2 * i], v[2 * i + 1]);
+        uint32_t mm =
+            absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(t8[0], t8[1]), absmax_bf16x2(t8[2], t8[3])),
+                          absmax_bf16x2(absmax_bf16x2(t8[4], t8[5]), absmax_bf16x2(t8[6], t8[7])));
+        mm &= 0x7fff7fffu;
+        b0 = __uint_as_float(mm << 16);
+        b1 = __uint_as_float(mm & 0xffff0000u);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        x0[i] = bf16_lo(v[i]);
+        x1[i] = bf16_hi(v[i]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 v = *reinterpret_cast<const float2*>(base + i * 128 + coff[i & 7]);
         x0[i] = v.x;
         x1[i] = v.y;
       }
+      if constexpr (!B2D) {
+        b0 = absmax16_f32(x0);
+        b1 = absmax16_f32(x1);
+      }
     }
-    uint32_t s8s = 0;
-    float e2 = 0.f;
+    uint32_t s2 = 0;
+    float e2 = 0.0f;
     if constexpr (B2D) {
-      const int sub = (rb >> 4) * G::SUBC + cl / 16;
-      s8s = s2d_s8[sub];
-      e2 = s2d_e[sub];
+      const int sub = ((rb0 >> 4) + jb) * (G::TILEC / 16) + cl / 16;
+      s2 = m.s2d[sub];
+      e2 = m.e2d[sub];
     }
-    sc0 |= encode_block<T, B2D>(x0, S0, a0, a.F_inv, FOS, s8s, e2, w0[2 * jb], w0[2 * jb + 1])
+    sc0 |= encode_block<FOS, B2D>(x0, b0, S0, A0, a.F_inv, s2, e2, w0[2 * jb], w0[2 * jb + 1])
            << (8 * jb);
-    sc1 |= encode_block<T, B2D>(x1, S1, a1, a.F_inv, FOS, s8s, e2, w1[2 * jb], w1[2 * jb + 1])
+    sc1 |= encode_block<FOS, B2D>(x1, b1, S1, A1, a.F_inv, s2, e2, w1[2 * jb], w1[2 * jb + 1])
            << (8 * jb);
-  }
-  const int64_t rem_r = a.M - gr0;
-  const int nrows = rem_r < G::RQ ? (int)rem_r : G::RQ;
-  const int nbytes = (int)((nrows + 1) / 2);
-  const int nsc = (int)((nrows + 15) / 16);
-  store_bytes(a.col_codes + gc * a.col_cpitch + gr0 / 2, w0, nbytes);
-  store_bytes(a.col_scales + gc * a.col_spitch + gr0 / 16, &sc0, nsc);
-  if (has1) {
-    store_bytes(a.col_codes + (gc + 1) * a.col_cpitch + gr0 / 2, w1, nbytes);
-    store_bytes(a.col_scales + (gc + 1) * a.col_spitch + gr0 / 16, &sc1, nsc);
   }
 }
 
-// 16x16 blocks: one thread per sub-tile picks its scale (and, with
-// four-over-six, its target by the error summed in row-major order).
+// Scales of a column pair (and, unless the codes went out through TMA, codes).
+template <typename T, int RG, bool CODES>
+__device__ __forceinline__ void colwise_store(const EncodeArgs& a, int cl, int rb0, int tm, int tn,
+                                              const uint32_t (&w0)[RG / 8],
+                                              const uint32_t (&w1)[RG / 8], uint32_t sc0,
+                                              uint32_t sc1, bool fast) {
+  using G = TileGeo<T>;
+  constexpr int NB = RG / 16;
+  const int64_t gc = (int64_t)tn * G::TILEC + cl;
+  const int64_t gr0 = (int64_t)tm * kTileRows + rb0;
+  if (gc >= a.K || gr0 >= a.M) return;
+  const bool has1 = gc + 1 < a.K;
+  uint8_t* c0p = a.col_codes + gc * a.col_cpitch + gr0 / 2;
+  uint8_t* s0p = a.col_scales + gc * a.col_spitch + gr0 / 16;
+  if (fast) {
+    if constexpr (CODES) {
+      if constexpr (NB == 1) {
+        stg_v2_cs(c0p, w0[0], w0[1]);
+        stg_v2_cs(c0p + a.col_cpitch, w1[0], w1[1]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < NB / 2; ++q) {
+          stg_v4_cs(c0p + 16 * q,
+                    make_uint4(w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]));
+          stg_v4_cs(c0p + a.col_cpitch + 16 * q,
+                    make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]));
+        }
+      }
+    }
+    const uint64_t keep = policy_evict_last();
+    if constexpr (NB == 4) {
+      stg_u32_keep(s0p, sc0, keep);
+      stg_u32_keep(s0p + a.col_spitch, sc1, keep);
+    } else if constexpr (NB == 2) {
+      stg_u16_keep(s0p, sc0, keep);
+      stg_u16_keep(s0p + a.col_spitch, sc1, keep);
+    } else {
+      s0p[0] = (uint8_t)sc0;
+      s0p[a.col_spitch] = (uint8_t)sc1;
+    }
+  } else {
+    const int64_t rem = a.M - gr0;
+    const int nrows = rem < RG ? (int)rem : RG;
+    const int nbytes = (nrows + 1) / 2, nsc = (nrows + 15) / 16;
+    if constexpr (CODES) store_tail_words<2 * NB>(c0p, w0, nbytes);
+    store_tail(s0p, nsc, sc0, 0, 0, 0, 0, 0, 0, 0);
+    if (has1) {
+      if constexpr (CODES) store_tail_words<2 * NB>(c0p + a.col_cpitch, w1, nbytes);
+      store_tail(s0p + a.col_spitch, nsc, sc1, 0, 0, 0, 0, 0, 0, 0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- 16x16 sub-tiles
+
+// One consumer thread per 16x16 sub-tile picks its scale (with four-over-six:
+// its target, by the error summed in row-major order inside the sub-tile).
 template <typename T, bool FOS>
-__device__ __forceinline__ void subtile_scales(const uint8_t* stage, const QuantKernelArgs& a,
-                                               float S, float amax, uint32_t* s2d_s8,
-                                               float* s2d_e) {
-  using G = Geo<T>;
-  const int tid = threadIdx.x;
-  if (tid >= G::NSUB) return;
-  const int sr = tid / G::SUBC, sc = tid % G::SUBC;
-  constexpr int CH = 16 * (int)sizeof(T) / 16;
+__device__ __forceinline__ void subtile_scales(const uint8_t* stage, StageMeta& m, float S,
+                                               float amax, float F_inv, int t) {
+  using G = TileGeo<T>;
+  constexpr int SUBC = G::TILEC / 16, NSUB = (kTileRows / 16) * SUBC;
+  if (t >= NSUB) return;
+  const int sr = t / SUBC, sc = t % SUBC;
+  constexpr int CH = (int)sizeof(T);  // 16-byte chunks per 16 values (2 or 4)
+  const int box = (sc * 16) / G::BOXC;
+  const int cb = ((sc * 16) % G::BOXC) * (int)sizeof(T) / 16;
   auto load_row = [&](int i, float* x) {
     const int r = sr * 16 + i;
-    const uint8_t* rowp = stage + ((sc * 16) / G::BOXC) * kBoxBytes + r * 128;
-    const int cb = ((sc * 16) % G::BOXC) * (int)sizeof(T) / 16;  // first chunk in the box row
-    uint4 v[4];
+    const uint8_t* rowp = stage + box * kBoxBytes + r * 128;
 #pragma unroll
-    for (int k = 0; k < CH; ++k) v[k] = lds128(rowp + ((((cb + k) ^ (r & 7))) << 4));
-    unpack16<T>(v[0], v[1], CH > 2 ? v[2] : v[0], CH > 2 ? v[3] : v[0], x);
+    for (int k = 0; k < CH; ++k) {
+      const uint4 v = lds128(rowp + ((((cb + k) ^ (r & 7))) << 4));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (sizeof(T) == 2) {
+          x[8 * k + 2 * q] = bf16_lo(u[q]);
+          x[8 * k + 2 * q + 1] = bf16_hi(u[q]);
+        } else {
+          x[4 * k + q] = __uint_as_float(u[q]);
+        }
+      }
+    }
   };
   float b = 0.0f;
   for (int i = 0; i < 16; ++i) {
     float x[16];
     load_row(i, x);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) b = fmaxf(b, fabsf(x[k]));
+    b = fmaxf(b, absmax16_f32(x));
   }
   BlockEnc e6 = block_encode<6>(b, S);
   if constexpr (FOS) {
     BlockEnc e4 = block_encode<4>(b, S);
-    const float D6 = dequant_factor(e6.sd, amax, a.F_inv);
-    const float D4 = dequant_factor(e4.sd, amax, a.F_inv);
+    const float D6 = dequant_factor(e6.sd, amax, F_inv);
+    const float D4 = dequant_factor(e4.sd, amax, F_inv);
     float err6 = 0.0f, err4 = 0.0f;
     for (int i = 0; i < 16; ++i) {
       float x[16];
       load_row(i, x);
-      uint32_t c[4];
-      c[0] = e2m1x8(__fmul_rn(x[0], e6.e), __fmul_rn(x[1], e6.e), __fmul_rn(x[2], e6.e),
-                    __fmul_rn(x[3], e6.e), __fmul_rn(x[4], e6.e), __fmul_rn(x[5], e6.e),
-                    __fmul_rn(x[6], e6.e), __fmul_rn(x[7], e6.e));
-      c[1] = e2m1x8(__fmul_rn(x[8], e6.e), __fmul_rn(x[9], e6.e), __fmul_rn(x[10], e6.e),
-                    __fmul_rn(x[11], e6.e), __fmul_rn(x[12], e6.e), __fmul_rn(x[13], e6.e),
-                    __fmul_rn(x[14], e6.e), __fmul_rn(x[15], e6.e));
-      c[2] = e2m1x8(__fmul_rn(x[0], e4.e), __fmul_rn(x[1], e4.e), __fmul_rn(x[2], e4.e),
-                    __fmul_rn(x[3], e4.e), __fmul_rn(x[4], e4.e), __fmul_rn(x[5], e4.e),
-                    __fmul_rn(x[6], e4.e), __fmul_rn(x[7], e4.e));
-      c[3] = e2m1x8(__fmul_rn(x[8], e4.e), __fmul_rn(x[9], e4.e), __fmul_rn(x[10], e4.e),
-                    __fmul_rn(x[11], e4.e), __fmul_rn(x[12], e4.e), __fmul_rn(x[13], e4.e),
-                    __fmul_rn(x[14], e4.e), __fmul_rn(x[15], e4.e));
-      err6 = sse8(sse8(err6, x, c[0], D6), x + 8, c[1], D6);
-      err4 = sse8(sse8(err4, x, c[2], D4), x + 8, c[3], D4);
+      uint32_t c0, c1, d0, d1;
+      codes16(x, e6.e, c0, c1);
+      codes16(x, e4.e, d0, d1);
+      err6 = sse8(sse8(err6, x, c0, D6), x + 8, c1, D6);
+      err4 = sse8(sse8(err4, x, d0, D4), x + 8, d1, D4);
     }
     if (err4 < err6) e6 = e4;
   }
-  s2d_s8[tid] = e6.s8;
-  s2d_e[tid] = e6.e;
+  m.s2d[t] = e6.s8;
+  m.e2d[t] = e6.e;
 }
 
 // ---------------------------------------------------------------- the kernel
 
-template <typename T, bool ROW, bool COL, bool FOS, bool B2D, bool TMA>
-__global__ void __launch_bounds__(kThreads, 2)
-    k_quantize(const __grid_constant__ CUtensorMap tmap, QuantKernelArgs a) {
-  using G = Geo<T>;
+// Staging bytes per consumer warp for the TMA stores of its codes.
+constexpr int kStagingPerWarp = 2048;
+
+template <bool TOUT>
+struct EncodeSmem {
+  static constexpr int kStagesUsed = TOUT ? 2 : 3;
+  static constexpr int kBytes =
+      kStagesUsed * kTileBytes + (TOUT ? kConsumerWarps * kStagingPerWarp : 0) + 1024;
+};
+
+// TOUT: codes leave through per-warp shared-memory staging and TMA tensor stores
+// (full lines instead of one 16-byte partial sector per thread); the ring then
+// has 2 stages so that 2 CTAs still fit on an SM.
+template <typename T, bool ROW, bool COL, bool FOS, bool B2D, bool TMA, bool TOUT>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+    k_encode(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap map_rc,
+             const __grid_constant__ CUtensorMap map_cc, EncodeArgs a) {
+  using G = TileGeo<T>;
+  constexpr int NS = EncodeSmem<TOUT>::kStagesUsed;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[kStages];
-  __shared__ uint32_t s2d_s8[B2D ? G::NSUB : 1];
-  __shared__ float s2d_e[B2D ? G::NSUB : 1];
+  __shared__ __align__(8) uint64_t full[NS];
+  __shared__ __align__(8) uint64_t empty[NS];
+  __shared__ StageMeta meta[NS];
+  __shared__ volatile int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   if (noop_set(a.noop)) return;
   if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) return;
-  const int tid = threadIdx.x;
-  if (blockIdx.x == 0 && tid == 0 && a.copy_dst != nullptr) *a.copy_dst = *a.copy_src;
-
-  const int64_t G_ = gridDim.x;
-  const int64_t first = blockIdx.x;
-  if (first >= a.num_tiles) return;
-  const int64_t count = (a.num_tiles - first + G_ - 1) / G_;
-  auto tile_of = [&](int64_t k) { return a.num_tiles - 1 - (first + k * G_); };
-
-  // per-tensor scales, one per direction (16x16 blocks share the rowwise one:
-  // the host launches the directions separately when their amax sources differ)
-  const float amax_r = (ROW && !a.row_scaled) ? a.row_amax[0] : 0.0f;
-  const float amax_c = (COL && !a.row_scaled) ? a.col_amax[0] : 0.0f;
-  const float S_row = a.row_scaled ? 1.0f : global_scale(amax_r, a.F);
-  const float S_col = a.row_scaled ? 1.0f : global_scale(amax_c, a.F);
-  const float amax_2d = ROW ? amax_r : amax_c;
-  const float S_2d = ROW ? S_row : S_col;
-
-  uint64_t policy = 0;
-  if constexpr (TMA) {
-    policy = policy_evict_first();
-    if (tid == 0) {
-      prefetch_tmap(&tmap);
-      for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-      fence_mbar_init();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int begin, end;
+  a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
+  const int count = end - begin;
+  const bool fwd = (blockIdx.x & 1) != 0;  // the amax kernel walks this chunk the other way
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 2);  // producer: TMA arrival (with bytes) + staged-meta arrival
+      mbar_init(&empty[s], kConsumerWarps);
     }
-    __syncthreads();
-    if (tid == 0) {
-      for (int s = 0; s < kStages && s < count; ++s) {
-        const int64_t t = tile_of(s);
-        const int32_t y = (int32_t)((t / a.tiles_n) * kTileRows);
-        const int32_t x0 = (int32_t)((t % a.tiles_n) * G::TILEC);
-        uint8_t* dst = smem + s * kStageBytes;
-        mbar_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(dst, &tmap, &full[s], x0, y, policy);
-        tma_load_2d(dst + kBoxBytes, &tmap, &full[s], x0 + G::BOXC, y, policy);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (count <= 0) return;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp
+    const uint64_t policy = policy_evict_first();
+    if (TMA && lane == 0) prefetch_tmap(&tmap);
+    auto issue = [&](int k) {
+      int tm, tn;
+      a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+      uint8_t* stage = smem + (k % NS) * kTileBytes;
+      if constexpr (TMA) {
+        if (lane == 0) issue_tile<T>(stage, &tmap, &full[k % NS], tm, tn, policy);
+      } else {
+        plain_load_tile<T>(stage, static_cast<const T*>(a.x), a.M, a.K, tm, tn, lane);
+      }
+    };
+    // the ring starts empty: fill it before waiting for the amax values
+    for (int k = 0; k < NS && k < count; ++k) issue(k);
+    pdl_wait();  // the amax values come from the preceding kernel
+    constexpr int RPL = kTileRows / 32, CPL = G::TILEC / 32;  // rows / columns per lane
+    const bool rs = a.row_scaled != 0;
+    // amax of a tile's rows and columns, loaded one tile ahead so that their L2
+    // latency overlaps the wait for the next free stage
+    float ra[RPL], ca[CPL];
+    auto load_amax = [&](int k, float (&r_)[RPL], float (&c_)[CPL]) {
+      int tm, tn;
+      a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+      if (ROW) {
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+          const int64_t gr = (int64_t)tm * kTileRows + lane + 32 * i;
+          r_[i] = gr < a.M ? a.row_amax[gr] : 0.0f;
+        }
+      }
+      if (COL) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int64_t gc = (int64_t)tn * G::TILEC + lane + 32 * i;
+          c_[i] = gc < a.K ? a.col_amax[gc] : 0.0f;
+        }
+      }
+    };
+    if (rs) load_amax(0, ra, ca);
+    int issued = count < NS ? count : NS;
+    for (int k = 0; k < count; ++k) {
+      const int s = k % NS;
+      if (k >= NS) {
+        const bool ok = mbar_wait_bounded(&empty[s], (uint32_t)(((k / NS) - 1) & 1));
+        if (!ok || abort_flag) {
+          if (lane == 0 && !ok) {
+            abort_flag = 1;
+            raise_status(a.status, kStatusTimeout);
+          }
+          break;
+        }
+        issue(k);
+        issued = k + 1;
+      }
+      if (rs) {
+        float rn[RPL], cn[CPL];
+        if (k + 1 < count) load_amax(k + 1, rn, cn);
+        StageMeta& m = meta[s];
+        if (ROW) {
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) {
+            m.rowA[lane + 32 * i] = ra[i];
+            m.rowS[lane + 32 * i] = global_scale(ra[i], a.F);
+          }
+        }
+        if (COL) {
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            m.colA[lane + 32 * i] = ca[i];
+            m.colS[lane + 32 * i] = global_scale(ca[i], a.F);
+          }
+        }
+        if (k + 1 < count) {
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) ra[i] = rn[i];
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) ca[i] = cn[i];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (!TMA) mbar_arrive(&full[s]);  // stands in for the TMA arrival
+        mbar_arrive(&full[s]);
       }
     }
+    // let copies still in flight land before the CTA's shared memory is released
+    if (abort_flag && lane == 0)
+      for (int k = issued - NS > 0 ? issued - NS : 0; k < issued; ++k)
+        (void)mbar_wait_bounded(&full[k % NS], (uint32_t)((k / NS) & 1));
+    return;
   }
 
-  for (int64_t k = 0; k < count; ++k) {
-    const int s = (int)(k % kStages);
-    const int64_t t = tile_of(k);
-    const int64_t tm = t / a.tiles_n, tn = t % a.tiles_n;
-    uint8_t* stage = smem + s * kStageBytes;
-    if constexpr (TMA) {
-      const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / kStages) & 1));
-      if (__syncthreads_or(!ok)) {
-        if (tid == 0) {
-          raise_status(a.status, kStatusTimeout);
-          // let the copies already issued land before this CTA's memory is released
-          for (int64_t j = k + 1; j < count && j < k + kStages; ++j)
-            (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
-        }
-        __syncthreads();
-        return;
-      }
-    } else {
-      // plain loads into the same swizzled layout (x rows not 16-byte aligned)
-      const T* x = static_cast<const T*>(a.x);
-      for (int idx = tid; idx < kTileRows * G::TILEC; idx += kThreads) {
-        const int r = idx / G::TILEC, c = idx % G::TILEC;
-        const int64_t gr = tm * kTileRows + r, gc = tn * G::TILEC + c;
-        T v = T(0);
-        if (gr < a.M && gc < a.K) v = x[gr * a.K + gc];
-        *reinterpret_cast<T*>(stage + soff<T>(r, c)) = v;
-      }
-      __syncthreads();
+  // ---------------- consumer warps
+  pdl_wait();
+  float S_r = 1.0f, A_r = 0.0f, S_c = 1.0f, A_c = 0.0f;
+  if (!a.row_scaled) {
+    if (ROW) {
+      A_r = a.row_amax[0];
+      S_r = global_scale(A_r, a.F);
     }
+    if (COL) {
+      A_c = a.col_amax[0];
+      S_c = global_scale(A_c, a.F);
+    }
+    if (blockIdx.x == 0 && tid == 0 && a.copy_dst != nullptr) *a.copy_dst = *a.copy_src;
+  }
+  constexpr bool BOTH = ROW && COL;
+  constexpr int NBOX = BOTH ? 2 : 1;          // boxes per rowwise thread
+  constexpr int NP = G::TILEC / 2;            // column pairs per tile
+  constexpr int NCT = BOTH ? 128 : 256;       // columnwise threads
+  constexpr int RG = kTileRows / (NCT / NP);  // rows per columnwise thread
+  constexpr int RWB = NBOX * G::BOXC / 2;     // code bytes per rowwise thread (TMA box width)
+  constexpr int CWB = RG / 2;                 // code bytes per column (TMA box width)
+  const bool is_row = ROW && (!BOTH || tid < 128);
+  const int ct = BOTH ? tid - 128 : tid;      // columnwise thread index
+  const int cl = 2 * (ct % NP), rb0 = (ct / NP) * RG;
+  const int r = BOTH ? tid : (tid & 127), b0 = BOTH ? 0 : (tid >> 7);
+  uint32_t coff[8];
+  {
+    const int box = cl / G::BOXC, byte = (cl % G::BOXC) * (int)sizeof(T);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      coff[k] = box * kBoxBytes + ((((byte >> 4) ^ k)) << 4) + (byte & 15);
+  }
+  uint8_t* staging = smem + NS * kTileBytes + warp * kStagingPerWarp;
+  const uint64_t out_policy = policy_evict_first();
+  for (int k = 0; k < count; ++k) {
+    const int s = k % NS;
+    int tm, tn;
+    a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / NS) & 1));
+    if (!ok) {
+      abort_flag = 1;
+      if (lane == 0) raise_status(a.status, kStatusTimeout);
+    }
+    if constexpr (B2D) consumer_sync();  // every consumer sees the same abort decision
+    if (abort_flag) break;
+    const uint8_t* stage = smem + s * kTileBytes;
+    StageMeta& m = meta[s];
+    const bool fast = a.vec_ok && tm < a.full_m && tn < a.full_n;
     if constexpr (B2D) {
-      subtile_scales<T, FOS>(stage, a, S_2d, amax_2d, s2d_s8, s2d_e);
-      __syncthreads();
+      subtile_scales<T, FOS>(stage, m, ROW ? S_r : S_c, ROW ? A_r : A_c, a.F_inv, tid);
+      consumer_sync();
     }
-    if constexpr (ROW) rowwise_tile<T, FOS, B2D>(stage, a, tm, tn, S_row, s2d_s8, s2d_e);
-    if constexpr (COL) colwise_tile<T, FOS, B2D>(stage, a, tm, tn, S_col, s2d_s8, s2d_e);
-    __syncthreads();  // stage s is free again
-    if constexpr (TMA) {
-      if (tid == 0 && k + kStages < count) {
-        const int64_t t2 = tile_of(k + kStages);
-        const int32_t y = (int32_t)((t2 / a.tiles_n) * kTileRows);
-        const int32_t x0 = (int32_t)((t2 % a.tiles_n) * G::TILEC);
-        mbar_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(stage, &tmap, &full[s], x0, y, policy);
-        tma_load_2d(stage + kBoxBytes, &tmap, &full[s], x0 + G::BOXC, y, policy);
+    if (is_row) {
+      uint32_t w[NBOX][G::BOXC / 8];
+      uint32_t sc[NBOX];
+      rowwise_compute<T, NBOX, FOS, B2D>(stage, m, a, r, b0, S_r, A_r, w, sc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done reading the stage
+      if constexpr (TOUT) {
+        if (lane == 0) bulk_wait_read();  // the previous tile's store has left the staging
+        __syncwarp();
+        uint8_t* dst = staging + lane * RWB;
+#pragma unroll
+        for (int bi = 0; bi < NBOX; ++bi)
+#pragma unroll
+          for (int q = 0; q < G::BOXC / 32; ++q)
+            sts_v4(dst + bi * (G::BOXC / 2) + 16 * q, w[bi][4 * q], w[bi][4 * q + 1],
+                   w[bi][4 * q + 2], w[bi][4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_rc, staging, tn * (G::TILEC / 2) + b0 * (G::BOXC / 2),
+                       tm * kTileRows + (r & ~31), out_policy);
+          bulk_commit();
+        }
+        rowwise_store_scales<T, NBOX>(a, r, b0, tm, tn, sc, fast);
+      } else {
+        rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, fast);
       }
+    } else if (COL) {
+      uint32_t w0[RG / 8], w1[RG / 8];
+      uint32_t sc0, sc1;
+      colwise_compute<T, RG, FOS, B2D>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1, sc0, sc1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if constexpr (TOUT) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        uint8_t* dst = staging + lane * 2 * CWB;
+#pragma unroll
+        for (int q = 0; q < CWB / 16; ++q) {
+          sts_v4(dst + 16 * q, w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]);
+          sts_v4(dst + CWB + 16 * q, w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_cc, staging, (tm * kTileRows + rb0) / 2,
+                       tn * G::TILEC + (cl & ~63), out_policy);
+          bulk_commit();
+        }
+      }
+      colwise_store<T, RG, !TOUT>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, fast);
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
+  }
+  if constexpr (TOUT) {
+    if (lane == 0) bulk_wait_all();
   }
 }
 
-using QuantFn = void (*)(const CUtensorMap, QuantKernelArgs);
+using EncodeFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, EncodeArgs);
 
 template <typename T, bool ROW, bool COL, bool FOS, bool B2D>
-QuantFn pick_tma(bool tma) {
-  return tma ? k_quantize<T, ROW, COL, FOS, B2D, true> : k_quantize<T, ROW, COL, FOS, B2D, false>;
+EncodeFn pick_io(bool tma, bool tout) {
+  if constexpr (sizeof(T) == 2) {
+    if (tma && tout) return k_encode<T, ROW, COL, FOS, B2D, true, true>;
+  }
+  return tma ? k_encode<T, ROW, COL, FOS, B2D, true, false>
+             : k_encode<T, ROW, COL, FOS, B2D, false, false>;
 }
 
 template <typename T, bool ROW, bool COL>
-QuantFn pick_mode(bool fos, bool b2d, bool tma) {
-  if (b2d) return fos ? pick_tma<T, ROW, COL, true, true>(tma) : pick_tma<T, ROW, COL, false, true>(tma);
-  return fos ? pick_tma<T, ROW, COL, true, false>(tma) : pick_tma<T, ROW, COL, false, false>(tma);
+EncodeFn pick_mode(bool fos, bool b2d, bool tma, bool tout) {
+  if (b2d)
+    return fos ? pick_io<T, ROW, COL, true, true>(tma, tout) : pick_io<T, ROW, COL, false, true>(tma, tout);
+  return fos ? pick_io<T, ROW, COL, true, false>(tma, tout) : pick_io<T, ROW, COL, false, false>(tma, tout);
 }
 
 template <typename T>
-QuantFn pick_dir(bool row, bool col, bool fos, bool b2d, bool tma) {
-  if (row && col) return pick_mode<T, true, true>(fos, b2d, tma);
-  if (row) return pick_mode<T, true, false>(fos, b2d, tma);
-  return pick_mode<T, false, true>(fos, b2d, tma);
+EncodeFn pick_dir(bool row, bool col, bool fos, bool b2d, bool tma, bool tout) {
+  if (row && col) return pick_mode<T, true, true>(fos, b2d, tma, tout);
+  if (row) return pick_mode<T, true, false>(fos, b2d, tma, tout);
+  return pick_mode<T, false, true>(fos, b2d, tma, tout);
 }
 
+bool aligned(const void* p, int n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
+
 }  // namespace
+
+int pipe_grid_size(int64_t num_tiles, int num_sms) {
+  return (int)std::min<int64_t>(num_tiles, 2LL * num_sms);
+}
 
 cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
   const bool row = q.row_codes != nullptr, col = q.col_codes != nullptr;
   if (!row && !col) return cudaSuccess;
   const bool bf16 = q.in == InType::BF16;
-  const int box_cols = bf16 ? Geo<uint16_t>::BOXC : Geo<float>::BOXC;
+  const int box_cols = bf16 ? TileGeo<uint16_t>::BOXC : TileGeo<float>::BOXC;
   const int tile_cols = 2 * box_cols;
-  QuantKernelArgs a{};
+  EncodeArgs a{};
   a.x = q.x;
   a.M = q.M;
   a.K = q.K;
-  a.tiles_n = (q.K + tile_cols - 1) / tile_cols;
-  a.num_tiles = ((q.M + kTileRows - 1) / kTileRows) * a.tiles_n;
+  a.grid.tiles_m = (int)((q.M + kTileRows - 1) / kTileRows);
+  a.grid.tiles_n = (int)((q.K + tile_cols - 1) / tile_cols);
+  a.grid.num_tiles = a.grid.tiles_m * a.grid.tiles_n;
+  a.full_m = (int)(q.M / kTileRows);
+  a.full_n = (int)(q.K / tile_cols);
   a.row_codes = q.row_codes;
   a.row_scales = q.row_scales;
   a.row_amax = q.row_amax;
@@ -437,19 +734,50 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.status = dev.status;
   a.ends = q.group_ends;
   a.G = q.num_groups;
-  if (a.num_tiles == 0) return cudaSuccess;
+  if (a.grid.num_tiles == 0) return cudaSuccess;
 
-  CUtensorMap map;
+  CUtensorMap map, map_rc, map_cc;
+  memset(&map_rc, 0, sizeof(map_rc));
+  memset(&map_cc, 0, sizeof(map_cc));
   const bool tma = make_tile_map(&map, q.x, q.in, q.M, q.K, box_cols, kTileRows);
   if (!tma) memset(&map, 0, sizeof(map));
-  QuantFn fn = bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma)
-                    : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma);
-  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+  // TMA stores of the codes (BF16 input): box = one consumer warp's codes
+  const bool both = row && col;
+  bool tout = bf16 && tma;
+  if (tout && row)
+    tout = make_byte_map(&map_rc, q.row_codes, q.M, a.row_cpitch, both ? 64 : 32, 32);
+  if (tout && col)
+    tout = make_byte_map(&map_cc, q.col_codes, q.K, a.col_cpitch, both ? 32 : 16, 64);
+  // aligned vector stores on interior tiles
+  const int rows_per_col_thread = bf16 ? (both ? 64 : 32) : (both ? 32 : 16);
+  const int row_scale_bytes = (bf16 ? 4 : 2) * ((tout && both) ? 2 : 1);
+  bool vec = true;
+  if (row)
+    vec = vec && (tout || (a.row_cpitch % 16 == 0 && aligned(q.row_codes, 16))) &&
+          a.row_spitch % row_scale_bytes == 0 && aligned(q.row_scales, row_scale_bytes);
+  if (col) {
+    const int cs = std::max(1, rows_per_col_thread / 16);
+    vec = vec && (tout || (a.col_cpitch % 16 == 0 && aligned(q.col_codes, 16))) &&
+          a.col_spitch % cs == 0 && aligned(q.col_scales, cs);
+  }
+  a.vec_ok = vec ? 1 : 0;
+
+  EncodeFn fn = bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, tout)
+                     : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, tout);
+  const int smem = tout ? EncodeSmem<true>::kBytes : EncodeSmem<false>::kBytes;
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const int64_t grid = std::min<int64_t>(a.num_tiles, 2LL * dev.num_sms);
-  fn<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(map, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pipe_grid_size(a.grid.num_tiles, dev.num_sms));
+  cfg.blockDim = dim3(kPipeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, map, map_rc, map_cc, a);
 }
 
 }  // namespace nvfp4
