@@ -136,8 +136,8 @@ struct BlockEnc {
 
 template <int T>
 __device__ __forceinline__ BlockEnc block_encode(float b, float S) {
-  float q = (T == 4) ? __fmul_rn(b, 0.25f) : __fdiv_rn(b, (float)T);  // b/4 == b*0.25 exactly
-  float s32 = __fmul_rn(q, S);
+  const float q = (T == 4) ? __fmul_rn(b, 0.25f) : __fdiv_rn(b, (float)T);  // b/4 == b*0.25 exactly
+  const float s32 = __fmul_rn(q, S);
   BlockEnc r;
   r.s8 = e4m3_byte(s32);
   r.sd = e4m3_value(r.s8);
@@ -148,6 +148,26 @@ __device__ __forceinline__ BlockEnc block_encode(float b, float S) {
 // Dequantize factor (decode(s8) * a) * F_inv of a block.
 __device__ __forceinline__ float dequant_factor(float sd, float a, float F_inv) {
   return __fmul_rn(__fmul_rn(sd, a), F_inv);
+}
+
+// Two IEEE round-to-nearest products with one packed FP32x2 multiply (sm_100+):
+// (ra, rb) = (fl(a * e), fl(b * e)), each rounded exactly like __fmul_rn.
+__device__ __forceinline__ void mul2_rn(float a, float b, float e, float& ra, float& rb) {
+  asm("{\n\t.reg .b64 t, u, v;\n\t"
+      "mov.b64 t, {%2, %3};\n\t"
+      "mov.b64 u, {%4, %4};\n\t"
+      "mul.rn.f32x2 v, t, u;\n\t"
+      "mov.b64 {%0, %1}, v;\n\t}"
+      : "=f"(ra), "=f"(rb)
+      : "f"(a), "f"(b), "f"(e));
+}
+
+// Eight codes of x[0..7] scaled by e (products via packed multiplies).
+__device__ __forceinline__ uint32_t codes8(const float* x, float e) {
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) mul2_rn(x[2 * i], x[2 * i + 1], e, y[2 * i], y[2 * i + 1]);
+  return e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 
 // Running squared error over 8 values and their 8 codes (packed), in order.
@@ -171,26 +191,18 @@ template <bool FOS>
 __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S, float a,
                                                float F_inv, uint32_t& c0, uint32_t& c1) {
   BlockEnc e6 = block_encode<6>(b, S);
-  c0 = e2m1x8(__fmul_rn(x[0], e6.e), __fmul_rn(x[1], e6.e), __fmul_rn(x[2], e6.e),
-              __fmul_rn(x[3], e6.e), __fmul_rn(x[4], e6.e), __fmul_rn(x[5], e6.e),
-              __fmul_rn(x[6], e6.e), __fmul_rn(x[7], e6.e));
-  c1 = e2m1x8(__fmul_rn(x[8], e6.e), __fmul_rn(x[9], e6.e), __fmul_rn(x[10], e6.e),
-              __fmul_rn(x[11], e6.e), __fmul_rn(x[12], e6.e), __fmul_rn(x[13], e6.e),
-              __fmul_rn(x[14], e6.e), __fmul_rn(x[15], e6.e));
+  c0 = codes8(x, e6.e);
+  c1 = codes8(x + 8, e6.e);
   if constexpr (!FOS) {
     return e6.s8;
   } else {
     BlockEnc e4 = block_encode<4>(b, S);
-    uint32_t d0 = e2m1x8(__fmul_rn(x[0], e4.e), __fmul_rn(x[1], e4.e), __fmul_rn(x[2], e4.e),
-                         __fmul_rn(x[3], e4.e), __fmul_rn(x[4], e4.e), __fmul_rn(x[5], e4.e),
-                         __fmul_rn(x[6], e4.e), __fmul_rn(x[7], e4.e));
-    uint32_t d1 = e2m1x8(__fmul_rn(x[8], e4.e), __fmul_rn(x[9], e4.e), __fmul_rn(x[10], e4.e),
-                         __fmul_rn(x[11], e4.e), __fmul_rn(x[12], e4.e), __fmul_rn(x[13], e4.e),
-                         __fmul_rn(x[14], e4.e), __fmul_rn(x[15], e4.e));
-    float D6 = dequant_factor(e6.sd, a, F_inv);
-    float D4 = dequant_factor(e4.sd, a, F_inv);
-    float err6 = sse8(sse8(0.0f, x, c0, D6), x + 8, c1, D6);
-    float err4 = sse8(sse8(0.0f, x, d0, D4), x + 8, d1, D4);
+    const uint32_t d0 = codes8(x, e4.e);
+    const uint32_t d1 = codes8(x + 8, e4.e);
+    const float D6 = dequant_factor(e6.sd, a, F_inv);
+    const float D4 = dequant_factor(e4.sd, a, F_inv);
+    const float err6 = sse8(sse8(0.0f, x, c0, D6), x + 8, c1, D6);
+    const float err4 = sse8(sse8(0.0f, x, d0, D4), x + 8, d1, D4);
     if (err4 < err6) {
       c0 = d0;
       c1 = d1;
@@ -202,10 +214,8 @@ __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S,
 
 // Codes of 16 values with a given encode factor (16x16 blocks: the tile's scale).
 __device__ __forceinline__ void codes16(const float* x, float e, uint32_t& c0, uint32_t& c1) {
-  c0 = e2m1x8(__fmul_rn(x[0], e), __fmul_rn(x[1], e), __fmul_rn(x[2], e), __fmul_rn(x[3], e),
-              __fmul_rn(x[4], e), __fmul_rn(x[5], e), __fmul_rn(x[6], e), __fmul_rn(x[7], e));
-  c1 = e2m1x8(__fmul_rn(x[8], e), __fmul_rn(x[9], e), __fmul_rn(x[10], e), __fmul_rn(x[11], e),
-              __fmul_rn(x[12], e), __fmul_rn(x[13], e), __fmul_rn(x[14], e), __fmul_rn(x[15], e));
+  c0 = codes8(x, e);
+  c1 = codes8(x + 8, e);
 }
 
 // ---------------------------------------------------------------- mbarrier / TMA
@@ -290,6 +300,11 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// wait until at most N committed bulk-store groups are still reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_allow() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 // wait until the committed bulk stores are complete
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -340,6 +355,13 @@ __device__ __forceinline__ void sts_v4(void* p, uint32_t a, uint32_t b, uint32_t
 __device__ __forceinline__ void sts_v2(void* p, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_addr(p)), "r"(a), "r"(b) : "memory");
 }
+// One full 32-byte sector per thread (256-bit store, sm_100+); p 32-byte aligned.
+__device__ __forceinline__ void stg_v8_cs(void* p, const uint32_t* w) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Stores that should stay in L2 until their 32-byte sector is complete (scale
 // bytes written in pieces by consecutive tiles).
 __device__ __forceinline__ void stg_v2_keep(void* p, uint32_t a, uint32_t b, uint64_t pol) {

@@ -17,8 +17,13 @@
 // thread = one row, 128 bytes of each box) and warps 4-7 encode columns (a thread
 // = a column pair over 64 rows).  Each consumer warp releases a stage through an
 // "empty" mbarrier, so warps never wait for each other.  Shared-memory reads are
-// bank-conflict free under the swizzle; stores are 16-byte streaming stores of
-// full 32-byte sectors on interior tiles.
+// bank-conflict free under the swizzle.  Codes leave as whole 32-byte sectors:
+// one 256-bit store per thread (a row's 64 code bytes of a tile are two sectors,
+// so are a column's), or, when the code pitches are only 16-byte aligned,
+// through per-warp shared-memory staging and TMA tensor stores.  A rowwise
+// thread keeps its row's scale bytes for the 4 tiles of a super-strip row and
+// writes the 32-byte sector once; columnwise scale bytes are written per tile
+// with an L2 evict_last hint so the sector completes in L2.
 #include <algorithm>
 #include <cstring>
 
@@ -52,6 +57,7 @@ struct EncodeArgs {
   int G;
   int full_m, full_n;  // tiles with tm < full_m and tn < full_n lie entirely inside x
   int vec_ok;          // output pitches / bases allow the 16-byte stores
+  int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
 };
 
 struct StageMeta {
@@ -415,25 +421,40 @@ __device__ __forceinline__ void subtile_scales(const uint8_t* stage, StageMeta& 
 
 // ---------------------------------------------------------------- the kernel
 
-// Staging bytes per consumer warp for the TMA stores of its codes.
+// Staging bytes per consumer warp for the TMA stores of its codes, per buffer.
 constexpr int kStagingPerWarp = 2048;
+#ifndef NVFP4_STAGING_BUFFERS
+#define NVFP4_STAGING_BUFFERS 2
+#endif
+// Each consumer warp alternates between kStagingBuffers staging buffers, so a
+// tile's codes can be written while the previous tile's TMA store is still
+// reading its buffer.
+constexpr int kStagingBuffers = NVFP4_STAGING_BUFFERS;
 
-template <bool TOUT>
+// Output paths for the codes: kOutDirect = 16-byte stores from registers (any
+// alignment, edge tiles), kOutTma = per-warp shared-memory staging and TMA tensor
+// stores, kOutSector = one 32-byte sector per thread with 256-bit stores.
+enum OutMode : int { kOutDirect = 0, kOutTma = 1, kOutSector = 2 };
+
+template <int OUTM>
 struct EncodeSmem {
-  static constexpr int kStagesUsed = TOUT ? 2 : 3;
+  static constexpr int kStagesUsed = OUTM == kOutTma ? 2 : 3;
   static constexpr int kBytes =
-      kStagesUsed * kTileBytes + (TOUT ? kConsumerWarps * kStagingPerWarp : 0) + 1024;
+      kStagesUsed * kTileBytes +
+      (OUTM == kOutTma ? kConsumerWarps * kStagingPerWarp * kStagingBuffers : 0) + 1024;
 };
 
 // TOUT: codes leave through per-warp shared-memory staging and TMA tensor stores
 // (full lines instead of one 16-byte partial sector per thread); the ring then
 // has 2 stages so that 2 CTAs still fit on an SM.
-template <typename T, bool ROW, bool COL, bool FOS, bool B2D, bool TMA, bool TOUT>
+template <typename T, bool ROW, bool COL, bool FOS, bool B2D, bool TMA, int OUTM>
 __global__ void __launch_bounds__(kPipeThreads, 2)
     k_encode(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap map_rc,
              const __grid_constant__ CUtensorMap map_cc, EncodeArgs a) {
   using G = TileGeo<T>;
-  constexpr int NS = EncodeSmem<TOUT>::kStagesUsed;
+  constexpr int NS = EncodeSmem<OUTM>::kStagesUsed;
+  constexpr bool TOUT = OUTM == kOutTma;
+  constexpr bool SECT = OUTM == kOutSector;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[NS];
   __shared__ __align__(8) uint64_t empty[NS];
@@ -586,7 +607,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     for (int k = 0; k < 8; ++k)
       coff[k] = box * kBoxBytes + ((((byte >> 4) ^ k)) << 4) + (byte & 15);
   }
-  uint8_t* staging = smem + NS * kTileBytes + warp * kStagingPerWarp;
+  uint8_t* staging0 = smem + NS * kTileBytes + warp * kStagingPerWarp * kStagingBuffers;
+  uint32_t rsg[TileGrid::kGroup][2];  // rowwise scale bytes of the current super-strip row
   const uint64_t out_policy = policy_evict_first();
   for (int k = 0; k < count; ++k) {
     const int s = k % NS;
@@ -602,6 +624,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     const uint8_t* stage = smem + s * kTileBytes;
     StageMeta& m = meta[s];
     const bool fast = a.vec_ok && tm < a.full_m && tn < a.full_n;
+    uint8_t* staging = staging0 + (k % kStagingBuffers) * kStagingPerWarp;
     if constexpr (B2D) {
       subtile_scales<T, FOS>(stage, m, ROW ? S_r : S_c, ROW ? A_r : A_c, a.F_inv, tid);
       consumer_sync();
@@ -612,8 +635,38 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       rowwise_compute<T, NBOX, FOS, B2D>(stage, m, a, r, b0, S_r, A_r, w, sc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done reading the stage
+      auto store_row_scales = [&]() {
+        if constexpr (BOTH && sizeof(T) == 2) {
+          // A super-strip row of 4 tiles carries 4 x 8 scale bytes per row: one
+          // 32-byte sector.  When the whole group lies in this CTA's chunk, the
+          // thread collects it in registers and writes the sector at once.
+          const int ss = tn / TileGrid::kGroup, jt = tn - ss * TileGrid::kGroup;
+          const int wdt = min(TileGrid::kGroup, a.grid.tiles_n - ss * TileGrid::kGroup);
+          const int g0 = ss * a.grid.tiles_m * TileGrid::kGroup + tm * wdt;
+          const bool grouped = a.row_scale_groups && wdt == TileGrid::kGroup && g0 >= begin &&
+                               g0 + wdt <= end;
+          if (grouped) {
+#pragma unroll
+            for (int jj = 0; jj < TileGrid::kGroup; ++jj)
+              if (jj == jt) {
+                rsg[jj][0] = sc[0];
+                rsg[jj][1] = sc[1];
+              }
+            const int last = fwd ? TileGrid::kGroup - 1 : 0;
+            const int64_t gr = (int64_t)tm * kTileRows + r;
+            if (jt == last && gr < a.M) {
+              uint8_t* sp = a.row_scales + gr * a.row_spitch + ss * 32;
+              stg_v4_cs(sp, make_uint4(rsg[0][0], rsg[0][1], rsg[1][0], rsg[1][1]));
+              stg_v4_cs(sp + 16, make_uint4(rsg[2][0], rsg[2][1], rsg[3][0], rsg[3][1]));
+            }
+            return;
+          }
+        }
+        rowwise_store_scales<T, NBOX>(a, r, b0, tm, tn, sc, fast);
+      };
       if constexpr (TOUT) {
-        if (lane == 0) bulk_wait_read();  // the previous tile's store has left the staging
+        // the store that last used this buffer has finished reading it
+        if (lane == 0) bulk_wait_read_allow<kStagingBuffers - 1>();
         __syncwarp();
         uint8_t* dst = staging + lane * RWB;
 #pragma unroll
@@ -629,7 +682,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
                        tm * kTileRows + (r & ~31), out_policy);
           bulk_commit();
         }
-        rowwise_store_scales<T, NBOX>(a, r, b0, tm, tn, sc, fast);
+        store_row_scales();
+      } else if constexpr (SECT) {
+        if (fast) {
+          uint8_t* cp = a.row_codes + ((int64_t)tm * kTileRows + r) * a.row_cpitch +
+                        (int64_t)tn * (G::TILEC / 2);
+#pragma unroll
+          for (int bi = 0; bi < NBOX; ++bi) stg_v8_cs(cp + bi * 32 + b0 * 32, w[bi]);
+          store_row_scales();
+        } else {
+          rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, false);
+        }
       } else {
         rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, fast);
       }
@@ -640,7 +703,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if constexpr (TOUT) {
-        if (lane == 0) bulk_wait_read();
+        if (lane == 0) bulk_wait_read_allow<kStagingBuffers - 1>();
         __syncwarp();
         uint8_t* dst = staging + lane * 2 * CWB;
 #pragma unroll
@@ -656,7 +719,19 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
           bulk_commit();
         }
       }
-      colwise_store<T, RG, !TOUT>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, fast);
+      if constexpr (SECT) {
+        if (fast) {
+          uint8_t* c0p = a.col_codes + ((int64_t)tn * G::TILEC + cl) * a.col_cpitch +
+                         ((int64_t)tm * kTileRows + rb0) / 2;
+          stg_v8_cs(c0p, w0);
+          stg_v8_cs(c0p + a.col_cpitch, w1);
+          colwise_store<T, RG, false>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, true);
+        } else {
+          colwise_store<T, RG, true>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, false);
+        }
+      } else {
+        colwise_store<T, RG, !TOUT>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, fast);
+      }
     } else {
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -670,26 +745,27 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
 using EncodeFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, EncodeArgs);
 
 template <typename T, bool ROW, bool COL, bool FOS, bool B2D>
-EncodeFn pick_io(bool tma, bool tout) {
-  if constexpr (sizeof(T) == 2) {
-    if (tma && tout) return k_encode<T, ROW, COL, FOS, B2D, true, true>;
+EncodeFn pick_io(bool tma, int outm) {
+  if constexpr (sizeof(T) == 2 && ROW && COL) {
+    if (tma && outm == kOutTma) return k_encode<T, ROW, COL, FOS, B2D, true, kOutTma>;
+    if (tma && outm == kOutSector) return k_encode<T, ROW, COL, FOS, B2D, true, kOutSector>;
   }
-  return tma ? k_encode<T, ROW, COL, FOS, B2D, true, false>
-             : k_encode<T, ROW, COL, FOS, B2D, false, false>;
+  return tma ? k_encode<T, ROW, COL, FOS, B2D, true, kOutDirect>
+             : k_encode<T, ROW, COL, FOS, B2D, false, kOutDirect>;
 }
 
 template <typename T, bool ROW, bool COL>
-EncodeFn pick_mode(bool fos, bool b2d, bool tma, bool tout) {
+EncodeFn pick_mode(bool fos, bool b2d, bool tma, int outm) {
   if (b2d)
-    return fos ? pick_io<T, ROW, COL, true, true>(tma, tout) : pick_io<T, ROW, COL, false, true>(tma, tout);
-  return fos ? pick_io<T, ROW, COL, true, false>(tma, tout) : pick_io<T, ROW, COL, false, false>(tma, tout);
+    return fos ? pick_io<T, ROW, COL, true, true>(tma, outm) : pick_io<T, ROW, COL, false, true>(tma, outm);
+  return fos ? pick_io<T, ROW, COL, true, false>(tma, outm) : pick_io<T, ROW, COL, false, false>(tma, outm);
 }
 
 template <typename T>
-EncodeFn pick_dir(bool row, bool col, bool fos, bool b2d, bool tma, bool tout) {
-  if (row && col) return pick_mode<T, true, true>(fos, b2d, tma, tout);
-  if (row) return pick_mode<T, true, false>(fos, b2d, tma, tout);
-  return pick_mode<T, false, true>(fos, b2d, tma, tout);
+EncodeFn pick_dir(bool row, bool col, bool fos, bool b2d, bool tma, int outm) {
+  if (row && col) return pick_mode<T, true, true>(fos, b2d, tma, outm);
+  if (row) return pick_mode<T, true, false>(fos, b2d, tma, outm);
+  return pick_mode<T, false, true>(fos, b2d, tma, outm);
 }
 
 bool aligned(const void* p, int n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
@@ -741,13 +817,19 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   memset(&map_cc, 0, sizeof(map_cc));
   const bool tma = make_tile_map(&map, q.x, q.in, q.M, q.K, box_cols, kTileRows);
   if (!tma) memset(&map, 0, sizeof(map));
-  // TMA stores of the codes (BF16 input): box = one consumer warp's codes
+  // Output path for the codes of BF16 input with both directions: 32-byte sector
+  // stores when the code pitches allow them, else TMA stores from staging.
   const bool both = row && col;
-  bool tout = bf16 && tma;
-  if (tout && row)
-    tout = make_byte_map(&map_rc, q.row_codes, q.M, a.row_cpitch, both ? 64 : 32, 32);
-  if (tout && col)
-    tout = make_byte_map(&map_cc, q.col_codes, q.K, a.col_cpitch, both ? 32 : 16, 64);
+  int outm = kOutDirect;
+  if (bf16 && tma && both) {
+    if (a.row_cpitch % 32 == 0 && a.col_cpitch % 32 == 0 && aligned(q.row_codes, 32) &&
+        aligned(q.col_codes, 32))
+      outm = kOutSector;
+    else if (make_byte_map(&map_rc, q.row_codes, q.M, a.row_cpitch, 64, 32) &&
+             make_byte_map(&map_cc, q.col_codes, q.K, a.col_cpitch, 32, 64))
+      outm = kOutTma;
+  }
+  const bool tout = outm != kOutDirect;
   // aligned vector stores on interior tiles
   const int rows_per_col_thread = bf16 ? (both ? 64 : 32) : (both ? 32 : 16);
   const int row_scale_bytes = (bf16 ? 4 : 2) * ((tout && both) ? 2 : 1);
@@ -761,10 +843,14 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
           a.col_spitch % cs == 0 && aligned(q.col_scales, cs);
   }
   a.vec_ok = vec ? 1 : 0;
+  a.row_scale_groups = (tout && both && bf16 && a.row_spitch % 32 == 0 &&
+                        aligned(q.row_scales, 32)) ? 1 : 0;
 
-  EncodeFn fn = bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, tout)
-                     : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, tout);
-  const int smem = tout ? EncodeSmem<true>::kBytes : EncodeSmem<false>::kBytes;
+  EncodeFn fn = bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, outm)
+                     : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, outm);
+  const int smem = outm == kOutTma ? EncodeSmem<kOutTma>::kBytes
+                   : outm == kOutSector ? EncodeSmem<kOutSector>::kBytes
+                                        : EncodeSmem<kOutDirect>::kBytes;
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};

@@ -314,3 +314,4 @@ def test_grouped_invalid_ends_write_nothing_and_set_status():
     assert torch.all(ga == -1.0) and torch.all(out.amax == -1.0)
     assert torch.all(out.codes == 0xA5) and torch.all(out.scales == 0xA5)
     assert nv.nvfp4_device_status() == 0
+
