@@ -130,6 +130,14 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def job_throughput(t_local: float, world: int, units_per_rank_step: float, steps: int,
+                   device=None):
+    """(slowest rank's time, whole-job rate): every rank processes the same units per
+    step (independent replicas), and the job is done when the slowest rank is."""
+    t_max = max_over_ranks(t_local, world, device)
+    return t_max, world * units_per_rank_step * steps / t_max
+
+
 # ---------------------------------------------------------------- CPU oracle leg
 
 def oracle_sample(sample_rows: int, seed: int = 2):
@@ -244,8 +252,9 @@ def run_ours(args):
     clocks = sampler.stop()
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    t_total = sum(step_ms) / 1e3
-    t_total = max_over_ranks(t_total, world, dev)
+    shapes = [t.shape for t in ops]
+    bio = sum(bytes_io(r, c) for r, c in shapes)
+    t_total, rate = job_throughput(sum(step_ms) / 1e3, world, bio, K, dev)
     ms_per_step = 1e3 * t_total / K
     # encode-kernel durations (between the event after amax and after quantize)
     enc_x = [mid[k][0].elapsed_time(mid[k][1]) for k in range(K)]
@@ -253,11 +262,9 @@ def run_ours(args):
     amax_x = [starts[k].elapsed_time(mid[k][0]) for k in range(K)]
     amax_dy = [mid[k][1].elapsed_time(mid[k][2]) for k in range(K)]
 
-    shapes = [t.shape for t in ops]
-    bio = sum(bytes_io(r, c) for r, c in shapes)
     bmin = sum(bytes_min(r, c) for r, c in shapes)
     elems = sum(r * c for r, c in shapes)
-    value = world * bio * K / t_total / 1e9
+    value = rate / 1e9
     peak, peak_src = measured_peaks()
     enc_bytes = sum(encode_bytes(r, c) for r, c in shapes) / 2  # per launch (mean of the two)
     enc_dur = (statistics.mean(enc_x) + statistics.mean(enc_dy)) / 2 / 1e3
