@@ -134,9 +134,26 @@ struct BlockEnc {
   float e;      // S / sd, or 0
 };
 
-template <int T>
+// fl(b / 6) for a b with at most 8 significant bits (every BF16 value): the
+// product with fl(1/6) = 0x3E2AAAAB, then one FMA correction step (Markstein's
+// division with a correctly rounded reciprocal).  The residual b - 6 q0 is exact,
+// and for each of the 32639 positive finite BF16 values (subnormal quotients
+// included) the corrected quotient equals the IEEE quotient, checked in exact
+// rational arithmetic.
+__device__ __forceinline__ float div6_short(float b) {
+  const float r = __uint_as_float(0x3E2AAAABu);
+  const float q0 = __fmul_rn(b, r);
+  const float rem = __fmaf_rn(-q0, 6.0f, b);
+  return __fmaf_rn(rem, r, q0);
+}
+
+// SHORT: b is a BF16 value (the block max of BF16 inputs), so fl(b / 6) may use
+// div6_short; otherwise it is an IEEE division.
+template <int T, bool SHORT = false>
 __device__ __forceinline__ BlockEnc block_encode(float b, float S) {
-  const float q = (T == 4) ? __fmul_rn(b, 0.25f) : __fdiv_rn(b, (float)T);  // b/4 == b*0.25 exactly
+  const float q = (T == 4) ? __fmul_rn(b, 0.25f)  // b/4 == b*0.25 exactly
+                  : SHORT  ? div6_short(b)
+                           : __fdiv_rn(b, (float)T);
   const float s32 = __fmul_rn(q, S);
   BlockEnc r;
   r.s8 = e4m3_byte(s32);
@@ -187,10 +204,10 @@ __device__ __forceinline__ float sse8(float err, const float* x, uint32_t codes,
 // Quantize 16 FP32 values of one block whose max |x| is b: writes the two code
 // words (value k in nibble k) and returns the scale byte.  FOS: four-over-six
 // (needs the line amax a and F_inv for the error of each candidate).
-template <bool FOS>
+template <bool FOS, bool SHORT = false>
 __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S, float a,
                                                float F_inv, uint32_t& c0, uint32_t& c1) {
-  BlockEnc e6 = block_encode<6>(b, S);
+  BlockEnc e6 = block_encode<6, SHORT>(b, S);
   c0 = codes8(x, e6.e);
   c1 = codes8(x + 8, e6.e);
   if constexpr (!FOS) {

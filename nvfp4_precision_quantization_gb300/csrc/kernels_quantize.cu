@@ -107,7 +107,7 @@ __device__ __forceinline__ void store_tail_words(uint8_t* p, const uint32_t (&w)
              NW > 7 ? w[7 < NW ? 7 : 0] : 0u);
 }
 
-template <bool FOS, bool B2D>
+template <bool FOS, bool B2D, bool SHORT>
 __device__ __forceinline__ uint32_t encode_block(const float* x, float b, float S, float a,
                                                  float F_inv, uint32_t s2d, float e2d,
                                                  uint32_t& c0, uint32_t& c1) {
@@ -115,7 +115,7 @@ __device__ __forceinline__ uint32_t encode_block(const float* x, float b, float 
     codes16(x, e2d, c0, c1);
     return s2d;
   } else {
-    return quantize16<FOS>(x, b, S, a, F_inv, c0, c1);
+    return quantize16<FOS, SHORT>(x, b, S, a, F_inv, c0, c1);
   }
 }
 
@@ -172,7 +172,7 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const Stag
         s2 = m.s2d[sub];
         e2 = m.e2d[sub];
       }
-      sc[bi] |= encode_block<FOS, B2D>(x, b, S, A, a.F_inv, s2, e2, w[bi][2 * j], w[bi][2 * j + 1])
+      sc[bi] |= encode_block<FOS, B2D, sizeof(T) == 2>(x, b, S, A, a.F_inv, s2, e2, w[bi][2 * j], w[bi][2 * j + 1])
                 << (8 * j);
     }
   }
@@ -300,9 +300,9 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const Stag
       s2 = m.s2d[sub];
       e2 = m.e2d[sub];
     }
-    sc0 |= encode_block<FOS, B2D>(x0, b0, S0, A0, a.F_inv, s2, e2, w0[2 * jb], w0[2 * jb + 1])
+    sc0 |= encode_block<FOS, B2D, sizeof(T) == 2>(x0, b0, S0, A0, a.F_inv, s2, e2, w0[2 * jb], w0[2 * jb + 1])
            << (8 * jb);
-    sc1 |= encode_block<FOS, B2D>(x1, b1, S1, A1, a.F_inv, s2, e2, w1[2 * jb], w1[2 * jb + 1])
+    sc1 |= encode_block<FOS, B2D, sizeof(T) == 2>(x1, b1, S1, A1, a.F_inv, s2, e2, w1[2 * jb], w1[2 * jb + 1])
            << (8 * jb);
   }
 }
@@ -398,7 +398,7 @@ __device__ __forceinline__ void subtile_scales(const uint8_t* stage, StageMeta& 
     load_row(i, x);
     b = fmaxf(b, absmax16_f32(x));
   }
-  BlockEnc e6 = block_encode<6>(b, S);
+  BlockEnc e6 = block_encode<6, sizeof(T) == 2>(b, S);
   if constexpr (FOS) {
     BlockEnc e4 = block_encode<4>(b, S);
     const float D6 = dequant_factor(e6.sd, amax, F_inv);
