@@ -407,6 +407,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     if (lane != 0) return;
     prefetch_tmap(&tmap);
     const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
+    TileCursor cur;
+    cur.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
     int issued = 0;
     for (int k = 0; k < count; ++k) {
       const int s = k % kStages;
@@ -417,10 +419,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         break;
       }
       if (abort_flag) break;
-      int tm, tn;
-      a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
-      issue_tile<T>(smem + s * kTileBytes, &tmap, &full[s], tm, tn,
+      issue_tile<T>(smem + s * kTileBytes, &tmap, &full[s], cur.tm, cur.tn(),
                     k >= count - a.keep_tiles ? pol_last : pol_first);
+      cur.step(a.grid, fwd);
       issued = k + 1;
     }
     if (abort_flag)
@@ -480,11 +481,58 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     }
   };
 
-  for (int k = 0; k < count; ++k) {
+  Acc rpa[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rpa[i] = 0;
+  int cur_tm = -1;
+  // Row maxima of tile row tm_ accumulated over consecutive tiles of that row:
+  // reduce over the 8 lanes that share a row, publish, reset.
+  auto flush_rows = [&](int tm_) {
+    const int64_t row0 = (int64_t)tm_ * kTileRows + rg * 32 + ro;
+    if constexpr (BF16) {
+      // fold each pair, pack two rows per word, reduce over the 8 lanes of the row
+      uint32_t P[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t f0 = absmax_bf16x2(rpa[2 * j], __byte_perm(rpa[2 * j], 0, 0x1032));
+        const uint32_t f1 = absmax_bf16x2(rpa[2 * j + 1], __byte_perm(rpa[2 * j + 1], 0, 0x1032));
+        P[j] = __byte_perm(f0, f1, 0x7610);
+      }
+      const bool u4 = lane & 4, u2 = lane & 2;
+      uint32_t q0 = absmax_bf16x2(u4 ? P[2] : P[0], __shfl_xor_sync(0xffffffffu, u4 ? P[0] : P[2], 4));
+      uint32_t q1 = absmax_bf16x2(u4 ? P[3] : P[1], __shfl_xor_sync(0xffffffffu, u4 ? P[1] : P[3], 4));
+      uint32_t rr = absmax_bf16x2(u2 ? q1 : q0, __shfl_xor_sync(0xffffffffu, u2 ? q0 : q1, 2));
+      rr = absmax_bf16x2(rr, __shfl_xor_sync(0xffffffffu, rr, 1)) & 0x7fff7fffu;
+      if ((lane & 1) == 0) {
+        const int i0 = (u4 ? 4 : 0) + (u2 ? 2 : 0);
+        const int64_t r0 = row0 + 4 * i0, r1 = r0 + 4;
+        if (r0 < a.M) atomic_max_nonneg(&a.row_amax[r0], __uint_as_float(rr << 16));
+        if (r1 < a.M) atomic_max_nonneg(&a.row_amax[r1], __uint_as_float(rr & 0xffff0000u));
+      }
+    } else {
+      const bool u4 = lane & 4, u2 = lane & 2, u1 = lane & 1;
+      float q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        q[j] = fmaxf(u4 ? rpa[4 + j] : rpa[j], __shfl_xor_sync(0xffffffffu, u4 ? rpa[j] : rpa[4 + j], 4));
+      float h[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        h[j] = fmaxf(u2 ? q[2 + j] : q[j], __shfl_xor_sync(0xffffffffu, u2 ? q[j] : q[2 + j], 2));
+      const float g = fmaxf(u1 ? h[1] : h[0], __shfl_xor_sync(0xffffffffu, u1 ? h[0] : h[1], 1));
+      const int i0 = (u4 ? 4 : 0) + (u2 ? 2 : 0) + (u1 ? 1 : 0);
+      const int64_t r0 = row0 + 4 * i0;
+      if (r0 < a.M) atomic_max_nonneg(&a.row_amax[r0], g);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rpa[i] = 0;
+  };
+
+  TileCursor cur;
+  cur.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
+  for (int k = 0; k < count; ++k, cur.step(a.grid, fwd)) {
     const int s = k % kStages;
-    int tm, tn;
-    a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
-    const int ss = tn / NG, gsel = tn - ss * NG;
+    const int tm = cur.tm, ss = cur.ss, gsel = cur.jt;
     if (COL && ss != cur_ss) {
       if (cur_ss >= 0) flush_cols(cur_ss);
       cur_ss = ss;
@@ -544,45 +592,19 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       }
     }
     if (ROW) {
-      const int64_t row0 = (int64_t)tm * kTileRows + rg * 32 + ro;
-      if constexpr (BF16) {
-        // fold each pair, pack two rows per word, reduce over the 8 lanes of the row
-        uint32_t P[4];
+      if (tm != cur_tm) {
+        if (cur_tm >= 0) flush_rows(cur_tm);
+        cur_tm = tm;
+      }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t f0 = absmax_bf16x2(rp[2 * j], __byte_perm(rp[2 * j], 0, 0x1032));
-          const uint32_t f1 = absmax_bf16x2(rp[2 * j + 1], __byte_perm(rp[2 * j + 1], 0, 0x1032));
-          P[j] = __byte_perm(f0, f1, 0x7610);
-        }
-        const bool u4 = lane & 4, u2 = lane & 2;
-        uint32_t q0 = absmax_bf16x2(u4 ? P[2] : P[0], __shfl_xor_sync(0xffffffffu, u4 ? P[0] : P[2], 4));
-        uint32_t q1 = absmax_bf16x2(u4 ? P[3] : P[1], __shfl_xor_sync(0xffffffffu, u4 ? P[1] : P[3], 4));
-        uint32_t rr = absmax_bf16x2(u2 ? q1 : q0, __shfl_xor_sync(0xffffffffu, u2 ? q0 : q1, 2));
-        rr = absmax_bf16x2(rr, __shfl_xor_sync(0xffffffffu, rr, 1)) & 0x7fff7fffu;
-        if ((lane & 1) == 0) {
-          const int i0 = (u4 ? 4 : 0) + (u2 ? 2 : 0);
-          const int64_t r0 = row0 + 4 * i0, r1 = r0 + 4;
-          if (r0 < a.M) atomic_max_nonneg(&a.row_amax[r0], __uint_as_float(rr << 16));
-          if (r1 < a.M) atomic_max_nonneg(&a.row_amax[r1], __uint_as_float(rr & 0xffff0000u));
-        }
-      } else {
-        const bool u4 = lane & 4, u2 = lane & 2, u1 = lane & 1;
-        float q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          q[j] = fmaxf(u4 ? rp[4 + j] : rp[j], __shfl_xor_sync(0xffffffffu, u4 ? rp[j] : rp[4 + j], 4));
-        float h[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          h[j] = fmaxf(u2 ? q[2 + j] : q[j], __shfl_xor_sync(0xffffffffu, u2 ? q[j] : q[2 + j], 2));
-        const float g = fmaxf(u1 ? h[1] : h[0], __shfl_xor_sync(0xffffffffu, u1 ? h[0] : h[1], 1));
-        const int i0 = (u4 ? 4 : 0) + (u2 ? 2 : 0) + (u1 ? 1 : 0);
-        const int64_t r0 = row0 + 4 * i0;
-        if (r0 < a.M) atomic_max_nonneg(&a.row_amax[r0], g);
+      for (int i = 0; i < 8; ++i) {
+        if constexpr (BF16) rpa[i] = absmax_bf16x2(rpa[i], rp[i]);
+        else rpa[i] = fmaxf(rpa[i], rp[i]);
       }
     }
   }
   if (COL && cur_ss >= 0 && !abort_flag) flush_cols(cur_ss);
+  if (ROW && cur_tm >= 0 && !abort_flag) flush_rows(cur_tm);
   if (TEN) {
     float m;
     if constexpr (BF16) m = bf16x2_hmax_f32(tmx);

@@ -485,9 +485,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     // ---------------- producer warp
     const uint64_t policy = policy_evict_first();
     if (TMA && lane == 0) prefetch_tmap(&tmap);
+    // tiles are issued in order k = 0, 1, ...: one cursor steps along with them
+    TileCursor ci;
+    ci.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
     auto issue = [&](int k) {
-      int tm, tn;
-      a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+      const int tm = ci.tm, tn = ci.tn();
+      ci.step(a.grid, fwd);
       uint8_t* stage = smem + (k % NS) * kTileBytes;
       if constexpr (TMA) {
         if (lane == 0) issue_tile<T>(stage, &tmap, &full[k % NS], tm, tn, policy);
@@ -503,9 +506,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     // amax of a tile's rows and columns, loaded one tile ahead so that their L2
     // latency overlaps the wait for the next free stage
     float ra[RPL], ca[CPL];
+    // the amax of tile k are loaded in order k = 0, 1, ... as well
+    TileCursor cm;
+    cm.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
     auto load_amax = [&](int k, float (&r_)[RPL], float (&c_)[CPL]) {
-      int tm, tn;
-      a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+      (void)k;
+      const int tm = cm.tm, tn = cm.tn();
+      cm.step(a.grid, fwd);
       if (ROW) {
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
@@ -610,10 +617,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   uint8_t* staging0 = smem + NS * kTileBytes + warp * kStagingPerWarp * kStagingBuffers;
   uint32_t rsg[TileGrid::kGroup][2];  // rowwise scale bytes of the current super-strip row
   const uint64_t out_policy = policy_evict_first();
-  for (int k = 0; k < count; ++k) {
+  TileCursor cur;
+  cur.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
+  for (int k = 0; k < count; ++k, cur.step(a.grid, fwd)) {
     const int s = k % NS;
-    int tm, tn;
-    a.grid.coords(a.grid.walk(begin, end, k, fwd), tm, tn);
+    const int tm = cur.tm, tn = cur.tn();
     const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / NS) & 1));
     if (!ok) {
       abort_flag = 1;
@@ -640,8 +648,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
           // A super-strip row of 4 tiles carries 4 x 8 scale bytes per row: one
           // 32-byte sector.  When the whole group lies in this CTA's chunk, the
           // thread collects it in registers and writes the sector at once.
-          const int ss = tn / TileGrid::kGroup, jt = tn - ss * TileGrid::kGroup;
-          const int wdt = min(TileGrid::kGroup, a.grid.tiles_n - ss * TileGrid::kGroup);
+          const int ss = cur.ss, jt = cur.jt, wdt = cur.wdt;
           const int g0 = ss * a.grid.tiles_m * TileGrid::kGroup + tm * wdt;
           const bool grouped = a.row_scale_groups && wdt == TileGrid::kGroup && g0 >= begin &&
                                g0 + wdt <= end;

@@ -55,6 +55,46 @@ struct TileGrid {
   }
 };
 
+// A position in the tile order that moves one tile at a time without integer
+// divisions: row tile tm, super-strip ss, tile jt inside the super-strip row, and
+// that row's width wdt (kGroup, or less in the last super-strip).
+struct TileCursor {
+  int tm, ss, jt, wdt;
+  __device__ __forceinline__ int tn() const { return ss * TileGrid::kGroup + jt; }
+
+  __device__ __forceinline__ void seek(const TileGrid& g, int L) {
+    const int per_ss = g.tiles_m * TileGrid::kGroup;
+    ss = L / per_ss;
+    const int rem = L - ss * per_ss;
+    wdt = min(TileGrid::kGroup, g.tiles_n - ss * TileGrid::kGroup);
+    tm = rem / wdt;
+    jt = rem - tm * wdt;
+  }
+  // the next tile of the order (fwd) or the previous one
+  __device__ __forceinline__ void step(const TileGrid& g, bool fwd) {
+    if (fwd) {
+      if (++jt < wdt) return;
+      jt = 0;
+      if (++tm < g.tiles_m) return;
+      tm = 0;
+      ++ss;
+      wdt = min(TileGrid::kGroup, g.tiles_n - ss * TileGrid::kGroup);
+    } else {
+      if (jt > 0) {
+        --jt;
+      } else if (tm > 0) {
+        --tm;
+        jt = wdt - 1;
+      } else {
+        --ss;
+        wdt = min(TileGrid::kGroup, g.tiles_n - ss * TileGrid::kGroup);
+        tm = g.tiles_m - 1;
+        jt = wdt - 1;
+      }
+    }
+  }
+};
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
