@@ -245,7 +245,7 @@ __device__ __forceinline__ void rowwise_store_scales(const EncodeArgs& a, int r,
 template <typename T, int RG, bool FOS, bool B2D>
 __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const StageMeta& m,
                                                 const EncodeArgs& a, int cl, int rb0,
-                                                const uint32_t (&coff)[8], float S_t, float A_t,
+                                                const int32_t (&coff)[8], float S_t, float A_t,
                                                 uint32_t (&w0)[RG / 8], uint32_t (&w1)[RG / 8],
                                                 uint32_t& sc0, uint32_t& sc1) {
   using G = TileGeo<T>;
@@ -605,15 +605,31 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   constexpr int CWB = RG / 2;                 // code bytes per column (TMA box width)
   const bool is_row = ROW && (!BOTH || tid < 128);
   const int ct = BOTH ? tid - 128 : tid;      // columnwise thread index
-  const int cl = 2 * (ct % NP), rb0 = (ct / NP) * RG;
+  // Columnwise thread mapping.  PAIRED (sector stores, both directions, 1x16,
+  // no four-over-six): lane bit 0 selects the row half and the other lane bits
+  // the column pair, so the two 32-byte halves of a column's 64 code bytes of a
+  // tile, and its two 4-byte scale halves, sit in neighbouring lanes and leave
+  // in one coalesced request.  The odd lanes visit the rows of each 16-row block
+  // in the order i ^ 4, which puts the two halves on disjoint shared-memory
+  // banks; their code words are put back in row order afterwards.  Otherwise
+  // consecutive threads take consecutive column pairs.
+  constexpr bool PAIRED = SECT && BOTH && sizeof(T) == 2 && !FOS && !B2D;
+  const int hh = PAIRED ? (lane & 1) : 0;
+  const int cl = PAIRED ? 2 * (((ct >> 5) << 4) + (lane >> 1)) : 2 * (ct % NP);
+  const int rb0 = PAIRED ? hh * RG : (ct / NP) * RG;
   const int r = BOTH ? tid : (tid & 127), b0 = BOTH ? 0 : (tid >> 7);
-  uint32_t coff[8];
+  // byte offset of row i of a 16-row block: i * 128 + coff[i & 7] (signed: with
+  // the i ^ 4 row order an entry can be negative, the sum never is)
+  int32_t coff[8];
   {
     const int box = cl / G::BOXC, byte = (cl % G::BOXC) * (int)sizeof(T);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      coff[k] = box * kBoxBytes + ((((byte >> 4) ^ k)) << 4) + (byte & 15);
+    for (int k = 0; k < 8; ++k) {
+      const int kk = k ^ (4 * hh);  // the row actually read, mod 8
+      coff[k] = box * kBoxBytes + ((((byte >> 4) ^ kk)) << 4) + (byte & 15) + (kk - k) * 128;
+    }
   }
+  const uint32_t word_sel = hh ? 0x1032u : 0x3210u;  // swaps the halves of a code word
   uint8_t* staging0 = smem + NS * kTileBytes + warp * kStagingPerWarp * kStagingBuffers;
   uint32_t rsg[TileGrid::kGroup][2];  // rowwise scale bytes of the current super-strip row
   const uint64_t out_policy = policy_evict_first();
@@ -709,6 +725,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       colwise_compute<T, RG, FOS, B2D>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1, sc0, sc1);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if constexpr (PAIRED) {
+#pragma unroll
+        for (int q = 0; q < RG / 8; ++q) {
+          w0[q] = __byte_perm(w0[q], 0, word_sel);
+          w1[q] = __byte_perm(w1[q], 0, word_sel);
+        }
+      }
       if constexpr (TOUT) {
         if (lane == 0) bulk_wait_read_allow<kStagingBuffers - 1>();
         __syncwarp();
