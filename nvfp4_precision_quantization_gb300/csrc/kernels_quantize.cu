@@ -123,18 +123,19 @@ __device__ __forceinline__ uint32_t encode_block(const float* x, float b, float 
 
 // Codes and scales of row r of boxes [b0, b0 + NBOX): w[box][word], sc[box].
 // Rows / columns outside x were zero-filled by the load, so they encode to 0;
-// the caller decides what is stored.
+// the caller decides what is stored.  rot = 4 (BF16) makes step j read block
+// j ^ 2 of the box row (its results land in the slots of block j).
 template <typename T, int NBOX, bool FOS, bool B2D>
 __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const StageMeta& m,
                                                 const EncodeArgs& a, int r, int b0, float S_t,
                                                 float A_t,
                                                 uint32_t (&w)[NBOX][TileGeo<T>::BOXC / 8],
-                                                uint32_t (&sc)[NBOX]) {
+                                                uint32_t (&sc)[NBOX], int rot = 0) {
   using G = TileGeo<T>;
   constexpr int NB = G::BOXC / 16;  // blocks per box row
   const float S = a.row_scaled ? m.rowS[r] : S_t;
   const float A = a.row_scaled ? m.rowA[r] : A_t;
-  const int sw = r & 7;
+  const int sw = (r & 7) ^ rot;
 #pragma unroll
   for (int bi = 0; bi < NBOX; ++bi) {
     const int box = b0 + bi;
@@ -653,7 +654,70 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       subtile_scales<T, FOS>(stage, m, ROW ? S_r : S_c, ROW ? A_r : A_c, a.F_inv, tid);
       consumer_sync();
     }
-    if (is_row) {
+    if (PAIRED && is_row) {
+      if constexpr (PAIRED) {
+        // Two rows r1, r1 + 16 of box hb = lane & 1: the two lanes of a pair write the
+        // two 32-byte halves of a row's 64 code bytes of the tile in one request.
+        // The box-1 lanes read the blocks in the order 2, 3, 0, 1 (rot = 4): the
+        // two boxes of a row then sit on disjoint shared-memory banks.
+        const int hb = lane & 1, r1 = 32 * warp + (lane >> 1);
+        const uint32_t bsel = hb ? 0x1032u : 0x3210u;
+        uint32_t sa[1], sb[1];
+        // codes of one row: computed, put back in block order 0, 1, 2, 3, stored
+        // (each row on its own keeps 8 code words live instead of 16)
+        auto row_codes = [&](int rr, uint32_t (&sx)[1]) {
+          uint32_t wx[1][8];
+          rowwise_compute<T, 1, FOS, B2D>(stage, m, a, rr, hb, S_r, A_r, wx, sx, 4 * hb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t lo = wx[0][q], hi = wx[0][q + 4];
+            wx[0][q] = hb ? hi : lo;
+            wx[0][q + 4] = hb ? lo : hi;
+          }
+          sx[0] = __byte_perm(sx[0], 0, bsel);
+          if (fast)
+            stg_v8_cs(a.row_codes + ((int64_t)tm * kTileRows + rr) * a.row_cpitch +
+                          (int64_t)tn * (G::TILEC / 2) + hb * 32,
+                      wx[0]);
+          else
+            rowwise_store<T, 1>(a, rr, hb, tm, tn, wx, sx, false);
+        };
+        row_codes(r1, sa);
+        row_codes(r1 + 16, sb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done reading the stage
+        if (fast) {
+          const int64_t gr1 = (int64_t)tm * kTileRows + r1;
+          const int ss = cur.ss, jt = cur.jt, wdt = cur.wdt;
+          const int g0 = ss * a.grid.tiles_m * TileGrid::kGroup + tm * wdt;
+          const bool grouped = a.row_scale_groups && wdt == TileGrid::kGroup && g0 >= begin &&
+                               g0 + wdt <= end;
+          if (grouped) {
+            // a row's 4 x 8 scale bytes of the super-strip row: one 32-byte sector,
+            // its first half written by the box-0 lane, the second by the box-1 lane
+#pragma unroll
+            for (int jj = 0; jj < TileGrid::kGroup; ++jj)
+              if (jj == jt) {
+                rsg[jj][0] = sa[0];
+                rsg[jj][1] = sb[0];
+              }
+            if (jt == (fwd ? TileGrid::kGroup - 1 : 0)) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t x1 = __shfl_xor_sync(0xffffffffu, hb ? rsg[0][h] : rsg[2][h], 1);
+                const uint32_t x2 = __shfl_xor_sync(0xffffffffu, hb ? rsg[1][h] : rsg[3][h], 1);
+                const uint4 v = hb ? make_uint4(x1, rsg[2][h], x2, rsg[3][h])
+                                   : make_uint4(rsg[0][h], x1, rsg[1][h], x2);
+                stg_v4_cs(a.row_scales + (gr1 + 16 * h) * a.row_spitch + ss * 32 + hb * 16, v);
+              }
+            }
+          } else {
+            rowwise_store_scales<T, 1>(a, r1, hb, tm, tn, sa, true);
+            rowwise_store_scales<T, 1>(a, r1 + 16, hb, tm, tn, sb, true);
+          }
+        }
+      }
+    } else if (is_row) {
       uint32_t w[NBOX][G::BOXC / 8];
       uint32_t sc[NBOX];
       rowwise_compute<T, NBOX, FOS, B2D>(stage, m, a, r, b0, S_r, A_r, w, sc);
