@@ -51,6 +51,14 @@ def encode_bytes(rows, cols):
     return bytes_io(rows, cols)
 
 
+# DRAM bytes (read + write) per launch of the encode kernel on this workload, mean of
+# the X and dY launches, from one ncu capture of a full step (dram__bytes_read.sum +
+# dram__bytes_write.sum, L2 left as the step leaves it); the capture and its command
+# are in profiles/traffic_linear_step_x16384x8192_dy16384x28672.md.  To be taken
+# again whenever the encode kernel changes.
+ENCODE_TRAFFIC_BYTES = (309.8e6 + 1370.7e6) / 2
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -296,10 +304,11 @@ def run_ours(args):
                 "ms_amax_x": statistics.mean(amax_x), "ms_encode_x": statistics.mean(enc_x),
                 "ms_amax_dy": statistics.mean(amax_dy), "ms_encode_dy": statistics.mean(enc_dy),
             },
-            "roofline": {"kernel": "k_quantize (encode pass)", "bound": "hbm",
+            "roofline": {"kernel": "k_encode (encode pass)", "bound": "hbm",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": None},
+                         "traffic": ENCODE_TRAFFIC_BYTES if args.rows == ROWS else None,
+                         "algorithmic_bytes": enc_bytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 6 * K,
