@@ -58,6 +58,7 @@ struct EncodeArgs {
   int full_m, full_n;  // tiles with tm < full_m and tn < full_n lie entirely inside x
   int vec_ok;          // output pitches / bases allow the 16-byte stores
   int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
+  int col_scale_pairs;   // columnwise scales of two tile rows go out as 16 bytes per column
 };
 
 struct StageMeta {
@@ -460,6 +461,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   __shared__ __align__(8) uint64_t full[NS];
   __shared__ __align__(8) uint64_t empty[NS];
   __shared__ StageMeta meta[NS];
+  // Columnwise scale bytes of the first tile row of a pair, per tile of the
+  // super-strip row and column, held until the CTA reaches the second tile row
+  // (4 tiles later in its walk): [tile in super-strip][column][row half].
+  __shared__ uint32_t csb[SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? TileGrid::kGroup : 1]
+                         [SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? 128 : 1][2];
   __shared__ volatile int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -819,7 +825,43 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
                          ((int64_t)tm * kTileRows + rb0) / 2;
           stg_v8_cs(c0p, w0);
           stg_v8_cs(c0p + a.col_cpitch, w1);
-          colwise_store<T, RG, false>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, true);
+          bool paired_scales = false;
+          if constexpr (PAIRED) {
+            // Tile rows 2p and 2p + 1 of this tile column are 4 tiles apart in the
+            // walk.  When both lie in this CTA's chunk and are full tiles, the first
+            // one visited parks its scale bytes in csb and the second writes the
+            // column's 16 bytes for both: lane hh = 0 the bytes of tile row 2p,
+            // lane hh = 1 those of 2p + 1, one coalesced request per column.
+            const int p0 = tm & ~1;
+            const int Lp0 = cur.ss * a.grid.tiles_m * TileGrid::kGroup + p0 * cur.wdt + cur.jt;
+            paired_scales = a.col_scale_pairs && p0 + 1 < a.full_m && Lp0 >= begin &&
+                            Lp0 + cur.wdt < end;
+            if (paired_scales) {
+              const bool first = fwd ? tm == p0 : tm != p0;
+              if (first) {
+                csb[cur.jt][cl][hh] = sc0;
+                csb[cur.jt][cl + 1][hh] = sc1;
+              } else {
+                const uint32_t o0 = __shfl_xor_sync(0xffffffffu, sc0, 1);
+                const uint32_t o1 = __shfl_xor_sync(0xffffffffu, sc1, 1);
+                // this tile's 8 bytes of each column: row half 0, then row half 1
+                const uint2 t0 = hh ? make_uint2(o0, sc0) : make_uint2(sc0, o0);
+                const uint2 t1 = hh ? make_uint2(o1, sc1) : make_uint2(sc1, o1);
+                const uint2 q0 = make_uint2(csb[cur.jt][cl][0], csb[cur.jt][cl][1]);
+                const uint2 q1 = make_uint2(csb[cur.jt][cl + 1][0], csb[cur.jt][cl + 1][1]);
+                // lane hh writes the bytes of tile row p0 + hh
+                const bool mine = (hh == 1) == (tm != p0);
+                const uint2 v0 = mine ? t0 : q0, v1 = mine ? t1 : q1;
+                uint8_t* s0p = a.col_scales + ((int64_t)tn * G::TILEC + cl) * a.col_spitch +
+                               (int64_t)p0 * (kTileRows / 16) + 8 * hh;
+                const uint64_t keep = policy_evict_last();
+                stg_v2_keep(s0p, v0.x, v0.y, keep);
+                stg_v2_keep(s0p + a.col_spitch, v1.x, v1.y, keep);
+              }
+            }
+          }
+          if (!paired_scales)
+            colwise_store<T, RG, false>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, true);
         } else {
           colwise_store<T, RG, true>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, false);
         }
@@ -937,6 +979,7 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
           a.col_spitch % cs == 0 && aligned(q.col_scales, cs);
   }
   a.vec_ok = vec ? 1 : 0;
+  a.col_scale_pairs = (both && bf16 && a.col_spitch % 16 == 0 && aligned(q.col_scales, 16)) ? 1 : 0;
   a.row_scale_groups = (tout && both && bf16 && a.row_spitch % 32 == 0 &&
                         aligned(q.row_scales, 32)) ? 1 : 0;
 
