@@ -58,14 +58,46 @@ struct EncodeArgs {
   int full_m, full_n;  // tiles with tm < full_m and tn < full_n lie entirely inside x
   int vec_ok;          // output pitches / bases allow the 16-byte stores
   int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
-  int col_scale_pairs;   // columnwise scales of two tile rows go out as 16 bytes per column
+  int col_scale_sectors;  // columnwise scales of four tile rows go out as one 32-byte sector
 };
 
-struct StageMeta {
-  float rowS[kTileRows], rowA[kTileRows];
-  float colS[128], colA[128];
-  uint32_t s2d[64];
-  float e2d[64];
+// Per-stage values staged by the producer: the tile's per-row and per-column
+// global scales, and (four-over-six or 16x16 blocks only) the amax values and the
+// 16x16 sub-tile scales.  FULL = false keeps only the scales (smaller footprint).
+template <bool FULL>
+struct StageMetaT {
+  float rowS[kTileRows], colS[128];
+  float rowA_[FULL ? kTileRows : 1], colA_[FULL ? 128 : 1];
+  uint32_t s2d_[FULL ? 64 : 1];
+  float e2d_[FULL ? 64 : 1];
+  __device__ __forceinline__ float rowA(int i) const {
+    if constexpr (FULL) return rowA_[i];
+    else return 0.0f;
+  }
+  __device__ __forceinline__ float colA(int i) const {
+    if constexpr (FULL) return colA_[i];
+    else return 0.0f;
+  }
+  __device__ __forceinline__ uint32_t s2d(int i) const {
+    if constexpr (FULL) return s2d_[i];
+    else return 0u;
+  }
+  __device__ __forceinline__ float e2d(int i) const {
+    if constexpr (FULL) return e2d_[i];
+    else return 0.0f;
+  }
+  __device__ __forceinline__ void set_rowA(int i, float v) {
+    if constexpr (FULL) rowA_[i] = v;
+  }
+  __device__ __forceinline__ void set_colA(int i, float v) {
+    if constexpr (FULL) colA_[i] = v;
+  }
+  __device__ __forceinline__ void set_2d(int i, uint32_t s8, float e) {
+    if constexpr (FULL) {
+      s2d_[i] = s8;
+      e2d_[i] = e;
+    }
+  }
 };
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -126,8 +158,8 @@ __device__ __forceinline__ uint32_t encode_block(const float* x, float b, float 
 // Rows / columns outside x were zero-filled by the load, so they encode to 0;
 // the caller decides what is stored.  rot = 4 (BF16) makes step j read block
 // j ^ 2 of the box row (its results land in the slots of block j).
-template <typename T, int NBOX, bool FOS, bool B2D>
-__device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const StageMeta& m,
+template <typename T, int NBOX, bool FOS, bool B2D, typename M>
+__device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m,
                                                 const EncodeArgs& a, int r, int b0, float S_t,
                                                 float A_t,
                                                 uint32_t (&w)[NBOX][TileGeo<T>::BOXC / 8],
@@ -135,7 +167,7 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const Stag
   using G = TileGeo<T>;
   constexpr int NB = G::BOXC / 16;  // blocks per box row
   const float S = a.row_scaled ? m.rowS[r] : S_t;
-  const float A = a.row_scaled ? m.rowA[r] : A_t;
+  const float A = a.row_scaled ? m.rowA(r) : A_t;
   const int sw = (r & 7) ^ rot;
 #pragma unroll
   for (int bi = 0; bi < NBOX; ++bi) {
@@ -171,8 +203,8 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const Stag
       float e2 = 0.0f;
       if constexpr (B2D) {
         const int sub = (r >> 4) * (G::TILEC / 16) + box * NB + j;
-        s2 = m.s2d[sub];
-        e2 = m.e2d[sub];
+        s2 = m.s2d(sub);
+        e2 = m.e2d(sub);
       }
       sc[bi] |= encode_block<FOS, B2D, sizeof(T) == 2>(x, b, S, A, a.F_inv, s2, e2, w[bi][2 * j], w[bi][2 * j + 1])
                 << (8 * j);
@@ -244,8 +276,8 @@ __device__ __forceinline__ void rowwise_store_scales(const EncodeArgs& a, int r,
 // ---------------------------------------------------------------- columnwise
 
 // Codes and scales of column pair (cl, cl + 1) over rows [rb0, rb0 + RG).
-template <typename T, int RG, bool FOS, bool B2D>
-__device__ __forceinline__ void colwise_compute(const uint8_t* stage, const StageMeta& m,
+template <typename T, int RG, bool FOS, bool B2D, typename M>
+__device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m,
                                                 const EncodeArgs& a, int cl, int rb0,
                                                 const int32_t (&coff)[8], float S_t, float A_t,
                                                 uint32_t (&w0)[RG / 8], uint32_t (&w1)[RG / 8],
@@ -254,8 +286,8 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const Stag
   constexpr int NB = RG / 16;
   const float S0 = a.row_scaled ? m.colS[cl] : S_t;
   const float S1 = a.row_scaled ? m.colS[cl + 1] : S_t;
-  const float A0 = a.row_scaled ? m.colA[cl] : A_t;
-  const float A1 = a.row_scaled ? m.colA[cl + 1] : A_t;
+  const float A0 = a.row_scaled ? m.colA(cl) : A_t;
+  const float A1 = a.row_scaled ? m.colA(cl + 1) : A_t;
   sc0 = sc1 = 0;
 #pragma unroll
   for (int jb = 0; jb < NB; ++jb) {
@@ -299,8 +331,8 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const Stag
     float e2 = 0.0f;
     if constexpr (B2D) {
       const int sub = ((rb0 >> 4) + jb) * (G::TILEC / 16) + cl / 16;
-      s2 = m.s2d[sub];
-      e2 = m.e2d[sub];
+      s2 = m.s2d(sub);
+      e2 = m.e2d(sub);
     }
     sc0 |= encode_block<FOS, B2D, sizeof(T) == 2>(x0, b0, S0, A0, a.F_inv, s2, e2, w0[2 * jb], w0[2 * jb + 1])
            << (8 * jb);
@@ -366,8 +398,8 @@ __device__ __forceinline__ void colwise_store(const EncodeArgs& a, int cl, int r
 
 // One consumer thread per 16x16 sub-tile picks its scale (with four-over-six:
 // its target, by the error summed in row-major order inside the sub-tile).
-template <typename T, bool FOS>
-__device__ __forceinline__ void subtile_scales(const uint8_t* stage, StageMeta& m, float S,
+template <typename T, bool FOS, typename M>
+__device__ __forceinline__ void subtile_scales(const uint8_t* stage, M& m, float S,
                                                float amax, float F_inv, int t) {
   using G = TileGeo<T>;
   constexpr int SUBC = G::TILEC / 16, NSUB = (kTileRows / 16) * SUBC;
@@ -417,8 +449,7 @@ __device__ __forceinline__ void subtile_scales(const uint8_t* stage, StageMeta& 
     }
     if (err4 < err6) e6 = e4;
   }
-  m.s2d[t] = e6.s8;
-  m.e2d[t] = e6.e;
+  m.set_2d(t, e6.s8, e6.e);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -460,12 +491,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[NS];
   __shared__ __align__(8) uint64_t empty[NS];
-  __shared__ StageMeta meta[NS];
-  // Columnwise scale bytes of the first tile row of a pair, per tile of the
-  // super-strip row and column, held until the CTA reaches the second tile row
-  // (4 tiles later in its walk): [tile in super-strip][column][row half].
+  __shared__ StageMetaT<FOS || B2D> meta[NS];
+  // Columnwise scale bytes of the first three tile rows of a column's 32-byte
+  // scale sector, per tile of the super-strip row and column, held until the CTA
+  // reaches the fourth (4 tiles apart in its walk): [tile][column][visit][row half].
   __shared__ uint32_t csb[SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? TileGrid::kGroup : 1]
-                         [SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? 128 : 1][2];
+                         [SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? 128 : 1][3][2];
   __shared__ volatile int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -554,18 +585,18 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       if (rs) {
         float rn[RPL], cn[CPL];
         if (k + 1 < count) load_amax(k + 1, rn, cn);
-        StageMeta& m = meta[s];
+        auto& m = meta[s];
         if (ROW) {
 #pragma unroll
           for (int i = 0; i < RPL; ++i) {
-            m.rowA[lane + 32 * i] = ra[i];
+            m.set_rowA(lane + 32 * i, ra[i]);
             m.rowS[lane + 32 * i] = global_scale(ra[i], a.F);
           }
         }
         if (COL) {
 #pragma unroll
           for (int i = 0; i < CPL; ++i) {
-            m.colA[lane + 32 * i] = ca[i];
+            m.set_colA(lane + 32 * i, ca[i]);
             m.colS[lane + 32 * i] = global_scale(ca[i], a.F);
           }
         }
@@ -653,7 +684,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     if constexpr (B2D) consumer_sync();  // every consumer sees the same abort decision
     if (abort_flag) break;
     const uint8_t* stage = smem + s * kTileBytes;
-    StageMeta& m = meta[s];
+    auto& m = meta[s];
     const bool fast = a.vec_ok && tm < a.full_m && tn < a.full_n;
     uint8_t* staging = staging0 + (k % kStagingBuffers) * kStagingPerWarp;
     if constexpr (B2D) {
@@ -825,42 +856,48 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
                          ((int64_t)tm * kTileRows + rb0) / 2;
           stg_v8_cs(c0p, w0);
           stg_v8_cs(c0p + a.col_cpitch, w1);
-          bool paired_scales = false;
+          bool sector_scales = false;
           if constexpr (PAIRED) {
-            // Tile rows 2p and 2p + 1 of this tile column are 4 tiles apart in the
-            // walk.  When both lie in this CTA's chunk and are full tiles, the first
-            // one visited parks its scale bytes in csb and the second writes the
-            // column's 16 bytes for both: lane hh = 0 the bytes of tile row 2p,
-            // lane hh = 1 those of 2p + 1, one coalesced request per column.
-            const int p0 = tm & ~1;
-            const int Lp0 = cur.ss * a.grid.tiles_m * TileGrid::kGroup + p0 * cur.wdt + cur.jt;
-            paired_scales = a.col_scale_pairs && p0 + 1 < a.full_m && Lp0 >= begin &&
-                            Lp0 + cur.wdt < end;
-            if (paired_scales) {
-              const bool first = fwd ? tm == p0 : tm != p0;
-              if (first) {
-                csb[cur.jt][cl][hh] = sc0;
-                csb[cur.jt][cl + 1][hh] = sc1;
+            // Tile rows 4p .. 4p + 3 of this tile column make up one 32-byte sector of
+            // each column's scale row and are 4 tiles apart in the walk.  When all four
+            // are full tiles of this CTA's chunk, the first three visited park their
+            // scale bytes in csb and the last writes the column's sector in one
+            // coalesced request: lane hh = 0 bytes 0-15 (tile rows 4p, 4p + 1),
+            // lane hh = 1 bytes 16-31 (tile rows 4p + 2, 4p + 3).
+            const int q0 = tm & ~3, q = tm & 3;
+            const int L0 = cur.ss * a.grid.tiles_m * TileGrid::kGroup + q0 * cur.wdt + cur.jt;
+            sector_scales = a.col_scale_sectors && q0 + 3 < a.full_m && L0 >= begin &&
+                            L0 + 3 * cur.wdt < end;
+            if (sector_scales) {
+              const int v = fwd ? q : 3 - q;  // visit index inside the sector
+              if (v < 3) {
+                csb[cur.jt][cl][v][hh] = sc0;
+                csb[cur.jt][cl + 1][v][hh] = sc1;
               } else {
                 const uint32_t o0 = __shfl_xor_sync(0xffffffffu, sc0, 1);
                 const uint32_t o1 = __shfl_xor_sync(0xffffffffu, sc1, 1);
                 // this tile's 8 bytes of each column: row half 0, then row half 1
                 const uint2 t0 = hh ? make_uint2(o0, sc0) : make_uint2(sc0, o0);
                 const uint2 t1 = hh ? make_uint2(o1, sc1) : make_uint2(sc1, o1);
-                const uint2 q0 = make_uint2(csb[cur.jt][cl][0], csb[cur.jt][cl][1]);
-                const uint2 q1 = make_uint2(csb[cur.jt][cl + 1][0], csb[cur.jt][cl + 1][1]);
-                // lane hh writes the bytes of tile row p0 + hh
-                const bool mine = (hh == 1) == (tm != p0);
-                const uint2 v0 = mine ? t0 : q0, v1 = mine ? t1 : q1;
+                uint2 r0[2], r1[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  const int qq = 2 * hh + i;  // tile row q0 + qq
+                  const int vv = fwd ? qq : 3 - qq;
+                  const bool here = qq == q;
+                  const int vs = here ? 0 : vv;
+                  r0[i] = here ? t0 : make_uint2(csb[cur.jt][cl][vs][0], csb[cur.jt][cl][vs][1]);
+                  r1[i] = here ? t1
+                               : make_uint2(csb[cur.jt][cl + 1][vs][0], csb[cur.jt][cl + 1][vs][1]);
+                }
                 uint8_t* s0p = a.col_scales + ((int64_t)tn * G::TILEC + cl) * a.col_spitch +
-                               (int64_t)p0 * (kTileRows / 16) + 8 * hh;
-                const uint64_t keep = policy_evict_last();
-                stg_v2_keep(s0p, v0.x, v0.y, keep);
-                stg_v2_keep(s0p + a.col_spitch, v1.x, v1.y, keep);
+                               (int64_t)q0 * (kTileRows / 16) + 16 * hh;
+                stg_v4_cs(s0p, make_uint4(r0[0].x, r0[0].y, r0[1].x, r0[1].y));
+                stg_v4_cs(s0p + a.col_spitch, make_uint4(r1[0].x, r1[0].y, r1[1].x, r1[1].y));
               }
             }
           }
-          if (!paired_scales)
+          if (!sector_scales)
             colwise_store<T, RG, false>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, true);
         } else {
           colwise_store<T, RG, true>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, false);
@@ -979,7 +1016,7 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
           a.col_spitch % cs == 0 && aligned(q.col_scales, cs);
   }
   a.vec_ok = vec ? 1 : 0;
-  a.col_scale_pairs = (both && bf16 && a.col_spitch % 16 == 0 && aligned(q.col_scales, 16)) ? 1 : 0;
+  a.col_scale_sectors = (both && bf16 && a.col_spitch % 32 == 0 && aligned(q.col_scales, 32)) ? 1 : 0;
   a.row_scale_groups = (tout && both && bf16 && a.row_spitch % 32 == 0 &&
                         aligned(q.row_scales, 32)) ? 1 : 0;
 
@@ -989,6 +1026,10 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
                    : outm == kOutSector ? EncodeSmem<kOutSector>::kBytes
                                         : EncodeSmem<kOutDirect>::kBytes;
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  // two CTAs per SM need nearly all of the SM's shared memory
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pipe_grid_size(a.grid.num_tiles, dev.num_sms));
