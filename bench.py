@@ -214,7 +214,8 @@ def run_ours(args):
 
     x, dy = workloads.linear(dev, rows=args.rows)
     ops = [x, dy]
-    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+    fos = args.workload == "linear-fos"
+    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, int(fos), 0)
     outs = []
     for t in ops:
         r, c = t.shape
@@ -288,12 +289,14 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "metric": METRIC if not fos else METRIC + ", four-over-six",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "pct_of_hbm_peak": 100.0 * value / world / peak,
             "config": {
-                "workload": WORKLOAD,
+                "workload": WORKLOAD + (", four-over-six (T in {6, 4} by squared error)"
+                                        if fos else ""),
                 "l2": "inputs larger than L2 (268 MB, 940 MB) and a 256 MB L2 flush before each step",
                 "bytes_io_per_step": bio, "bytes_min_per_step": bmin,
                 "elements_per_step": elems,
@@ -307,7 +310,8 @@ def run_ours(args):
             "roofline": {"kernel": "k_encode (encode pass)", "bound": "hbm",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": ENCODE_TRAFFIC_BYTES if args.rows == ROWS else None,
+                         "traffic": (ENCODE_TRAFFIC_BYTES if args.rows == ROWS and not fos
+                                     else None),
                          "algorithmic_bytes": enc_bytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -315,6 +319,148 @@ def run_ours(args):
             "clocks": clocks,
         }
         print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- other rows of the path
+
+SUPPLEMENTARY = {
+    "weights16x16": "weights 8192x8192 BF16 N(0,0.02), per-tensor amax, 16x16 block scales, "
+                    "rowwise + columnwise (tensor amax pass, then the encode pass)",
+    "moe": "MoE tokens: 32 groups, counts Multinomial(65536, uniform), each zero-padded to a "
+           "multiple of 128 rows, K 7168, N(0,1) BF16; grouped amax -> per-row expansion -> "
+           "rowwise quantize, four-over-six, bound 256",
+    "dequant": "dequantize of a row-scaled 4096x4096 quantization (0.1 % outliers x50): "
+               "rowwise codes -> BF16 and columnwise codes -> FP32",
+}
+
+
+def run_supplementary(args):
+    """One JSON line for a row of the path other than the headline workload: same
+    timing rules (warm-up, 256 MB L2 flush before each step, CUDA events on the
+    launching stream, clocks sampled during the timed region)."""
+    import torch
+
+    import nvfp4_precision_quantization_gb300 as nv
+    import workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    nv.load_library()
+    w = args.workload
+    if w == "weights16x16":
+        x = workloads.edge_normal(8192, 8192, torch.bfloat16, dev, std=0.02)
+        M, K = x.shape
+        cfg = nv.Config(nv.NVFP4_PER_TENSOR, 448.0, 0, 1)
+        t = torch.empty(1, dtype=torch.float32, device=dev)
+        row, col = nv.alloc_out(M, K, 1, dev), nv.alloc_out(K, M, 1, dev)
+        row.amax, col.amax, row.amax_in, col.amax_in = t, t, t, t
+
+        def step(ev):
+            nv.nvfp4_amax(x, tensor_amax=t, stream=stream)
+            ev[0].record(stream)
+            nv.nvfp4_quantize_both(x, cfg, row, col, stream=stream)
+        bio = 2 * M * K + 2 * (M * K // 2 + M * K // 16) + 8
+        bmin = bio + 2 * M * K
+        kern, kbytes, launches = "k_encode (16x16)", bio - 4, 3
+        dtype, elems = "bf16", M * K
+    elif w == "moe":
+        x, ends, _, _ = workloads.moe(dev)
+        M, K = x.shape
+        G = ends.numel()
+        cfg = nv.Config(nv.NVFP4_ROW_SCALED, 256.0, 1, 0)
+        row = nv.alloc_out(M, K, M, dev)
+        gam = torch.empty(G, dtype=torch.float32, device=dev)
+
+        def step(ev):
+            # the kernels nvfp4_grouped_quantize_rowwise (per-group amax) launches:
+            # group check, grouped amax, expansion to rows, then the rowwise encode
+            nv.nvfp4_grouped_amax(x, ends, gam, row_amax_expanded=row.amax, stream=stream)
+            ev[0].record(stream)
+            row.amax_in = row.amax
+            nv.nvfp4_quantize_rowwise(x, cfg, row, stream=stream)
+        bio = 2 * M * K + M * K // 2 + M * K // 16 + 4 * M + 4 * G
+        bmin = bio + 2 * M * K
+        kern, kbytes, launches = "k_encode (rowwise, four-over-six)", bio - 4 * G, 4
+        dtype, elems = "bf16", M * K
+    elif w == "dequant":
+        x = workloads.outliers(dev)
+        M, K = x.shape
+        cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+        row, col = nv.alloc_out(M, K, M, dev), nv.alloc_out(K, M, K, dev)
+        nv.nvfp4_quantize_both(x, cfg, row, col, stream=stream)
+        out_bf16 = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        out_f32 = torch.empty(K, M, dtype=torch.float32, device=dev)
+
+        def step(ev):
+            nv.nvfp4_dequantize(row.codes, row.scales, row.amax, nv.NVFP4_ROW_SCALED, M, K, 448.0,
+                                out_bf16, stream=stream)
+            ev[0].record(stream)
+            nv.nvfp4_dequantize(col.codes, col.scales, col.amax, nv.NVFP4_ROW_SCALED, K, M, 448.0,
+                                out_f32, stream=stream)
+        codes_scales = M * K // 2 + M * K // 16
+        bio = (codes_scales + 4 * M + 2 * M * K) + (codes_scales + 4 * K + 4 * M * K)
+        bmin = bio
+        kern, kbytes, launches = "k_dequantize (FP32 out)", codes_scales + 4 * K + 4 * M * K, 2
+        dtype, elems = "f32", 2 * M * K
+    else:
+        raise SystemExit(f"unknown workload {w}")
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step([torch.cuda.Event(enable_timing=True)])
+    torch.cuda.synchronize()
+    K_ = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K_)]
+    ends_ = [torch.cuda.Event(enable_timing=True) for _ in range(K_)]
+    mids = [[torch.cuda.Event(enable_timing=True)] for _ in range(K_)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    for k in range(K_):
+        flush.zero_()
+        starts[k].record(stream)
+        step(mids[k])
+        ends_[k].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends_)]
+    t_total, rate = job_throughput(sum(step_ms) / 1e3, world, bio, K_, dev)
+    kern_ms = statistics.mean(m[0].elapsed_time(e) for m, e in zip(mids, ends_))
+    peak, peak_src = measured_peaks()
+    achieved = kbytes / (kern_ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": f"NVFP4 {w} GB/s (algorithmic bytes in + out) and % of GB300 HBM peak",
+            "value": rate / 1e9, "unit": "GB/s", "n_gpus": world, "steps": K_,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K_, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "pct_of_hbm_peak": 100.0 * rate / 1e9 / world / peak,
+            "config": {"workload": SUPPLEMENTARY[w],
+                       "l2": "a 256 MB L2 flush before each step",
+                       "bytes_io_per_step": bio, "bytes_min_per_step": bmin,
+                       "gbps_bytes_min": world * bmin * K_ / t_total / 1e9,
+                       "pct_of_hbm_peak_bytes_min": 100.0 * bmin * K_ / t_total / 1e9 / peak,
+                       "elements_per_s": world * elems * K_ / t_total,
+                       "peak_gbs": peak, "peak_source": peak_src},
+            "roofline": {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": None, "algorithmic_bytes": kbytes},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": launches * K_,
+            "clocks": clocks}))
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -367,9 +513,16 @@ def main():
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows of X and dY (default 16384; smaller only for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="linear",
+                    choices=["linear", "linear-fos", *SUPPLEMENTARY],
+                    help="linear (default): the headline workload; the others measure the "
+                         "remaining rows of the path (four-over-six, 16x16 weights, grouped "
+                         "MoE, dequantize), one JSON line each")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in SUPPLEMENTARY:
+        run_supplementary(args)
     else:
         run_ours(args)
 

@@ -6,8 +6,10 @@
 // BF16 output rounded to nearest even from the FP32 value.
 //
 // The kernel is write-bound (0.5625 bytes in, 2 or 4 bytes out per element): a
-// thread expands one 16-element block (8 code bytes + 1 scale byte) into 32 or
-// 64 contiguous output bytes, so a warp writes 1 or 2 KB contiguous.
+// thread expands 8 consecutive values (4 code bytes and their block's scale) into
+// 16 (BF16) or 32 (FP32) contiguous output bytes, so one store instruction of a
+// warp writes 512 B or 1 KB of contiguous output.  A CTA works on 2048-value
+// segments of one row at a time (the row index is computed once per segment).
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -24,64 +26,69 @@ struct DequantKernelArgs {
   const uint8_t* scales;
   const float* amax;
   int row_scaled;
-  int64_t rows, cols, nblk;
+  int64_t rows, cols;
   int64_t cpitch, spitch;
   float F_inv;
   void* out;
 };
 
+constexpr int kDqThreads = 256;
+constexpr int kDqPerThread = 8;
+constexpr int kDqSegment = kDqThreads * kDqPerThread;  // values of a row per CTA item
+
 template <bool BF16, bool VEC>
-__global__ void __launch_bounds__(256) k_dequantize(DequantKernelArgs a) {
-  const int64_t total = a.rows * a.nblk;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / a.nblk, j = i % a.nblk;
-    const int64_t c0 = j * 16;
-    const int n = (a.cols - c0) < 16 ? (int)(a.cols - c0) : 16;
+__global__ void __launch_bounds__(kDqThreads) k_dequantize(DequantKernelArgs a) {
+  const int64_t per_row = (a.cols + kDqSegment - 1) / kDqSegment;
+  const int64_t items = a.rows * per_row;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int64_t r = it / per_row;
+    const int64_t c0 = (it - r * per_row) * kDqSegment + (int64_t)threadIdx.x * kDqPerThread;
+    if (c0 >= a.cols) continue;
+    const int n = (a.cols - c0) < kDqPerThread ? (int)(a.cols - c0) : kDqPerThread;
     const float amax = a.amax[a.row_scaled ? r : 0];
-    const float D = dequant_factor(e4m3_value(a.scales[r * a.spitch + j]), amax, a.F_inv);
+    const float D = dequant_factor(e4m3_value(a.scales[r * a.spitch + c0 / 16]), amax, a.F_inv);
     const uint8_t* cp = a.codes + r * a.cpitch + c0 / 2;
-    uint32_t w[2];
-    if (VEC && n == 16) {
-      const uint2 u = *reinterpret_cast<const uint2*>(cp);
-      w[0] = u.x;
-      w[1] = u.y;
+    uint32_t w;
+    if (VEC && n == kDqPerThread) {
+      w = *reinterpret_cast<const uint32_t*>(cp);
     } else {
-      w[0] = w[1] = 0;
-      for (int b = 0; b < (n + 1) / 2; ++b) w[b >> 2] |= (uint32_t)cp[b] << (8 * (b & 3));
+      w = 0;
+      for (int b = 0; b < (n + 1) / 2; ++b) w |= (uint32_t)cp[b] << (8 * b);
     }
-    float v[16];
+    float v[kDqPerThread];
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
+    for (int b = 0; b < kDqPerThread / 2; ++b) {
       float lo, hi;
-      e2m1x2_values(w[b >> 2] >> (8 * (b & 3)), lo, hi);
+      e2m1x2_values(w >> (8 * b), lo, hi);
       v[2 * b] = __fmul_rn(lo, D);
       v[2 * b + 1] = __fmul_rn(hi, D);
     }
     if constexpr (BF16) {
       __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + r * a.cols + c0;
-      if (VEC && n == 16) {
-        uint32_t p[8];
+      if (VEC && n == kDqPerThread) {
+        uint32_t p[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
           __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
           p[k] = *reinterpret_cast<uint32_t*>(&h);
         }
         stg_v4_cs(o, make_uint4(p[0], p[1], p[2], p[3]));
-        stg_v4_cs(o + 8, make_uint4(p[4], p[5], p[6], p[7]));
       } else {
-        for (int k = 0; k < n; ++k) o[k] = __float2bfloat16_rn(v[k]);
+#pragma unroll
+        for (int k = 0; k < kDqPerThread; ++k)
+          if (k < n) o[k] = __float2bfloat16_rn(v[k]);
       }
     } else {
       float* o = static_cast<float*>(a.out) + r * a.cols + c0;
-      if (VEC && n == 16) {
+      if (VEC && n == kDqPerThread) {
+        uint32_t p[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          stg_v4_cs(o + 4 * k, make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
-                                          __float_as_uint(v[4 * k + 2]),
-                                          __float_as_uint(v[4 * k + 3])));
+        for (int k = 0; k < 8; ++k) p[k] = __float_as_uint(v[k]);
+        stg_v8_cs(o, p);
       } else {
-        for (int k = 0; k < n; ++k) o[k] = v[k];
+#pragma unroll
+        for (int k = 0; k < kDqPerThread; ++k)
+          if (k < n) o[k] = v[k];
       }
     }
   }
@@ -118,22 +125,22 @@ cudaError_t launch_dequantize(const DequantArgs& q, const DeviceInfo& dev, cudaS
   a.row_scaled = q.row_scaled ? 1 : 0;
   a.rows = q.rows;
   a.cols = q.cols;
-  a.nblk = (q.cols + 15) / 16;
   a.cpitch = (q.cols + 1) / 2;
   a.spitch = (q.cols + 15) / 16;
   a.F_inv = 1.0f / (q.bound * 6.0f);
   a.out = q.out;
-  const int64_t total = a.rows * a.nblk;
-  if (total == 0) return cudaSuccess;
+  if (a.rows == 0 || a.cols == 0) return cudaSuccess;
+  // whole 8-value groups: 4-byte code loads and 16-byte (BF16) / 32-byte (FP32)
+  // stores, which need the row pitches and bases aligned to those sizes
   const int elem = q.out_bf16 ? 2 : 4;
-  const bool vec = (a.cpitch % 8 == 0) && ((q.cols * elem) % 16 == 0) &&
-                   (reinterpret_cast<uintptr_t>(q.codes) % 8 == 0) &&
-                   (reinterpret_cast<uintptr_t>(q.out) % 16 == 0);
-  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 8LL * dev.num_sms);
+  const bool vec = (q.cols % 8 == 0) && (reinterpret_cast<uintptr_t>(q.codes) % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(q.out) % (8 * elem) == 0);
+  const int64_t items = a.rows * ((a.cols + kDqSegment - 1) / kDqSegment);
+  const int64_t blocks = std::min<int64_t>(items, 8LL * dev.num_sms);
   void (*fn)(DequantKernelArgs);
   if (q.out_bf16) fn = vec ? k_dequantize<true, true> : k_dequantize<true, false>;
   else fn = vec ? k_dequantize<false, true> : k_dequantize<false, false>;
-  fn<<<(unsigned)blocks, 256, 0, stream>>>(a);
+  fn<<<(unsigned)blocks, kDqThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
