@@ -452,6 +452,35 @@ __device__ __forceinline__ void subtile_scales(const uint8_t* stage, M& m, float
   m.set_2d(t, e6.s8, e6.e);
 }
 
+// 16x16 sub-tile scales without four-over-six (BF16): the scale needs only the
+// sub-tile's max, so all 256 consumer threads take part.  Thread (row r, box h)
+// reads its 128-byte box row (the rowwise access pattern: conflict free), takes
+// the max of each of its 4 blocks of 16 values, and the 16 rows of a sub-tile --
+// lanes 0-15 or 16-31 of the warp -- combine theirs with 4 shuffle steps; the
+// first lane of the 16 encodes the 4 sub-tile scales.
+template <typename M>
+__device__ __forceinline__ void subtile_scales_max(const uint8_t* stage, M& m, float S, int t) {
+  const int r = t & (kTileRows - 1), h = t >> 7;
+  const uint8_t* rowp = stage + h * kBoxBytes + r * 128;
+  const int sw = r & 7;
+  float bmax[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    bmax[j] = absmax8_bf16(lds128(rowp + (((2 * j) ^ sw) << 4)),
+                           lds128(rowp + (((2 * j + 1) ^ sw) << 4)));
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) bmax[j] = fmaxf(bmax[j], __shfl_xor_sync(0xffffffffu, bmax[j], o));
+  if ((r & 15) == 0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const BlockEnc e = block_encode<6, true>(bmax[j], S);
+      m.set_2d((r >> 4) * (TileGeo<uint16_t>::TILEC / 16) + h * 4 + j, e.s8, e.e);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 
 // Staging bytes per consumer warp for the TMA stores of its codes, per buffer.
@@ -688,7 +717,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     const bool fast = a.vec_ok && tm < a.full_m && tn < a.full_n;
     uint8_t* staging = staging0 + (k % kStagingBuffers) * kStagingPerWarp;
     if constexpr (B2D) {
-      subtile_scales<T, FOS>(stage, m, ROW ? S_r : S_c, ROW ? A_r : A_c, a.F_inv, tid);
+      if constexpr (!FOS && sizeof(T) == 2)
+        subtile_scales_max(stage, m, ROW ? S_r : S_c, tid);
+      else
+        subtile_scales<T, FOS>(stage, m, ROW ? S_r : S_c, ROW ? A_r : A_c, a.F_inv, tid);
       consumer_sync();
     }
     if (PAIRED && is_row) {
