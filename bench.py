@@ -333,6 +333,9 @@ SUPPLEMENTARY = {
            "rowwise quantize, four-over-six, bound 256",
     "dequant": "dequantize of a row-scaled 4096x4096 quantization (0.1 % outliers x50): "
                "rowwise codes -> BF16 and columnwise codes -> FP32",
+    "moe-ragged": "MoE tokens as above, quantized straight from the unpadded tokens into the "
+                  "padded layout (padding rows not read): per-group amax, four-over-six, "
+                  "bound 256, rowwise",
 }
 
 
@@ -390,6 +393,26 @@ def run_supplementary(args):
         bio = 2 * M * K + M * K // 2 + M * K // 16 + 4 * M + 4 * G
         bmin = bio + 2 * M * K
         kern, kbytes, launches = "k_encode (rowwise, four-over-six)", bio - 4 * G, 4
+        dtype, elems = "bf16", M * K
+    elif w == "moe-ragged":
+        xp, pad_ends, counts, padded = workloads.moe(dev)
+        x, rag_ends = workloads.moe_ragged(xp, counts, padded)
+        x, rag_ends = x.contiguous(), rag_ends.to(dev)
+        del xp
+        T, K = x.shape
+        M = int(padded.sum())
+        G = len(counts)
+        cfg = nv.Config(nv.NVFP4_PER_TENSOR, 256.0, 1, 0)
+        row = nv.alloc_out(M, K, M, dev)
+        gam = torch.empty(G, dtype=torch.float32, device=dev)
+
+        def step(ev):
+            ev[0].record(stream)
+            nv.nvfp4_grouped_quantize_rowwise_padded(x, rag_ends, pad_ends, M, cfg, row, gam,
+                                                     stream=stream)
+        bio = 2 * T * K + M * K // 2 + M * K // 16 + 4 * M + 4 * G
+        bmin = bio + 2 * T * K
+        kern, kbytes, launches = "whole step (check, grouped amax, expand, rowwise encode)", bio, 4
         dtype, elems = "bf16", M * K
     elif w == "dequant":
         x = workloads.outliers(dev)

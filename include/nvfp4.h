@@ -184,6 +184,30 @@ NVFP4_API nvfp4_status nvfp4_grouped_quantize_rowwise(const void *x, int32_t in_
                                             const nvfp4_out *row, float *group_amax,
                                             const float *noop, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_grouped_quantize_rowwise_padded -- rowwise quantize of grouped tokens
+ * straight from the ragged (unpadded) tensor into the padded layout that "Add NVFP4
+ * four-over-six grouped GEMM for MoE training" (torchao PR #9, description) pads
+ * each group to; the result is bit-identical to zero-padding x into that layout and
+ * calling nvfp4_grouped_quantize_rowwise (NVFP4_PER_TENSOR: each group's amax),
+ * without reading or materialising the padding rows.
+ *   x: device [tokens][cols] (BF16 or FP32), the groups' rows back to back.
+ *   ragged_ends: device int64 [num_groups], cumulative token ends (last == tokens).
+ *   padded_ends: device int64 [num_groups], cumulative padded ends (last ==
+ *   padded_rows); every padded group is at least as long as its ragged group and
+ *   starts on a multiple of 128 rows.
+ *   row->codes [padded_rows][ceil(cols/2)], row->scales [padded_rows][ceil(cols/16)],
+ *   row->amax [padded_rows] receives each padded row's group amax; row->amax_in must be
+ *   NULL.  Padding rows get zero codes and zero scales.
+ *   group_amax [num_groups] (required).
+ *   cfg->mode must be NVFP4_PER_TENSOR (NVFP4_ERR_UNSUPPORTED otherwise), cfg->block_2d 0.
+ *   Invalid ends or layouts set NVFP4_DEVICE_BAD_GROUPS and nothing is written.
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_quantize_rowwise_padded(
+    const void *x, int32_t in_dtype, int64_t tokens, int64_t cols, const int64_t *ragged_ends,
+    const int64_t *padded_ends, int32_t num_groups, int64_t padded_rows, const nvfp4_config *cfg,
+    const nvfp4_out *row, float *group_amax, const float *noop, nvfp4_stream_t stream);
+
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 NVFP4_API const char *nvfp4_last_error(void);
 

@@ -24,6 +24,7 @@ __all__ = [
     "Config", "Out", "NVFP4Error", "load_library", "library_path",
     "nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise", "nvfp4_quantize_both",
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
+    "nvfp4_grouped_quantize_rowwise_padded",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "alloc_out", "EXPORTED_SYMBOLS",
 ]
@@ -45,6 +46,7 @@ NVFP4_DEVICE_BAD_GROUPS = 2
 EXPORTED_SYMBOLS = (
     "nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise", "nvfp4_quantize_both",
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
+    "nvfp4_grouped_quantize_rowwise_padded",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
 )
 
@@ -108,6 +110,8 @@ def load_library():
         "nvfp4_dequantize": [vp, vp, vp, i32, i64, i64, f32, vp, i32, vp],
         "nvfp4_grouped_amax": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp],
         "nvfp4_grouped_quantize_rowwise": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp, vp],
+        "nvfp4_grouped_quantize_rowwise_padded": [vp, i32, i64, i64, vp, vp, i32, i64, vp, vp,
+                                                  vp, vp, vp],
         "nvfp4_device_status": [C.POINTER(C.c_int32), i32],
         "nvfp4_selftest_convert": [vp, i64, vp, vp, vp],
     }
@@ -221,6 +225,18 @@ def nvfp4_grouped_quantize_rowwise(x: torch.Tensor, group_ends: torch.Tensor, cf
     _check(load_library().nvfp4_grouped_quantize_rowwise(
         _ptr(x), _in_dtype(x), rows, cols, _ptr(group_ends), int(group_ends.numel()),
         C.byref(cfg), C.byref(r), _ptr(group_amax), _ptr(noop), _stream(stream)))
+
+
+def nvfp4_grouped_quantize_rowwise_padded(x: torch.Tensor, ragged_ends: torch.Tensor,
+                                          padded_ends: torch.Tensor, padded_rows: int,
+                                          cfg: Config, row: Out, group_amax: torch.Tensor,
+                                          noop=None, stream=None) -> None:
+    tokens, cols = _matrix(x)
+    r = row._c()
+    _check(load_library().nvfp4_grouped_quantize_rowwise_padded(
+        _ptr(x), _in_dtype(x), tokens, cols, _ptr(ragged_ends), _ptr(padded_ends),
+        int(ragged_ends.numel()), int(padded_rows), C.byref(cfg), C.byref(r), _ptr(group_amax),
+        _ptr(noop), _stream(stream)))
 
 
 def nvfp4_device_status(reset: bool = False) -> int:

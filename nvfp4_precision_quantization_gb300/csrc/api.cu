@@ -463,6 +463,85 @@ nvfp4_status nvfp4_grouped_quantize_rowwise(const void* x, int32_t in_dtype, int
                        num_groups);
 }
 
+nvfp4_status nvfp4_grouped_quantize_rowwise_padded(
+    const void* x, int32_t in_dtype, int64_t tokens, int64_t cols, const int64_t* ragged_ends,
+    const int64_t* padded_ends, int32_t num_groups, int64_t padded_rows, const nvfp4_config* cfg,
+    const nvfp4_out* row, float* group_amax, const float* noop, nvfp4_stream_t stream) {
+  nvfp4_status st;
+  if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
+  if ((st = check_sizes(tokens, cols)) != NVFP4_OK) return st;
+  if ((st = check_sizes(padded_rows, cols)) != NVFP4_OK) return st;
+  if ((st = check_config(cfg)) != NVFP4_OK) return st;
+  if (cfg->mode != NVFP4_PER_TENSOR)
+    return fail(NVFP4_ERR_UNSUPPORTED,
+                "padded grouped quantize uses each group's amax (cfg->mode NVFP4_PER_TENSOR)");
+  if (num_groups < 1 || num_groups > 4096)
+    return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
+  if (ragged_ends == nullptr || padded_ends == nullptr || group_amax == nullptr)
+    return fail(NVFP4_ERR_INVALID, "ragged_ends, padded_ends and group_amax must be non-NULL");
+  if (row == nullptr) return fail(NVFP4_ERR_INVALID, "row is NULL");
+  if (row->amax_in != nullptr)
+    return fail(NVFP4_ERR_INVALID, "grouped quantize computes its amax: row->amax_in must be NULL");
+  if ((st = check_out(row, "row", padded_rows, cols, padded_rows)) != NVFP4_OK) return st;
+  if (x == nullptr && tokens * cols > 0) return fail(NVFP4_ERR_INVALID, "x is NULL");
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+  const InType in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+  // 1. both layouts valid?  zero the group maxima
+  GroupCheckArgs g{};
+  g.M = padded_rows;
+  g.group_ends = padded_ends;
+  g.num_groups = num_groups;
+  g.noop = noop;
+  g.rag_ends = ragged_ends;
+  g.in_rows = tokens;
+  g.prep.zero_ptr[0] = group_amax;
+  g.prep.zero_n[0] = num_groups;
+  g.prep.noop = noop;
+  cudaError_t e = launch_group_check(g, dev, stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "group check launch");
+  // 2. group maxima over the ragged rows
+  GroupedAmaxArgs a{};
+  a.x = x;
+  a.in = in;
+  a.M = tokens;
+  a.K = cols;
+  a.group_ends = ragged_ends;
+  a.num_groups = num_groups;
+  a.group_amax = group_amax;
+  a.noop = noop;
+  a.pad_ends = padded_ends;
+  a.pad_rows = padded_rows;
+  if ((e = launch_grouped_amax(a, dev, stream)) != cudaSuccess)
+    return cuda_fail(e, "grouped amax launch");
+  // 3. every padded row (padding included) takes its group's amax
+  g.prep = PrepArgs{};
+  g.group_amax = group_amax;
+  g.expand = row->amax;
+  if ((e = launch_group_check(g, dev, stream, true)) != cudaSuccess)
+    return cuda_fail(e, "group expand launch");
+  // 4. rowwise encode of the padded rows, reading only the ragged rows of x
+  QuantArgs q{};
+  q.x = x;
+  q.in = in;
+  q.M = padded_rows;
+  q.K = cols;
+  q.row_scaled = true;
+  q.four_over_six = cfg->four_over_six != 0;
+  q.block_2d = false;
+  q.bound = cfg->bound;
+  q.noop = noop;
+  q.num_groups = num_groups;
+  q.row_codes = row->codes;
+  q.row_scales = row->scales;
+  q.row_amax = row->amax;
+  q.pad_ends = padded_ends;
+  q.rag_ends = ragged_ends;
+  q.in_rows = tokens;
+  if ((e = launch_quantize(q, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize");
+  return NVFP4_OK;
+}
+
 const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
 
 nvfp4_status nvfp4_device_status(int32_t* status, int32_t reset) {

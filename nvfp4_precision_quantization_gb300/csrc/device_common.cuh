@@ -44,6 +44,24 @@ __device__ __forceinline__ bool groups_valid(const int64_t* ends, int G, int64_t
   return !__syncthreads_or(bad);
 }
 
+// Ragged tokens quantized into a padded layout: group g has ragged rows
+// [rag_ends[g-1], rag_ends[g]) of x and padded output rows [pad_ends[g-1],
+// pad_ends[g]).  Valid when both are non-decreasing, end at their row counts, every
+// padded group is at least as long as its ragged one and starts on a 128-row tile
+// boundary.  Every thread of the block must call it.
+__device__ __forceinline__ bool pad_layout_valid(const int64_t* rag_ends, const int64_t* pad_ends,
+                                                 int G, int64_t in_rows, int64_t out_rows) {
+  int bad = 0;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const int64_t re = rag_ends[g], rp = g ? rag_ends[g - 1] : 0;
+    const int64_t pe = pad_ends[g], pp = g ? pad_ends[g - 1] : 0;
+    if (re < rp || re > in_rows || (g == G - 1 && re != in_rows)) bad = 1;
+    if (pe < pp || pe > out_rows || (g == G - 1 && pe != out_rows)) bad = 1;
+    if (pe - pp < re - rp || (pp & 127) != 0) bad = 1;
+  }
+  return !__syncthreads_or(bad);
+}
+
 // ---------------------------------------------------------------- BF16 helpers
 
 // The two BF16 halves of a packed pair, widened exactly to FP32.

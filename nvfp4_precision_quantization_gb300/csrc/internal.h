@@ -52,6 +52,8 @@ struct GroupedAmaxArgs {
   int num_groups;
   float* group_amax;
   const float* noop;
+  const int64_t* pad_ends;  // optional: do nothing unless this padded layout is valid too
+  int64_t pad_rows;
 };
 cudaError_t launch_grouped_amax(const GroupedAmaxArgs& a, const DeviceInfo& dev,
                                 cudaStream_t stream);
@@ -67,6 +69,9 @@ struct GroupCheckArgs {
   float* expand;
   const float* noop;
   PrepArgs prep;
+  // optional: group_ends are padded ends of ragged x (ragged ends rag_ends, in_rows rows)
+  const int64_t* rag_ends;
+  int64_t in_rows;
 };
 cudaError_t launch_group_check(const GroupCheckArgs& a, const DeviceInfo& dev,
                                cudaStream_t stream, bool expand_pass);
@@ -94,6 +99,11 @@ struct QuantArgs {
   const float* noop;
   const int64_t* group_ends;  // optional: do nothing unless these group ends are valid
   int num_groups;
+  // optional: x is ragged (in_rows rows) and the output padded: group g's output rows
+  // [pad_ends[g-1], pad_ends[g]) take x rows from rag_ends[g-1] on (rowwise only)
+  const int64_t* pad_ends;
+  const int64_t* rag_ends;
+  int64_t in_rows;
 };
 cudaError_t launch_quantize(const QuantArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 

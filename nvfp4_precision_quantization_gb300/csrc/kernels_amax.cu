@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         break;
       }
       if (abort_flag) break;
-      issue_tile<T>(smem + s * kTileBytes, &tmap, &full[s], cur.tm, cur.tn(),
+      issue_tile<T>(smem + s * kTileBytes, &tmap, &full[s], cur.tm * kTileRows, cur.tn(),
                     k >= count - a.keep_tiles ? pol_last : pol_first);
       cur.step(a.grid, fwd);
       issued = k + 1;
@@ -663,6 +663,8 @@ struct GroupedKernelArgs {
   int* status;
   int64_t rows_per_item;
   int num_col_items;
+  const int64_t* pad_ends;  // optional: also require this padded layout of the groups
+  int64_t pad_rows;
 };
 
 // Per-group amax: like the tensor reduction, but a CTA item is split at group
@@ -673,7 +675,9 @@ __global__ void __launch_bounds__(kThreads) k_grouped_amax(GroupedKernelArgs a) 
   __shared__ int64_t s_ends[kMaxGroups];
   __shared__ float row_red[kColWarps][512];
   if (noop_set(a.noop)) return;
-  if (!load_group_ends(a.ends, a.G, a.M, s_ends)) {
+  const bool ok = load_group_ends(a.ends, a.G, a.M, s_ends);
+  if (!ok || (a.pad_ends != nullptr &&
+              !pad_layout_valid(a.ends, a.pad_ends, a.G, a.M, a.pad_rows))) {
     if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(a.status, kStatusBadGroups);
     return;
   }
@@ -730,7 +734,11 @@ __global__ void __launch_bounds__(kThreads) k_grouped_amax(GroupedKernelArgs a) 
 __global__ void k_group_check(GroupCheckArgs a, int* status, bool expand_pass) {
   __shared__ int64_t s_ends[kMaxGroups];
   if (noop_set(a.noop)) return;
-  if (!load_group_ends(a.group_ends, a.num_groups, a.M, s_ends)) {
+  const bool ok = load_group_ends(a.group_ends, a.num_groups, a.M, s_ends);
+  // padded layout: group_ends are the padded ends (M output rows), rag_ends the
+  // ragged ends of x (in_rows rows)
+  if (!ok || (a.rag_ends != nullptr && !pad_layout_valid(a.rag_ends, a.group_ends, a.num_groups,
+                                                         a.in_rows, a.M))) {
     if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(status, kStatusBadGroups);
     return;
   }
@@ -856,6 +864,8 @@ cudaError_t launch_grouped_amax(const GroupedAmaxArgs& a, const DeviceInfo& dev,
   k.group_amax = a.group_amax;
   k.noop = a.noop;
   k.status = dev.status;
+  k.pad_ends = a.pad_ends;
+  k.pad_rows = a.pad_rows;
   k.num_col_items = (int)((a.K + CW - 1) / CW);
   k.rows_per_item = pick_rows_per_item(a.M, k.num_col_items, dev.num_sms);
   const int64_t items = ((a.M + k.rows_per_item - 1) / k.rows_per_item) * k.num_col_items;

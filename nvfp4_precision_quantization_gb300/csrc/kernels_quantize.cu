@@ -57,6 +57,12 @@ struct EncodeArgs {
   int G;
   int full_m, full_n;  // tiles with tm < full_m and tn < full_n lie entirely inside x
   int vec_ok;          // output pitches / bases allow the 16-byte stores
+  // ragged x into a padded output (grouped tokens): group g's output rows
+  // [pad_ends[g-1], pad_ends[g]) take x rows from rag_ends[g-1] on, as many as the
+  // group has; the rest of the group's rows are padding (zero codes and scales).
+  const int64_t* pad_ends;
+  const int64_t* rag_ends;
+  int64_t in_rows;
   int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
   int col_scale_sectors;  // columnwise scales of four tile rows go out as one 32-byte sector
 };
@@ -67,6 +73,7 @@ struct EncodeArgs {
 template <bool FULL>
 struct StageMetaT {
   float rowS[kTileRows], colS[128];
+  int nrows;  // rows of the tile that hold data (the rest are padding rows)
   float rowA_[FULL ? kTileRows : 1], colA_[FULL ? 128 : 1];
   uint32_t s2d_[FULL ? 64 : 1];
   float e2d_[FULL ? 64 : 1];
@@ -481,6 +488,28 @@ __device__ __forceinline__ void subtile_scales_max(const uint8_t* stage, M& m, f
   }
 }
 
+// x row of the tile's first row and how many of its rows hold data: tile row tm of
+// the output, through the padded layout when x is ragged.
+__device__ __forceinline__ void tile_source(const EncodeArgs& a, int tm, int64_t& src_row0,
+                                            int& nvalid) {
+  const int64_t p0 = (int64_t)tm * kTileRows;
+  if (a.pad_ends == nullptr) {
+    src_row0 = p0;
+    nvalid = (int)(a.M - p0 < kTileRows ? a.M - p0 : kTileRows);
+    return;
+  }
+  int lo = 0, hi = a.G;  // group: the first whose padded end lies beyond p0
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a.pad_ends[mid] <= p0) lo = mid + 1;
+    else hi = mid;
+  }
+  const int64_t pstart = lo ? a.pad_ends[lo - 1] : 0, rstart = lo ? a.rag_ends[lo - 1] : 0;
+  const int64_t have = a.rag_ends[lo] - rstart - (p0 - pstart);
+  src_row0 = rstart + (p0 - pstart);
+  nvalid = (int)(have < 0 ? 0 : have < kTileRows ? have : kTileRows);
+}
+
 // ---------------------------------------------------------------- the kernel
 
 // Staging bytes per consumer warp for the TMA stores of its codes, per buffer.
@@ -530,7 +559,15 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   if (noop_set(a.noop)) return;
-  if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) return;
+  if constexpr (ROW && !COL) {
+    if (a.pad_ends != nullptr) {
+      if (!pad_layout_valid(a.rag_ends, a.pad_ends, a.G, a.in_rows, a.M)) return;
+    } else if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) {
+      return;
+    }
+  } else if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) {
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int begin, end;
   a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
@@ -555,14 +592,37 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     // tiles are issued in order k = 0, 1, ...: one cursor steps along with them
     TileCursor ci;
     ci.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
+    uint32_t no_load = 0;  // stages whose tile is all padding: nothing loaded
+    // the source of the last tile row looked up (the 4 tiles of a super-strip row share it)
+    int src_tm = -1, src_n = 0;
+    int64_t src_row = 0;
     auto issue = [&](int k) {
       const int tm = ci.tm, tn = ci.tn();
       ci.step(a.grid, fwd);
-      uint8_t* stage = smem + (k % NS) * kTileBytes;
+      const int s = k % NS;
+      uint8_t* stage = smem + s * kTileBytes;
+      int64_t src0 = (int64_t)tm * kTileRows;
+      int nvalid = kTileRows;
+      if constexpr (ROW && !COL) {  // a ragged x is quantized rowwise only
+        if (tm != src_tm) {
+          tile_source(a, tm, src_row, src_n);
+          src_tm = tm;
+        }
+        src0 = src_row;
+        nvalid = src_n;
+        if (lane == 0) meta[s].nrows = nvalid;
+        if (nvalid == 0) {
+          no_load |= 1u << s;
+          return;
+        }
+        no_load &= ~(1u << s);
+      } else if constexpr (!TMA) {
+        tile_source(a, tm, src0, nvalid);
+      }
       if constexpr (TMA) {
-        if (lane == 0) issue_tile<T>(stage, &tmap, &full[k % NS], tm, tn, policy);
+        if (lane == 0) issue_tile<T>(stage, &tmap, &full[s], (int)src0, tn, policy);
       } else {
-        plain_load_tile<T>(stage, static_cast<const T*>(a.x), a.M, a.K, tm, tn, lane);
+        plain_load_tile<T>(stage, static_cast<const T*>(a.x), a.K, src0, nvalid, tn, lane);
       }
     };
     // the ring starts empty: fill it before waiting for the amax values
@@ -638,7 +698,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       }
       __syncwarp();
       if (lane == 0) {
-        if (!TMA) mbar_arrive(&full[s]);  // stands in for the TMA arrival
+        // stands in for the TMA arrival when nothing was loaded by TMA
+        if (!TMA || (ROW && !COL && (no_load >> s & 1u))) mbar_arrive(&full[s]);
         mbar_arrive(&full[s]);
       }
     }
@@ -790,6 +851,15 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       uint32_t w[NBOX][G::BOXC / 8];
       uint32_t sc[NBOX];
       rowwise_compute<T, NBOX, FOS, B2D>(stage, m, a, r, b0, S_r, A_r, w, sc);
+      if (ROW && !COL && a.pad_ends != nullptr && r >= m.nrows) {
+        // a padding row: zero codes and scales (what a zero row encodes to)
+#pragma unroll
+        for (int bi = 0; bi < NBOX; ++bi) {
+          sc[bi] = 0;
+#pragma unroll
+          for (int q = 0; q < G::BOXC / 8; ++q) w[bi][q] = 0;
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done reading the stage
       auto store_row_scales = [&]() {
@@ -1015,12 +1085,15 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.status = dev.status;
   a.ends = q.group_ends;
   a.G = q.num_groups;
+  a.pad_ends = q.pad_ends;
+  a.rag_ends = q.rag_ends;
+  a.in_rows = q.pad_ends != nullptr ? q.in_rows : q.M;
   if (a.grid.num_tiles == 0) return cudaSuccess;
 
   CUtensorMap map, map_rc, map_cc;
   memset(&map_rc, 0, sizeof(map_rc));
   memset(&map_cc, 0, sizeof(map_cc));
-  const bool tma = make_tile_map(&map, q.x, q.in, q.M, q.K, box_cols, kTileRows);
+  const bool tma = a.in_rows > 0 && make_tile_map(&map, q.x, q.in, a.in_rows, q.K, box_cols, kTileRows);
   if (!tma) memset(&map, 0, sizeof(map));
   // Output path for the codes of BF16 input with both directions: 32-byte sector
   // stores when the code pitches allow them, else TMA stores from staging.

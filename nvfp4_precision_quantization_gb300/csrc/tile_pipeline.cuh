@@ -111,14 +111,15 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// Issue the two TMA boxes of tile (tm, tn) into `dst`, completing on `bar`.
+// Issue the two TMA boxes of tile (tm, tn) into `dst`, completing on `bar`; the
+// tile's rows start at x row src_row0 (tm * kTileRows unless x is ragged).
 template <typename T>
 __device__ __forceinline__ void issue_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                           int tm, int tn, uint64_t policy) {
+                                           int src_row0, int tn, uint64_t policy) {
   using G = TileGeo<T>;
   mbar_expect_tx(bar, kTileBytes);
-  tma_load_2d(dst, map, bar, tn * G::TILEC, tm * kTileRows, policy);
-  tma_load_2d(dst + kBoxBytes, map, bar, tn * G::TILEC + G::BOXC, tm * kTileRows, policy);
+  tma_load_2d(dst, map, bar, tn * G::TILEC, src_row0, policy);
+  tma_load_2d(dst + kBoxBytes, map, bar, tn * G::TILEC + G::BOXC, src_row0, policy);
 }
 
 // Byte offset of element (r, c) of a tile in its stage buffer: the 16-byte
@@ -133,16 +134,17 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c) {
 
 // Fallback when x cannot be described by a tensor map (rows not 16-byte aligned):
 // the 32 lanes of the producer warp copy the tile with plain loads into the same
-// swizzled layout (zero outside the matrix).
+// swizzled layout.  Tile row r comes from x row src_row0 + r for r < nvalid and is
+// zero otherwise (zero outside the matrix too).
 template <typename T>
-__device__ __forceinline__ void plain_load_tile(uint8_t* dst, const T* x, int64_t M, int64_t K,
-                                                int tm, int tn, int lane) {
+__device__ __forceinline__ void plain_load_tile(uint8_t* dst, const T* x, int64_t K,
+                                                int64_t src_row0, int nvalid, int tn, int lane) {
   using G = TileGeo<T>;
   for (int idx = lane; idx < kTileRows * G::TILEC; idx += 32) {
     const int r = idx / G::TILEC, c = idx % G::TILEC;
-    const int64_t gr = (int64_t)tm * kTileRows + r, gc = (int64_t)tn * G::TILEC + c;
+    const int64_t gc = (int64_t)tn * G::TILEC + c;
     T v = T(0);
-    if (gr < M && gc < K) v = x[gr * K + gc];
+    if (r < nvalid && gc < K) v = x[(src_row0 + r) * K + gc];
     *reinterpret_cast<T*>(dst + swz_off<T>(r, c)) = v;
   }
 }
