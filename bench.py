@@ -333,6 +333,8 @@ SUPPLEMENTARY = {
            "rowwise quantize, four-over-six, bound 256",
     "dequant": "dequantize of a row-scaled 4096x4096 quantization (0.1 % outliers x50): "
                "rowwise codes -> BF16 and columnwise codes -> FP32",
+    "moe-col": "MoE tokens as above (padded), grouped columnwise for the weight-gradient "
+               "GEMMs: each group's column amax over its rows, row-scaled, bound 448",
     "moe-ragged": "MoE tokens as above, quantized straight from the unpadded tokens into the "
                   "padded layout (padding rows not read): per-group amax, four-over-six, "
                   "bound 256, rowwise",
@@ -393,6 +395,22 @@ def run_supplementary(args):
         bio = 2 * M * K + M * K // 2 + M * K // 16 + 4 * M + 4 * G
         bmin = bio + 2 * M * K
         kern, kbytes, launches = "k_encode (rowwise, four-over-six)", bio - 4 * G, 4
+        dtype, elems = "bf16", M * K
+    elif w == "moe-col":
+        x, ends, _, _ = workloads.moe(dev)
+        M, K = x.shape
+        G = ends.numel()
+        cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+        col = nv.alloc_out(K, M, G * K, dev)
+
+        def step(ev):
+            # the same launches as nvfp4_grouped_quantize_columnwise: check, the amax
+            # pass publishing per group, then the columnwise encode
+            ev[0].record(stream)
+            nv.nvfp4_grouped_quantize_columnwise(x, ends, cfg, col, stream=stream)
+        bio = 2 * M * K + M * K // 2 + M * K // 16 + 4 * G * K
+        bmin = bio + 2 * M * K
+        kern, kbytes, launches = "whole step (check, grouped column amax, encode)", bio, 3
         dtype, elems = "bf16", M * K
     elif w == "moe-ragged":
         xp, pad_ends, counts, padded = workloads.moe(dev)

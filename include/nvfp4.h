@@ -208,6 +208,30 @@ NVFP4_API nvfp4_status nvfp4_grouped_quantize_rowwise_padded(
     const int64_t *padded_ends, int32_t num_groups, int64_t padded_rows, const nvfp4_config *cfg,
     const nvfp4_out *row, float *group_amax, const float *noop, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_grouped_quantize_columnwise -- columnwise (transposed, wgrad) quantize of
+ * grouped tokens with each group's own amax: the columnwise operand of the
+ * per-expert weight-gradient GEMMs of "Add NVFP4 four-over-six grouped GEMM for MoE
+ * training" (torchao PR #9, description), in the row-scaled columnwise form of
+ * "NVFP4: enable row-scaled transpose quantization for backward" (TransformerEngine
+ * PR #3206, description).  Equal to quantizing each group's rows on their own
+ * columnwise and placing the results side by side along the token axis.
+ *   x: device [rows][cols]; group_ends: device int64 [num_groups], cumulative, every
+ *   end a multiple of 128 (groups of whole 128-row tiles, as padded MoE tokens are),
+ *   last == rows.
+ *   col->codes [cols][rows/2], col->scales [cols][rows/16] (the columnwise layout of x).
+ *   cfg->mode NVFP4_ROW_SCALED: col->amax [num_groups][cols], column c's amax over
+ *   group g's rows; NVFP4_PER_TENSOR: col->amax [num_groups], each group's amax.
+ *   col->amax_in: optional amax of that shape (else computed).  cfg->block_2d must
+ *   be 0.  The rows of x must be 16-byte aligned (NVFP4_ERR_UNSUPPORTED otherwise).
+ *   Invalid or unaligned ends set NVFP4_DEVICE_BAD_GROUPS and nothing is written.
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_quantize_columnwise(const void *x, int32_t in_dtype,
+                                               int64_t rows, int64_t cols,
+                                               const int64_t *group_ends, int32_t num_groups,
+                                               const nvfp4_config *cfg, const nvfp4_out *col,
+                                               const float *noop, nvfp4_stream_t stream);
+
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 NVFP4_API const char *nvfp4_last_error(void);
 

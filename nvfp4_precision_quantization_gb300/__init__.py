@@ -24,7 +24,7 @@ __all__ = [
     "Config", "Out", "NVFP4Error", "load_library", "library_path",
     "nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise", "nvfp4_quantize_both",
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
-    "nvfp4_grouped_quantize_rowwise_padded",
+    "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "alloc_out", "EXPORTED_SYMBOLS",
 ]
@@ -46,7 +46,7 @@ NVFP4_DEVICE_BAD_GROUPS = 2
 EXPORTED_SYMBOLS = (
     "nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise", "nvfp4_quantize_both",
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
-    "nvfp4_grouped_quantize_rowwise_padded",
+    "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
 )
 
@@ -112,6 +112,7 @@ def load_library():
         "nvfp4_grouped_quantize_rowwise": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp, vp],
         "nvfp4_grouped_quantize_rowwise_padded": [vp, i32, i64, i64, vp, vp, i32, i64, vp, vp,
                                                   vp, vp, vp],
+        "nvfp4_grouped_quantize_columnwise": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp],
         "nvfp4_device_status": [C.POINTER(C.c_int32), i32],
         "nvfp4_selftest_convert": [vp, i64, vp, vp, vp],
     }
@@ -237,6 +238,15 @@ def nvfp4_grouped_quantize_rowwise_padded(x: torch.Tensor, ragged_ends: torch.Te
         _ptr(x), _in_dtype(x), tokens, cols, _ptr(ragged_ends), _ptr(padded_ends),
         int(ragged_ends.numel()), int(padded_rows), C.byref(cfg), C.byref(r), _ptr(group_amax),
         _ptr(noop), _stream(stream)))
+
+
+def nvfp4_grouped_quantize_columnwise(x: torch.Tensor, group_ends: torch.Tensor, cfg: Config,
+                                      col: Out, noop=None, stream=None) -> None:
+    rows, cols = _matrix(x)
+    c = col._c()
+    _check(load_library().nvfp4_grouped_quantize_columnwise(
+        _ptr(x), _in_dtype(x), rows, cols, _ptr(group_ends), int(group_ends.numel()),
+        C.byref(cfg), C.byref(c), _ptr(noop), _stream(stream)))
 
 
 def nvfp4_device_status(reset: bool = False) -> int:

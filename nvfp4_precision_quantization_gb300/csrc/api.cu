@@ -542,6 +542,100 @@ nvfp4_status nvfp4_grouped_quantize_rowwise_padded(
   return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_grouped_quantize_columnwise(const void* x, int32_t in_dtype, int64_t rows,
+                                               int64_t cols, const int64_t* group_ends,
+                                               int32_t num_groups, const nvfp4_config* cfg,
+                                               const nvfp4_out* col, const float* noop,
+                                               nvfp4_stream_t stream) {
+  nvfp4_status st;
+  if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
+  if ((st = check_sizes(rows, cols)) != NVFP4_OK) return st;
+  if ((st = check_config(cfg)) != NVFP4_OK) return st;
+  if (cfg->block_2d) return fail(NVFP4_ERR_INVALID, "grouped quantize uses 1x16 blocks");
+  if (num_groups < 1 || num_groups > 4096)
+    return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
+  if (group_ends == nullptr) return fail(NVFP4_ERR_INVALID, "group_ends is NULL");
+  const bool rs = cfg->mode == NVFP4_ROW_SCALED;
+  const int64_t namax = rs ? (int64_t)num_groups * cols : num_groups;
+  if ((st = check_out(col, "col", cols, rows, namax)) != NVFP4_OK) return st;
+  if (x == nullptr && rows * cols > 0) return fail(NVFP4_ERR_INVALID, "x is NULL");
+  const int elem = in_dtype == NVFP4_IN_BF16 ? 2 : 4;
+  if (rows * cols > 0 &&
+      ((cols * elem) % 16 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0))
+    return fail(NVFP4_ERR_UNSUPPORTED,
+                "grouped columnwise quantize needs 16-byte aligned rows of x (TMA tiles)");
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+  const InType in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+  // validate the ends (whole 128-row tiles) and clear (or copy in) the maxima
+  GroupCheckArgs g{};
+  g.M = rows;
+  g.group_ends = group_ends;
+  g.num_groups = num_groups;
+  g.noop = noop;
+  g.tile_aligned = true;
+  g.prep.noop = noop;
+  if (col->amax_in == nullptr) {
+    g.prep.zero_ptr[0] = col->amax;
+    g.prep.zero_n[0] = namax;
+  } else if (col->amax_in != col->amax) {
+    g.prep.copy_dst[0] = col->amax;
+    g.prep.copy_src[0] = col->amax_in;
+    g.prep.copy_n[0] = namax;
+  }
+  cudaError_t e = launch_group_check(g, dev, stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "group check launch");
+  if (col->amax_in == nullptr) {
+    if (rs) {
+      // each group's column maxima: the TMA amax pass publishing per group
+      AmaxArgs am{};
+      am.x = x;
+      am.in = in;
+      am.M = rows;
+      am.K = cols;
+      am.col_amax = col->amax;
+      am.noop = noop;
+      am.group_ends = group_ends;
+      am.num_groups = num_groups;
+      am.col_grouped = true;
+      if ((e = launch_amax(am, dev, stream)) != cudaSuccess)
+        return cuda_fail(e, "amax launch");
+    } else {
+      GroupedAmaxArgs ga{};
+      ga.x = x;
+      ga.in = in;
+      ga.M = rows;
+      ga.K = cols;
+      ga.group_ends = group_ends;
+      ga.num_groups = num_groups;
+      ga.group_amax = col->amax;
+      ga.noop = noop;
+      ga.tile_aligned = true;
+      if ((e = launch_grouped_amax(ga, dev, stream)) != cudaSuccess)
+        return cuda_fail(e, "grouped amax launch");
+    }
+  }
+  QuantArgs q{};
+  q.x = x;
+  q.in = in;
+  q.M = rows;
+  q.K = cols;
+  q.row_scaled = true;  // the producer stages each tile's column scales from its group's amax
+  q.four_over_six = cfg->four_over_six != 0;
+  q.block_2d = false;
+  q.bound = cfg->bound;
+  q.noop = noop;
+  q.col_codes = col->codes;
+  q.col_scales = col->scales;
+  q.col_amax = col->amax;
+  q.group_ends = group_ends;
+  q.num_groups = num_groups;
+  q.col_grouped = true;
+  q.col_grouped_per_tensor = !rs;
+  if ((e = launch_quantize(q, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize");
+  return NVFP4_OK;
+}
+
 const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
 
 nvfp4_status nvfp4_device_status(int32_t* status, int32_t reset) {

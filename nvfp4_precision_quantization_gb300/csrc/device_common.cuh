@@ -44,6 +44,15 @@ __device__ __forceinline__ bool groups_valid(const int64_t* ends, int G, int64_t
   return !__syncthreads_or(bad);
 }
 
+// Every group end a multiple of n (groups made of whole tiles).  Every thread of
+// the block must call it.
+__device__ __forceinline__ bool ends_aligned(const int64_t* ends, int G, int64_t n) {
+  int bad = 0;
+  for (int g = threadIdx.x; g < G; g += blockDim.x)
+    if (ends[g] % n != 0) bad = 1;
+  return !__syncthreads_or(bad);
+}
+
 // Ragged tokens quantized into a padded layout: group g has ragged rows
 // [rag_ends[g-1], rag_ends[g]) of x and padded output rows [pad_ends[g-1],
 // pad_ends[g]).  Valid when both are non-decreasing, end at their row counts, every

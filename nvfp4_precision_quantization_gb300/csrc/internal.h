@@ -40,6 +40,9 @@ struct AmaxArgs {
   const float* noop;
   const int64_t* group_ends;  // optional: do nothing unless these group ends are valid
   int num_groups;
+  // grouped columns (TMA path): col_amax is [num_groups][K], each group's column maxima;
+  // the group ends must be multiples of 128
+  bool col_grouped;
 };
 cudaError_t launch_amax(const AmaxArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
@@ -54,6 +57,7 @@ struct GroupedAmaxArgs {
   const float* noop;
   const int64_t* pad_ends;  // optional: do nothing unless this padded layout is valid too
   int64_t pad_rows;
+  bool tile_aligned;  // also require every group end to be a multiple of 128
 };
 cudaError_t launch_grouped_amax(const GroupedAmaxArgs& a, const DeviceInfo& dev,
                                 cudaStream_t stream);
@@ -72,6 +76,7 @@ struct GroupCheckArgs {
   // optional: group_ends are padded ends of ragged x (ragged ends rag_ends, in_rows rows)
   const int64_t* rag_ends;
   int64_t in_rows;
+  bool tile_aligned;  // also require every group end to be a multiple of 128
 };
 cudaError_t launch_group_check(const GroupCheckArgs& a, const DeviceInfo& dev,
                                cudaStream_t stream, bool expand_pass);
@@ -104,6 +109,10 @@ struct QuantArgs {
   const int64_t* pad_ends;
   const int64_t* rag_ends;
   int64_t in_rows;
+  // optional, columnwise only: each group (ends multiples of 128) is quantized with its
+  // own amax -- col_amax [num_groups][K] (per column) or [num_groups] (per tensor)
+  bool col_grouped;
+  bool col_grouped_per_tensor;
 };
 cudaError_t launch_quantize(const QuantArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 

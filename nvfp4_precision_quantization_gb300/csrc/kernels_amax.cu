@@ -372,7 +372,23 @@ struct AmaxTmaArgs {
   int G;
   int keep_tiles;  // the last keep_tiles tiles of a chunk are loaded with evict_last
   int* status;
+  // grouped columns: col_amax is [G][K], the column maxima of each group's rows (the
+  // group ends, multiples of kTileRows, are ends / G)
+  int col_grouped;
 };
+
+// group of tile row tm (group ends are multiples of kTileRows): a binary search
+// over the ends in global memory
+__device__ __forceinline__ int group_of_tile_row(const int64_t* ends, int G, int tm) {
+  const int64_t r = (int64_t)tm * kTileRows;
+  int lo = 0, hi = G;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(ends + mid) <= r) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
 
 template <typename T, bool ROW, bool COL, bool TEN>
 __global__ void __launch_bounds__(kPipeThreads, 2)
@@ -385,7 +401,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   if (noop_set(a.noop)) return;
-  if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) return;
+  if (a.ends != nullptr && (!groups_valid(a.ends, a.G, a.M) ||
+                            (a.col_grouped && !ends_aligned(a.ends, a.G, kTileRows))))
+    return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int begin, end;
   a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
@@ -447,7 +465,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   Acc tmx = 0;
   int cur_ss = -1;
 
+  int cur_g = 0, grp_tm = -1, grp = 0;  // grouped columns: group of the partials / of tile row grp_tm
   auto flush_cols = [&](int ss) {
+    float* const cbase = a.col_amax + (a.col_grouped ? (int64_t)cur_g * a.K : 0);
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       const int tn = ss * NG + g;
@@ -468,11 +488,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
           if constexpr (BF16) {
             const uint32_t mv = cm[g][j] & 0x7fff7fffu;
             if (col0 + 2 * j < a.K)
-              atomic_max_nonneg(&a.col_amax[col0 + 2 * j], __uint_as_float(mv << 16));
+              atomic_max_nonneg(&cbase[col0 + 2 * j], __uint_as_float(mv << 16));
             if (col0 + 2 * j + 1 < a.K)
-              atomic_max_nonneg(&a.col_amax[col0 + 2 * j + 1], __uint_as_float(mv & 0xffff0000u));
+              atomic_max_nonneg(&cbase[col0 + 2 * j + 1], __uint_as_float(mv & 0xffff0000u));
           } else {
-            if (col0 + j < a.K) atomic_max_nonneg(&a.col_amax[col0 + j], cm[g][j]);
+            if (col0 + j < a.K) atomic_max_nonneg(&cbase[col0 + j], cm[g][j]);
           }
         }
       }
@@ -533,9 +553,18 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   for (int k = 0; k < count; ++k, cur.step(a.grid, fwd)) {
     const int s = k % kStages;
     const int tm = cur.tm, ss = cur.ss, gsel = cur.jt;
-    if (COL && ss != cur_ss) {
-      if (cur_ss >= 0) flush_cols(cur_ss);
-      cur_ss = ss;
+    if (COL) {
+      // a new super-strip, or (grouped columns) a new group: publish the partials
+      if (a.col_grouped && tm != grp_tm) {
+        grp = group_of_tile_row(a.ends, a.G, tm);
+        grp_tm = tm;
+      }
+      const int g_now = a.col_grouped ? grp : 0;
+      if (ss != cur_ss || g_now != cur_g) {
+        if (cur_ss >= 0) flush_cols(cur_ss);
+        cur_ss = ss;
+        cur_g = g_now;
+      }
     }
     if (!mbar_wait_bounded(&full[s], (uint32_t)((k / kStages) & 1))) {
       abort_flag = 1;
@@ -665,6 +694,7 @@ struct GroupedKernelArgs {
   int num_col_items;
   const int64_t* pad_ends;  // optional: also require this padded layout of the groups
   int64_t pad_rows;
+  int tile_aligned;  // also require every group end to be a multiple of kTileRows
 };
 
 // Per-group amax: like the tensor reduction, but a CTA item is split at group
@@ -676,8 +706,9 @@ __global__ void __launch_bounds__(kThreads) k_grouped_amax(GroupedKernelArgs a) 
   __shared__ float row_red[kColWarps][512];
   if (noop_set(a.noop)) return;
   const bool ok = load_group_ends(a.ends, a.G, a.M, s_ends);
-  if (!ok || (a.pad_ends != nullptr &&
-              !pad_layout_valid(a.ends, a.pad_ends, a.G, a.M, a.pad_rows))) {
+  if (!ok ||
+      (a.pad_ends != nullptr && !pad_layout_valid(a.ends, a.pad_ends, a.G, a.M, a.pad_rows)) ||
+      (a.tile_aligned && !ends_aligned(a.ends, a.G, kTileRows))) {
     if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(a.status, kStatusBadGroups);
     return;
   }
@@ -737,8 +768,10 @@ __global__ void k_group_check(GroupCheckArgs a, int* status, bool expand_pass) {
   const bool ok = load_group_ends(a.group_ends, a.num_groups, a.M, s_ends);
   // padded layout: group_ends are the padded ends (M output rows), rag_ends the
   // ragged ends of x (in_rows rows)
-  if (!ok || (a.rag_ends != nullptr && !pad_layout_valid(a.rag_ends, a.group_ends, a.num_groups,
-                                                         a.in_rows, a.M))) {
+  if (!ok ||
+      (a.rag_ends != nullptr &&
+       !pad_layout_valid(a.rag_ends, a.group_ends, a.num_groups, a.in_rows, a.M)) ||
+      (a.tile_aligned && !ends_aligned(a.group_ends, a.num_groups, kTileRows))) {
     if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(status, kStatusBadGroups);
     return;
   }
@@ -797,6 +830,7 @@ cudaError_t launch_amax(const AmaxArgs& a, const DeviceInfo& dev, cudaStream_t s
       k.ends = a.group_ends;
       k.G = a.num_groups;
       k.status = dev.status;
+      k.col_grouped = a.col_grouped ? 1 : 0;
       const int grid = pipe_grid_size(k.grid.num_tiles, dev.num_sms);
       // keep about 80 MB of the tail of the walk in L2 for the encode pass
       k.keep_tiles = (int)std::max<int64_t>(1, (80LL << 20) / ((int64_t)grid * kTileBytes));
@@ -866,6 +900,7 @@ cudaError_t launch_grouped_amax(const GroupedAmaxArgs& a, const DeviceInfo& dev,
   k.status = dev.status;
   k.pad_ends = a.pad_ends;
   k.pad_rows = a.pad_rows;
+  k.tile_aligned = a.tile_aligned ? 1 : 0;
   k.num_col_items = (int)((a.K + CW - 1) / CW);
   k.rows_per_item = pick_rows_per_item(a.M, k.num_col_items, dev.num_sms);
   const int64_t items = ((a.M + k.rows_per_item - 1) / k.rows_per_item) * k.num_col_items;

@@ -63,6 +63,9 @@ struct EncodeArgs {
   const int64_t* pad_ends;
   const int64_t* rag_ends;
   int64_t in_rows;
+  // grouped columns: col_amax is [G][K] (or [G] with col_grouped_pt), one row per group
+  // of ends (multiples of kTileRows); the producer stages each tile's column scales
+  int col_grouped, col_grouped_pt;
   int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
   int col_scale_sectors;  // columnwise scales of four tile rows go out as one 32-byte sector
 };
@@ -568,6 +571,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   } else if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) {
     return;
   }
+  if constexpr (COL && !ROW) {
+    if (a.col_grouped && !ends_aligned(a.ends, a.G, kTileRows)) return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int begin, end;
   a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
@@ -634,6 +640,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     // latency overlaps the wait for the next free stage
     float ra[RPL], ca[CPL];
     // the amax of tile k are loaded in order k = 0, 1, ... as well
+    int grp_tm = -1, grp = 0;  // grouped columns: group of tile row grp_tm
     TileCursor cm;
     cm.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
     auto load_amax = [&](int k, float (&r_)[RPL], float (&c_)[CPL]) {
@@ -648,10 +655,28 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         }
       }
       if (COL) {
+        const float* cam = a.col_amax;
+        bool one = false;  // one amax for the whole tile (a group's tensor amax)
+        if constexpr (COL && !ROW) {
+          if (a.col_grouped) {
+            if (tm != grp_tm) {  // the group of this tile row (ends are whole tiles)
+              int lo = 0, hi = a.G;
+              while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (a.ends[mid] <= (int64_t)tm * kTileRows) lo = mid + 1;
+                else hi = mid;
+              }
+              grp = lo;
+              grp_tm = tm;
+            }
+            cam += a.col_grouped_pt ? (int64_t)grp : (int64_t)grp * a.K;
+            one = a.col_grouped_pt != 0;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
           const int64_t gc = (int64_t)tn * G::TILEC + lane + 32 * i;
-          c_[i] = gc < a.K ? a.col_amax[gc] : 0.0f;
+          c_[i] = gc < a.K ? cam[one ? 0 : gc] : 0.0f;
         }
       }
     };
@@ -1087,6 +1112,8 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.G = q.num_groups;
   a.pad_ends = q.pad_ends;
   a.rag_ends = q.rag_ends;
+  a.col_grouped = q.col_grouped ? 1 : 0;
+  a.col_grouped_pt = q.col_grouped_per_tensor ? 1 : 0;
   a.in_rows = q.pad_ends != nullptr ? q.in_rows : q.M;
   if (a.grid.num_tiles == 0) return cudaSuccess;
 
