@@ -341,6 +341,54 @@ SUPPLEMENTARY = {
 }
 
 
+def supplementary_oracle_sample(w: str, sample_rows: int):
+    """The oracle (single thread) on the first rows of the workload's input, in the
+    same unit (algorithmic GB/s of the rows processed)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads
+    if w in ("moe", "moe-ragged", "moe-col"):
+        x = workloads.seeded_normal(sample_rows, 7168, seed=workloads.SEEDS["moe"] + 1000)
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        ends = np.array([sample_rows], np.int64)
+        rows, cols = xb.shape
+        t0 = time.perf_counter()
+        if w == "moe-col":
+            oracle.quantize(xb, "bf16", mode=oracle.ROW_SCALED, bound=448.0, rowwise=False)
+            nbytes = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + 4 * cols
+        else:
+            oracle.grouped_quantize_rowwise(xb, "bf16", ends, mode=oracle.PER_TENSOR, bound=256.0,
+                                            four_over_six=True)
+            nbytes = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + 4 * rows
+        dt = time.perf_counter() - t0
+        what = f"{sample_rows} tokens x 7168 (one group)"
+    elif w == "weights16x16":
+        x = workloads.edge_normal(sample_rows, 8192, torch.bfloat16, "cpu", std=0.02)
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        rows, cols = xb.shape
+        t0 = time.perf_counter()
+        oracle.quantize(xb, "bf16", mode=oracle.PER_TENSOR, bound=448.0, block_2d=True)
+        dt = time.perf_counter() - t0
+        nbytes = 2 * rows * cols + 2 * (rows * cols // 2 + rows * cols // 16) + 8
+        what = f"first {sample_rows} rows of the 8192x8192 weights, both directions"
+    else:  # dequant
+        x = workloads.outliers("cpu")[:sample_rows]
+        xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+        rows, cols = xb.shape
+        o = oracle.quantize(xb, "bf16", mode=oracle.ROW_SCALED, bound=448.0, columnwise=False)
+        codes, scales, amax = o["row"]
+        t0 = time.perf_counter()
+        oracle.dequantize(codes, scales, amax, row_scaled=True, rows=rows, cols=cols, bound=448.0,
+                          out_dtype="fp32")
+        dt = time.perf_counter() - t0
+        nbytes = rows * cols // 2 + rows * cols // 16 + 4 * rows + 4 * rows * cols
+        what = f"first {sample_rows} rows of the 4096x4096 rowwise quantization, to FP32"
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": what, "seconds": dt}
+
+
 def run_supplementary(args):
     """One JSON line for a row of the path other than the headline workload: same
     timing rules (warm-up, 256 MB L2 flush before each step, CUDA events on the
@@ -455,6 +503,10 @@ def run_supplementary(args):
     else:
         raise SystemExit(f"unknown workload {w}")
 
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = supplementary_oracle_sample(w, args.oracle_rows or 256)
+
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
         flush.zero_()
@@ -500,7 +552,7 @@ def run_supplementary(args):
             "roofline": {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                          "traffic": None, "algorithmic_bytes": kbytes},
-            "cpu_baseline": None, "e2e": None, "gpu_launches": launches * K_,
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches * K_,
             "clocks": clocks}))
     if world > 1:
         torch.distributed.destroy_process_group()
