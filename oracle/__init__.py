@@ -71,6 +71,10 @@ def lib():
         L.oracle_grouped_quantize_rowwise.restype = C.c_int
         L.oracle_grouped_quantize_rowwise.argtypes = [f32p, i64, i64, i64p, C.c_int, C.c_int,
                                                       C.c_float, C.c_int, vp, vp, vp, vp, vp]
+        f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+        L.oracle_gemm.restype = None
+        L.oracle_gemm.argtypes = [u8p, u8p, f32p, C.c_int, C.c_float, u8p, u8p, f32p, C.c_int,
+                                  C.c_float, i64, i64, i64, f64p, vp]
         _lib = L
     return _lib
 
@@ -242,3 +246,23 @@ def grouped_quantize_rowwise(x: np.ndarray, dtype: str, group_ends, *, mode: int
     if rc != 0:
         raise ValueError("invalid grouped arguments")
     return codes, scales, ra[:rows], ga[:len(ends)]
+
+
+def gemm(a, b, *, with_abs: bool = False):
+    """D = dequant(A) x dequant(B)^T in FP64 (the GEMM that consumes NVFP4 operands).
+
+    a, b: dicts with "codes" [lines][k/2], "scales" [lines][k/16], "amax" ([lines] or
+    [1]), "row_scaled" (bool) and "bound".  Returns D [m][n] (and, with with_abs, the
+    per-element sum of |terms| that rounding bounds scale with)."""
+    ac = np.ascontiguousarray(a["codes"], np.uint8)
+    bc = np.ascontiguousarray(b["codes"], np.uint8)
+    m, n, k = ac.shape[0], bc.shape[0], ac.shape[1] * 2
+    assert bc.shape[1] * 2 == k and k % 16 == 0
+    d = np.zeros((m, n), np.float64)
+    da = np.zeros((m, n), np.float64) if with_abs else None
+    lib().oracle_gemm(ac.reshape(-1), np.ascontiguousarray(a["scales"], np.uint8).reshape(-1),
+                      _f32(a["amax"]).reshape(-1), int(a["row_scaled"]), float(a["bound"]),
+                      bc.reshape(-1), np.ascontiguousarray(b["scales"], np.uint8).reshape(-1),
+                      _f32(b["amax"]).reshape(-1), int(b["row_scaled"]), float(b["bound"]),
+                      m, n, k, d, _ptr(da))
+    return (d, da) if with_abs else d

@@ -52,6 +52,11 @@
  *   R8  layouts: codes two per byte, low nibble = even element; scales one byte
  *       per block, row-major [lines][ceil(n/16)], no GEMM swizzle.
  *   R9  noop: a non-NULL flag equal to 1.0f means nothing at all is written.
+ *   R13 GEMM consumer (sequence diagram of [TE-3206]: output times the outer
+ *       product of the operands' per-line amax): the matrix product of the two
+ *       dequantized operands, each element code * decode(scale) * amax /
+ *       (bound * 6) as a real number; computed here in FP64, not FP32, because it
+ *       is the exact target that the GPU's FP32 accumulation is bounded against.
  *
  * Parity pins: every function here is checked in tests/ against something other
  * than itself (brute force, library conversions, closed forms, invariants from
@@ -499,4 +504,57 @@ ORACLE_API int oracle_grouped_quantize_rowwise(const float *x, int64_t rows, int
     free(expanded);
     free(gam);
     return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* GEMM consumer [TE-3206]: D = dequant(A) x dequant(B)^T                     */
+/* ------------------------------------------------------------------------- */
+
+/* The value an NVFP4 element stands for, as a real number: code * decode(scale)
+ * * amax / (bound * 6).  In FP64 the product is exact (at most 2 + 4 + 24
+ * significant bits) and the division rounds once. */
+static double element_value(const uint8_t *codes, const uint8_t *scales, const float *amax,
+                            int row_scaled, float bound, int64_t k, int64_t r, int64_t c)
+{
+    uint8_t byte = codes[r * (k / 2) + c / 2];
+    uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15u);
+    double sd = (double)oracle_e4m3_decode(scales[r * (k / 16) + c / 16]);
+    double a = (double)amax[row_scaled ? r : 0];
+    return (double)oracle_e2m1_decode(code) * sd * a / ((double)bound * 6.0);
+}
+
+/* The GEMM that consumes two NVFP4 operands (sequence diagram of [TE-3206]: the
+ * fprop GEMM scales its output by the activation's per-row amax and the weight's
+ * amax; the wgrad GEMM by the outer product of both operands' per-line amax).
+ * Its plain definition: the matrix product of the two dequantized operands.
+ *   A: codes [m][k/2], scales [m][k/16], amax [m] (a_row_scaled) or [1];
+ *   B: codes [n][k/2], scales [n][k/16], amax [n] or [1]  (both K-major, the
+ *      layout of a rowwise output, or of a columnwise output for the transposed
+ *      operand); k even and a multiple of 16 here.
+ *   d [m][n] = sum over c of value_A(i, c) * value_B(j, c), summed in FP64 in
+ *   column order; d_abs (optional) [m][n] = sum of |value_A * value_B|, the
+ *   magnitude the tests scale their rounding bound by. */
+ORACLE_API void oracle_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_amax,
+                            int a_row_scaled, float a_bound, const uint8_t *b_codes,
+                            const uint8_t *b_scales, const float *b_amax, int b_row_scaled,
+                            float b_bound, int64_t m, int64_t n, int64_t k, double *d,
+                            double *d_abs)
+{
+    double *va = (double *)malloc((size_t)(k > 0 ? k : 1) * sizeof(double));
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t c = 0; c < k; ++c)
+            va[c] = element_value(a_codes, a_scales, a_amax, a_row_scaled, a_bound, k, i, c);
+        for (int64_t j = 0; j < n; ++j) {
+            double s = 0.0, sa = 0.0;
+            for (int64_t c = 0; c < k; ++c) {
+                double t = va[c] *
+                           element_value(b_codes, b_scales, b_amax, b_row_scaled, b_bound, k, j, c);
+                s += t;
+                sa += fabs(t);
+            }
+            d[i * n + j] = s;
+            if (d_abs) d_abs[i * n + j] = sa;
+        }
+    }
+    free(va);
 }

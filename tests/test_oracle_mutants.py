@@ -41,6 +41,16 @@ MUTANTS = {
     "16x16 error summed in column-major order":
         ("for (int j = 0; j < w; ++j) v[i * w + j] = x[(ti * 16 + i) * cols + tj * 16 + j];",
          "for (int j = 0; j < w; ++j) v[j * h + i] = x[(ti * 16 + i) * cols + tj * 16 + j];"),
+    "GEMM uses the first amax for every line":
+        ("double a = (double)amax[row_scaled ? r : 0];", "double a = (double)amax[0];"),
+    "GEMM drops the code sign":
+        ("return (double)oracle_e2m1_decode(code) * sd", "return (double)oracle_e2m1_decode(code & 7u) * sd"),
+    "GEMM scale index per 32 columns":
+        ("scales[r * (k / 16) + c / 16]", "scales[r * (k / 16) + c / 32]"),
+    "GEMM reads B with A's row index":
+        ("element_value(b_codes, b_scales, b_amax, b_row_scaled, b_bound, k, j, c)",
+         "element_value(b_codes, b_scales, b_amax, b_row_scaled, b_bound, k, i % n, c)"),
+    "GEMM divides by bound * 4": ("a / ((double)bound * 6.0)", "a / ((double)bound * 4.0)"),
 }
 
 
@@ -54,6 +64,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, NVFP4_ORACLE_LIBRARY=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_formats.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_recipe.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_recipe.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_gemm.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
