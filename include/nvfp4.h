@@ -232,6 +232,49 @@ NVFP4_API nvfp4_status nvfp4_grouped_quantize_columnwise(const void *x, int32_t 
                                                const nvfp4_config *cfg, const nvfp4_out *col,
                                                const float *noop, nvfp4_stream_t stream);
 
+/*
+ * One operand of nvfp4_gemm: an NVFP4 tensor in K-major layout -- a rowwise output
+ * (lines = rows of x) or a columnwise output (lines = columns of x, the operand
+ * that enters the GEMM transposed).
+ */
+typedef struct {
+    const uint8_t *codes;   /* [lines][k/2], 16-byte aligned */
+    const uint8_t *scales;  /* [lines][k/16]; a 16x16-block operand carries its tile's
+                               scale on each of the tile's lines, as the quantize
+                               entry points write it */
+    const float *amax;      /* [lines] (NVFP4_ROW_SCALED) or [1] (NVFP4_PER_TENSOR) */
+    int32_t mode;           /* nvfp4_amax_mode of amax */
+    float bound;            /* 448 or 256: the bound the operand was quantized with */
+} nvfp4_operand;
+
+/*
+ * nvfp4_gemm -- the GEMM that consumes two NVFP4 operands, with the bilateral amax
+ * post-scale of "NVFP4: enable row-scaled transpose quantization for backward"
+ * (TransformerEngine PR #3206, sequence diagram: the fprop output is scaled by the
+ * activation's per-row amax and the weight's amax, the wgrad output by the outer
+ * product of both operands' per-line amax).  Defined as the product of the two
+ * dequantized operands:
+ *   d[i][j] = sum_c value_a(i, c) * value_b(j, c),
+ *   value   = code * decode(scale) * amax / (bound * 6)
+ * for a: m lines, b: n lines, both with k values per line.  Computed on the
+ * tensor cores with one E4M3 scale per 16 values and FP32 accumulation, then
+ * d = fl(fl(acc * alpha_i) * beta_j) with alpha_i = amax_a[i] * fl(1/(bound_a*6)),
+ * beta_j = amax_b[j] * fl(1/(bound_b*6)), written row-major [m][n] as BF16 (round
+ * to nearest even) or FP32 (out_dtype).  Not bit-identical to an FP64 product:
+ * the FP32 accumulation order is the tensor core's.
+ *   k: a multiple of 32 (NVFP4_ERR_UNSUPPORTED otherwise); k == 0 writes zeros;
+ *   m == 0 or n == 0 writes nothing.
+ *   workspace: device, 256-byte aligned, at least nvfp4_gemm_workspace_size(m, n,
+ *   k) bytes, owned by the caller and used by the call (the scales rewritten in
+ *   the tensor core's chunk layout); two calls in flight at once need two
+ *   workspaces.
+ *   A wait that gives up sets NVFP4_DEVICE_TIMEOUT and d is left unwritten.
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint64_t *bytes);
+NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_operand *a, const nvfp4_operand *b, int64_t m,
+                        int64_t n, int64_t k, void *d, int32_t out_dtype, void *workspace,
+                        uint64_t workspace_bytes, nvfp4_stream_t stream);
+
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 NVFP4_API const char *nvfp4_last_error(void);
 

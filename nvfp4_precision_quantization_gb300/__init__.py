@@ -26,6 +26,7 @@ __all__ = [
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
+    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "Operand",
     "alloc_out", "EXPORTED_SYMBOLS",
 ]
 
@@ -48,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
+    "nvfp4_gemm_workspace_size", "nvfp4_gemm",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +85,9 @@ class Out:
     def _c(self) -> _COut:
         return _COut(_ptr(self.codes), _ptr(self.scales), _ptr(self.amax), _ptr(self.amax_in))
 
+    def as_operand(self, mode: int, bound: float) -> "Operand":
+        return Operand(self.codes, self.scales, self.amax, mode, bound)
+
 
 def library_path() -> str:
     return os.path.join(_HERE, f"libnvfp4_{platform.machine()}.so")
@@ -115,6 +120,8 @@ def load_library():
         "nvfp4_grouped_quantize_columnwise": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp],
         "nvfp4_device_status": [C.POINTER(C.c_int32), i32],
         "nvfp4_selftest_convert": [vp, i64, vp, vp, vp],
+        "nvfp4_gemm_workspace_size": [i64, i64, i64, C.POINTER(C.c_uint64)],
+        "nvfp4_gemm": [vp, vp, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -260,6 +267,58 @@ def nvfp4_selftest_convert(x: torch.Tensor, e2m1_out=None, e4m3_out=None, stream
         raise TypeError("x must be contiguous float32")
     _check(load_library().nvfp4_selftest_convert(_ptr(x), x.numel(), _ptr(e2m1_out),
                                                  _ptr(e4m3_out), _stream(stream)))
+
+
+class _COperand(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("amax", C.c_void_p),
+                ("mode", C.c_int32), ("bound", C.c_float)]
+
+
+@dataclass
+class Operand:
+    """One nvfp4_gemm operand (nvfp4_operand): K-major codes [lines][k/2], scales
+    [lines][k/16], amax [lines] (ROW_SCALED) or [1] (PER_TENSOR), the bound it was
+    quantized with.  Out.as_operand() builds one from a quantize output."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    amax: torch.Tensor
+    mode: int
+    bound: float
+
+    def _c(self) -> _COperand:
+        return _COperand(_ptr(self.codes), _ptr(self.scales), _ptr(self.amax), self.mode,
+                         self.bound)
+
+
+def nvfp4_gemm_workspace_size(m: int, n: int, k: int) -> int:
+    v = C.c_uint64(0)
+    _check(load_library().nvfp4_gemm_workspace_size(m, n, k, C.byref(v)))
+    return v.value
+
+
+def nvfp4_gemm(a: Operand, b: Operand, d: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> None:
+    """d [m][n] (bfloat16 or float32) = dequant(a) x dequant(b)^T on the tensor cores.
+    workspace: uint8 device tensor of nvfp4_gemm_workspace_size(m, n, k) bytes (allocated
+    here with torch if not given)."""
+    if d.dim() != 2 or not d.is_contiguous():
+        raise ValueError("d must be a contiguous 2-D tensor")
+    if d.dtype == torch.bfloat16:
+        od = NVFP4_OUT_BF16
+    elif d.dtype == torch.float32:
+        od = NVFP4_OUT_FP32
+    else:
+        raise TypeError("d must be bfloat16 or float32")
+    m, n = d.shape
+    k = a.codes.shape[1] * 2
+    if a.codes.shape[0] != m or b.codes.shape[0] != n or b.codes.shape[1] * 2 != k:
+        raise ValueError("operand shapes do not match d")
+    need = nvfp4_gemm_workspace_size(m, n, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=d.device)
+    ca, cb = a._c(), b._c()
+    _check(load_library().nvfp4_gemm(C.byref(ca), C.byref(cb), m, n, k, _ptr(d), od,
+                                      _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def alloc_out(lines: int, n: int, amax_len: int, device="cuda", fill=None) -> Out:

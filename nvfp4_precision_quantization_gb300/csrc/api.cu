@@ -293,6 +293,24 @@ bool make_byte_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pit
   return r == CUDA_SUCCESS;
 }
 
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pitch,
+                      int box_bytes, int box_rows) {
+  if (rows <= 0 || pitch <= 0) return false;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || pitch % 16 != 0) return false;
+  if (rows >= (1LL << 31) || pitch >= (1LL << 31)) return false;
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)pitch};
+  const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -379,6 +397,74 @@ nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const
   d.out_bf16 = out_dtype == NVFP4_OUT_BF16;
   cudaError_t e = launch_dequantize(d, dev, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint64_t* bytes) {
+  if (bytes == nullptr) return fail(NVFP4_ERR_INVALID, "bytes is NULL");
+  nvfp4_status st;
+  if ((st = check_sizes(m, n)) != NVFP4_OK) return st;
+  if ((st = check_sizes(k, 0)) != NVFP4_OK) return st;
+  *bytes = (m == 0 || n == 0 || k == 0) ? 0 : (uint64_t)gemm_layout(m, n, k).workspace_bytes;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m, int64_t n,
+                        int64_t k, void* d, int32_t out_dtype, void* workspace,
+                        uint64_t workspace_bytes, nvfp4_stream_t stream) {
+  nvfp4_status st;
+  if ((st = check_sizes(m, n)) != NVFP4_OK) return st;
+  if ((st = check_sizes(k, 0)) != NVFP4_OK) return st;
+  if (a == nullptr || b == nullptr) return fail(NVFP4_ERR_INVALID, "a or b is NULL");
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+    return fail(NVFP4_ERR_INVALID, "unknown out_dtype");
+  for (const nvfp4_operand* o : {a, b}) {
+    if (o->mode != NVFP4_PER_TENSOR && o->mode != NVFP4_ROW_SCALED)
+      return fail(NVFP4_ERR_INVALID, "operand mode must be NVFP4_PER_TENSOR or NVFP4_ROW_SCALED");
+    if (!(o->bound == 448.0f || o->bound == 256.0f))
+      return fail(NVFP4_ERR_INVALID, "operand bound must be 448 or 256");
+  }
+  if (m == 0 || n == 0) return NVFP4_OK;
+  if (d == nullptr) return fail(NVFP4_ERR_INVALID, "d is NULL");
+  const size_t esize = out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
+  if (k == 0) {  // the empty sum
+    cudaError_t e = cudaMemsetAsync(d, 0, (size_t)m * (size_t)n * esize, stream);
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "cudaMemsetAsync");
+  }
+  if (k % 32 != 0) return fail(NVFP4_ERR_UNSUPPORTED, "k must be a multiple of 32");
+  for (const nvfp4_operand* o : {a, b}) {
+    if (!o->codes || !o->scales || !o->amax)
+      return fail(NVFP4_ERR_INVALID, "operand codes, scales and amax must be non-NULL");
+    if (reinterpret_cast<uintptr_t>(o->codes) % 16 != 0)
+      return fail(NVFP4_ERR_UNSUPPORTED, "operand codes must be 16-byte aligned");
+  }
+  const GemmLayout L = gemm_layout(m, n, k);
+  if (L.tiles_m * L.tiles_n >= (1LL << 31)) return fail(NVFP4_ERR_UNSUPPORTED, "too many tiles");
+  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(NVFP4_ERR_INVALID, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < (uint64_t)L.workspace_bytes)
+    return fail(NVFP4_ERR_INVALID, "workspace smaller than nvfp4_gemm_workspace_size");
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+  GemmArgs g{};
+  g.a_codes = a->codes;
+  g.a_scales = a->scales;
+  g.a_amax = a->amax;
+  g.a_row_scaled = a->mode == NVFP4_ROW_SCALED;
+  g.a_bound = a->bound;
+  g.b_codes = b->codes;
+  g.b_scales = b->scales;
+  g.b_amax = b->amax;
+  g.b_row_scaled = b->mode == NVFP4_ROW_SCALED;
+  g.b_bound = b->bound;
+  g.M = m;
+  g.N = n;
+  g.K = k;
+  g.d = d;
+  g.d_bf16 = out_dtype == NVFP4_OUT_BF16;
+  g.workspace = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_gemm(g, dev, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return NVFP4_OK;
 }
 

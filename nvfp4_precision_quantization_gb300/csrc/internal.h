@@ -131,12 +131,41 @@ cudaError_t launch_dequantize(const DequantArgs& a, const DeviceInfo& dev, cudaS
 cudaError_t launch_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3,
                                     cudaStream_t stream);
 
+// GEMM consumer of two NVFP4 operands (kernels_gemm.cu): D [M][N] = A [M][K] x B [N][K]^T
+// on the dequantized values, K-major codes [lines][K/2] and compact scales [lines][K/16].
+struct GemmArgs {
+  const uint8_t* a_codes;
+  const uint8_t* a_scales;
+  const float* a_amax;  // [M] (a_row_scaled) or [1]
+  bool a_row_scaled;
+  float a_bound;
+  const uint8_t* b_codes;
+  const uint8_t* b_scales;
+  const float* b_amax;  // [N] or [1]
+  bool b_row_scaled;
+  float b_bound;
+  int64_t M, N, K;  // M, N >= 1; K >= 32 and a multiple of 32
+  void* d;
+  bool d_bf16;
+  uint8_t* workspace;  // >= gemm_layout(M, N, K).workspace_bytes, 256-byte aligned
+};
+struct GemmLayout {
+  int64_t k_tiles, n_kc, tiles_m, tiles_n;
+  int64_t sfa_bytes, sfb_bytes, sfb_offset, workspace_bytes;
+};
+GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
 // Grid size shared by the TMA amax and encode kernels (same tile -> CTA mapping).
 int pipe_grid_size(int64_t num_tiles, int num_sms);
 
 // Host helpers (api.cu): encode 2D tiled tensor maps; false if TMA cannot be used.
 bool make_tile_map(CUtensorMap* map, const void* base, InType in, int64_t rows, int64_t cols,
                    int box_cols, int box_rows);
+// K-major code matrix [rows][pitch] read by the GEMM: box of box_bytes (128) x box_rows,
+// 128B swizzle, zero fill outside the matrix
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pitch,
+                      int box_bytes, int box_rows);
 // byte matrix [rows][pitch] (an output of codes), box of box_bytes x box_rows
 bool make_byte_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pitch,
                    int box_bytes, int box_rows);

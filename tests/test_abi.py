@@ -81,3 +81,28 @@ def test_host_validation_without_gpu(lib_path):
     assert st == nv.NVFP4_ERR_INVALID and "num_groups" in nv.nvfp4_last_error()
     st = L.nvfp4_amax(1, nv.NVFP4_IN_BF16, 4, 4, None, None, None, None, None)
     assert st == nv.NVFP4_ERR_INVALID
+
+
+def test_gemm_host_validation_without_gpu(lib_path):
+    """nvfp4_gemm's argument checks and workspace size are host-only."""
+    import nvfp4_precision_quantization_gb300 as nv
+    L = nv.load_library()
+    # chunked scales: A 3 x 128 chunks of 512 B, B 2 tiles x 2 halves x 128 chunks
+    assert nv.nvfp4_gemm_workspace_size(300, 500, 8192) == 3 * 128 * 512 + 4 * 128 * 512
+    assert nv.nvfp4_gemm_workspace_size(0, 500, 8192) == 0
+    ok = nv._COperand(256, 256, 256, nv.NVFP4_ROW_SCALED, 448.0)
+    bad_bound = nv._COperand(256, 256, 256, nv.NVFP4_ROW_SCALED, 500.0)
+    unaligned = nv._COperand(257, 256, 256, nv.NVFP4_PER_TENSOR, 256.0)
+    R = ctypes.byref
+    st = L.nvfp4_gemm(R(ok), R(bad_bound), 4, 4, 64, 256, nv.NVFP4_OUT_BF16, 256, 1 << 20, None)
+    assert st == nv.NVFP4_ERR_INVALID and "bound" in nv.nvfp4_last_error()
+    st = L.nvfp4_gemm(R(ok), R(ok), 4, 4, 48, 256, nv.NVFP4_OUT_BF16, 256, 1 << 20, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "multiple of 32" in nv.nvfp4_last_error()
+    st = L.nvfp4_gemm(R(ok), R(unaligned), 4, 4, 64, 256, nv.NVFP4_OUT_FP32, 256, 1 << 20, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "aligned" in nv.nvfp4_last_error()
+    st = L.nvfp4_gemm(R(ok), R(ok), 4, 4, 64, 256, nv.NVFP4_OUT_FP32, 256, 16, None)
+    assert st == nv.NVFP4_ERR_INVALID and "workspace" in nv.nvfp4_last_error()
+    st = L.nvfp4_gemm(R(ok), R(ok), 4, 4, 64, 256, 5, 256, 1 << 20, None)
+    assert st == nv.NVFP4_ERR_INVALID and "out_dtype" in nv.nvfp4_last_error()
+    st = L.nvfp4_gemm(None, R(ok), 4, 4, 64, 256, nv.NVFP4_OUT_FP32, 256, 1 << 20, None)
+    assert st == nv.NVFP4_ERR_INVALID

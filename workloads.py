@@ -16,6 +16,13 @@ operands they describe):
               each group zero-padded to a multiple of 128 rows, K = 7168, N(0,1).
   edge        4000 x 5000 N(0,1) in BF16 and FP32, 8192 x 8192 N(0, 0.02),
               4096 x 4096 with every 8th row zero, an all-zero tensor (seed 4).
+  gemm        NVFP4 operand bytes for the GEMM consumer, drawn directly: code bytes
+              uniform over all 256 values (every pair of E2M1 codes, both signs),
+              scale bytes uniform over the normal positive E4M3 codes 0x08..0x7E,
+              amax log-uniform in [1e-2, 1e2] per line (or one value per tensor).
+              Shapes of the linear layer above: fprop X (16384 x 8192) times the
+              weight W (28672 x 8192)^T, wgrad dY^T (28672 x 16384) times X^T
+              (8192 x 16384)^T (seed 5 and up).
 """
 from __future__ import annotations
 
@@ -23,7 +30,7 @@ import math
 
 import torch
 
-SEEDS = {"tiny": 0, "outliers": 1, "linear": 2, "moe": 3, "edge": 4}
+SEEDS = {"tiny": 0, "outliers": 1, "linear": 2, "moe": 3, "edge": 4, "gemm": 5}
 
 
 def generator(seed: int, device) -> torch.Generator:
@@ -130,3 +137,20 @@ def seeded_normal(rows: int, cols: int, seed: int, dtype=torch.bfloat16, device=
         u = torch.rand(rows, 1, generator=g, device=device) * 2.0 - 1.0
         x = x * torch.pow(10.0, row_scale_decades * u)
     return x.to(dtype)
+
+
+def nvfp4_operand(lines: int, k: int, seed: int, row_scaled: bool = True, device="cpu"):
+    """Random NVFP4 operand bytes (codes [lines][k/2], scales [lines][k/16], amax
+    [lines] or [1]) for the GEMM consumer; see the module docstring."""
+    g = generator(SEEDS["gemm"] * 1000 + seed, device)
+    codes = torch.randint(0, 256, (lines, k // 2), generator=g, device=device, dtype=torch.int32)
+    scales = torch.randint(0x08, 0x7F, (lines, k // 16), generator=g, device=device,
+                           dtype=torch.int32)
+    u = torch.rand(lines if row_scaled else 1, generator=g, device=device)
+    lo, hi = math.log(1e-2), math.log(1e2)
+    amax = torch.exp(lo + (hi - lo) * u).to(torch.float32)
+    return codes.to(torch.uint8), scales.to(torch.uint8), amax
+
+
+# linear-layer GEMM shapes (m, n, k): fprop Y = X W^T and wgrad dW = dY^T X
+GEMM_SHAPES = {"fprop": (16384, 28672, 8192), "wgrad": (28672, 8192, 16384)}
