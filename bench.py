@@ -338,6 +338,10 @@ SUPPLEMENTARY = {
     "moe-ragged": "MoE tokens as above, quantized straight from the unpadded tokens into the "
                   "padded layout (padding rows not read): per-group amax, four-over-six, "
                   "bound 256, rowwise",
+    "gemm": "NVFP4 GEMM consumer of the linear layer: fprop Y[16384x28672] = X[16384x8192] "
+            "W[28672x8192]^T (X row-scaled, W per-tensor) and wgrad dW[28672x8192] = "
+            "dY^T[28672x16384] X (both row-scaled: bilateral post-scale); random NVFP4 operand "
+            "bytes, BF16 output",
 }
 
 
@@ -609,6 +613,125 @@ def measure_e2e(nv, ops, outs, cfg, stream, dev, steps):
             "overlap": "H2D, quantize and D2H on separate streams"}
 
 
+def tensor_peak():
+    """FP4 dense tensor peak: the measured BF16 burst GEMM rate times the nominal
+    FP4 / BF16 ratio (13.5 / 2.25 = 6)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return 6.0 * float(json.load(open(p))["bf16_tflops"]), "of measured bf16 burst x 6"
+    return 6.0 * 1900.0, "of fallback bf16 x 6"
+
+
+def gemm_oracle_sample(lines: int):
+    """The oracle's FP64 GEMM (single thread) on lines x lines outputs of the fprop
+    shape's K, in TFLOP/s of the products it forms."""
+    import numpy as np
+
+    import oracle
+    import workloads
+    k = workloads.GEMM_SHAPES["fprop"][2]
+    ops = []
+    for seed, rs in ((21, True), (22, False)):
+        c, sc, a = workloads.nvfp4_operand(lines, k, seed, row_scaled=rs)
+        ops.append(dict(codes=c.numpy(), scales=sc.numpy(), amax=a.numpy(), row_scaled=rs,
+                        bound=448.0))
+    t0 = time.perf_counter()
+    oracle.gemm(ops[0], ops[1])
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * lines * lines * k / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{lines} x {lines} outputs of the fprop GEMM (k = {k}), FP64"}
+
+
+def run_gemm(args):
+    """The GEMM consumer of the linear layer's NVFP4 operands: fprop Y = X W^T
+    (X row-scaled, W per-tensor) and wgrad dW = dY^T X (both row-scaled: the
+    bilateral post-scale), BF16 output; one step = both GEMMs."""
+    import torch
+
+    import nvfp4_precision_quantization_gb300 as nv
+    import workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    nv.load_library()
+    calls, flops = [], 0
+    for i, (name, b_rs) in enumerate((("fprop", False), ("wgrad", True))):
+        m, n, k = workloads.GEMM_SHAPES[name]
+        ca, sa, aa = workloads.nvfp4_operand(m, k, 31 + 2 * i, row_scaled=True, device=dev)
+        cb, sb, ab = workloads.nvfp4_operand(n, k, 32 + 2 * i, row_scaled=b_rs, device=dev)
+        a = nv.Operand(ca, sa, aa, nv.NVFP4_ROW_SCALED, 448.0)
+        b = nv.Operand(cb, sb, ab, nv.NVFP4_ROW_SCALED if b_rs else nv.NVFP4_PER_TENSOR, 448.0)
+        d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(nv.nvfp4_gemm_workspace_size(m, n, k), dtype=torch.uint8, device=dev)
+        calls.append((a, b, d, ws, 2.0 * m * n * k))
+        flops += 2.0 * m * n * k
+
+    def step(ev):
+        for j, (a, b, d, ws, _) in enumerate(calls):
+            if j == 1:
+                ev[0].record(stream)
+            nv.nvfp4_gemm(a, b, d, ws, stream=stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = gemm_oracle_sample(args.oracle_rows or 64)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step([torch.cuda.Event(enable_timing=True)])
+    torch.cuda.synchronize()
+    K_ = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K_)]
+    ends_ = [torch.cuda.Event(enable_timing=True) for _ in range(K_)]
+    mids = [[torch.cuda.Event(enable_timing=True)] for _ in range(K_)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    for k_ in range(K_):
+        flush.zero_()
+        starts[k_].record(stream)
+        step(mids[k_])
+        ends_[k_].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends_)]
+    t_total, rate = job_throughput(sum(step_ms) / 1e3, world, flops, K_, dev)
+    kern_ms = statistics.mean(m[0].elapsed_time(e) for m, e in zip(mids, ends_))
+    peak, peak_src = tensor_peak()
+    achieved = calls[1][4] / (kern_ms / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "NVFP4 GEMM consumer TFLOP/s (fprop + wgrad of the linear layer)",
+            "value": rate / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K_,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K_, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32 acc, bf16 out",
+            "data": "synthetic",
+            "config": {"workload": SUPPLEMENTARY["gemm"],
+                       "l2": "a 256 MB L2 flush before each step",
+                       "flops_per_step": flops, "peak_tflops": peak, "peak_source": peak_src,
+                       "pct_of_tensor_peak": 100.0 * rate / 1e12 / world / peak},
+            "roofline": {"kernel": "nvfp4_gemm wgrad call (scale pre-pass + k_gemm_nvf4)",
+                         "bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": None, "algorithmic_flops": calls[1][4]},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": 3 * len(calls) * K_,
+            "clocks": clocks}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -630,6 +753,8 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "gemm":
+        run_gemm(args)
     elif args.workload in SUPPLEMENTARY:
         run_supplementary(args)
     else:

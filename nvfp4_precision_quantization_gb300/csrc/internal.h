@@ -150,7 +150,7 @@ struct GemmArgs {
   uint8_t* workspace;  // >= gemm_layout(M, N, K).workspace_bytes, 256-byte aligned
 };
 struct GemmLayout {
-  int64_t k_tiles, n_kc, tiles_m, tiles_n;
+  int64_t k_tiles, tiles_m, tiles_n;
   int64_t sfa_bytes, sfb_bytes, sfb_offset, workspace_bytes;
 };
 GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K);

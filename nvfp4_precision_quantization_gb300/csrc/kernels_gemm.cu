@@ -15,18 +15,22 @@
 // D = fl(fl(acc * alpha_i) * beta_j) -- the bilateral post-scale, fused, so the
 // accumulator never goes to HBM.
 //
-// Structure (one CTA per 128 x 256 output tile, 1 CTA per SM):
-//   warp 0   producer: TMA loads of the A and B code tiles (128 B of K per row,
-//            128B swizzle) and 1D bulk copies of their scale chunks, into a
-//            4-stage shared-memory ring guarded by mbarriers;
-//   warp 1   allocates TMEM (512 columns) and, from one thread, copies each
-//            stage's scales to TMEM (tcgen05.cp) and issues the MMAs (M = 128,
-//            N = 128, K = 64; two per K step for the 256 columns), releasing each
-//            stage with tcgen05.commit;
-//   warps 2-5 epilogue: read the accumulator (tcgen05.ld, one lane quarter per
-//            warp), apply alpha_i * beta_j, convert and store D.
+// Structure (persistent: one CTA per SM walks 128 x 256 output tiles, tile c,
+// c + gridDim.x, ..., groups of 16 M tiles side by side so their A tiles stay in L2):
+//   warp 0    producer: TMA loads of the A and B code tiles (128 B of K per row,
+//             128B swizzle) and 1D bulk copies of their scale chunks, into a
+//             4-stage shared-memory ring guarded by mbarriers, running on across
+//             tile boundaries;
+//   warp 1    allocates TMEM (512 columns) and, from one thread, copies each
+//             stage's scales to TMEM (tcgen05.cp) and issues the MMAs (M = 128,
+//             N = 256, K = 64, four per stage), releasing each stage with
+//             tcgen05.commit and the finished accumulator with one more;
+//   warps 2-9 epilogue, two per TMEM lane quarter (128 columns each): copy the
+//             accumulator to registers (tcgen05.ld), hand TMEM back to the MMA
+//             warp at once (the next tile's MMAs overlap the rest), then apply
+//             alpha_i * beta_j, convert and store D.
 // Scales reach the kernel in the tensor core's chunk layout: a pre-pass
-// (k_sf_block) rewrites the compact [lines][k/16] scales into 512-byte chunks of
+// (k_sf_chunks) rewrites the compact [lines][k/16] scales into 512-byte chunks of
 // 128 lines x 4 scales, byte (l % 32) * 16 + (l / 32) * 4 + s, which one
 // tcgen05.cp .32x128b.warpx4 moves into four TMEM columns.
 //
@@ -44,27 +48,43 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kBM = 128;                   // tile rows of A = MMA M
-constexpr int kBN = 256;                   // tile rows of B = output columns per tile
-constexpr int kUmmaN = 128;                // N of one MMA instruction
-constexpr int kHalves = kBN / kUmmaN;      // MMAs per K step
+constexpr int kBN = 256;                   // tile rows of B = output columns per tile = MMA N
 constexpr int kBKBytes = 128;              // K bytes per stage and row: 256 E2M1 values
 constexpr int kUmmaKBytes = 32;            // K = 64 values per MMA
 constexpr int kKSteps = kBKBytes / kUmmaKBytes;  // 4
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBKBytes;    // 16 KB
 constexpr int kBBytes = kBN * kBKBytes;    // 32 KB
-constexpr int kSfChunk = 512;              // 128 lines x 4 scales
-constexpr int kSfaBytes = kKSteps * kSfChunk;            // 2 KB
-constexpr int kSfbBytes = kHalves * kKSteps * kSfChunk;  // 4 KB
-constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-constexpr int kThreads = 192;
+constexpr int kEpilogueWarps = 8;                    // two per TMEM lane quarter
+constexpr int kEpiCols = kBN / 2;                     // accumulator columns per epilogue warp
+constexpr int kThreads = 64 + 32 * kEpilogueWarps;    // producer, MMA, epilogue
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSfCol0 = kBN;                            // scale columns follow the accumulator
-constexpr int kSfColsPerStage = kKSteps * 4 * (1 + kHalves);
-constexpr int kMetaBytes = 2048;  // barriers, TMEM address, error flag, beta of the tile
-constexpr int kSmemBytes = kStages * kStageBytes + kMetaBytes + 1024 /* alignment */;
-static_assert(kSfCol0 + kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM columns");
-static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128B swizzle");
+constexpr int kSfCol0 = kBN;                          // scale columns follow the accumulator
+constexpr int kMetaBytes = 1024;                      // barriers, TMEM address, error flag
+
+// Where the tensor core reads the scales of a block-scaled MMA with M = 128 and
+// scale_vec::4X: the four scales (one 32-bit TMEM word) of line l of A for the
+// MMA's K = 64 sit in TMEM lane l at column base + l / 32; for B (N = 256) line n
+// sits in lane n % 128 at column base + n / 32, base a multiple of 4 columns.  They
+// get there as 512-byte chunks of 128 lines x 4 scales, byte (l % 32) * 16 +
+// (l / 32) * 4 + s, each moved by one tcgen05.cp .32x128b.warpx4 (replicated into
+// all four lane quarters): 4 copies for A and 8 for B per stage, base columns 4
+// (A) and 8 (B) apart per K step.
+struct ChunkSf {
+  static constexpr int kStages = 4;
+  static constexpr int kSfaBytes = kKSteps * 512;
+  static constexpr int kSfbBytes = 2 * kKSteps * 512;
+  static constexpr int kSfaCols = 4 * kKSteps, kSfbCols = 8 * kKSteps;
+};
+template <class SF>
+struct GemmGeom {
+  static constexpr int kStageBytes = kABytes + kBBytes + SF::kSfaBytes + SF::kSfbBytes;
+  static constexpr int kSfColsPerStage = SF::kSfaCols + SF::kSfbCols;
+  static constexpr int kSmemBytes = SF::kStages * kStageBytes + kMetaBytes + 1024 /* alignment */;
+  static_assert(kSfCol0 + SF::kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM columns");
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128B swizzle");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
 
 // ---------------------------------------------------------------- tcgen05 wrappers
 
@@ -94,7 +114,7 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                : "memory");
 }
 // 32 lanes x 128 bits from shared memory, replicated into all four lane quarters.
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
 }
@@ -136,11 +156,11 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Descriptor of one 512-byte scale chunk read as 32 rows of 16 bytes, no swizzle:
-// 8-row core matrices 128 bytes apart, one core matrix along the 16-byte width.
-__device__ __forceinline__ uint64_t desc_sf_chunk(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) |
-         ((uint64_t)1 << 46);
+// Descriptor of a no-swizzle K-major scale matrix: 8-row x 16-byte core matrices
+// `sbo` bytes apart along the lines and `lbo` bytes apart along the row.
+__device__ __forceinline__ uint64_t desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | ((uint64_t)1 << 46);
 }
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -152,15 +172,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // ---------------------------------------------------------------- scale pre-pass
 
-// Compact scales [rows][k16] -> chunks [n_rb][n_kc][512 bytes]: chunk (rb, kc)
-// holds lines rb*128 .. +127 and scales kc*4 .. +3, line l at byte
-// (l % 32) * 16 + (l / 32) * 4, scale s at + s.  Lines and scales past the
-// operand are zero (a zero scale times the zero-filled codes there adds 0).
-__global__ void __launch_bounds__(256) k_sf_block(const uint8_t* __restrict__ sc, int64_t rows,
-                                                  int64_t k16, int64_t n_kc, int64_t n_words,
-                                                  uint32_t* __restrict__ out) {
+// Compact scales [rows][k16] -> chunks [n_rb][n_kc][512 bytes]:
+// chunk (rb, kc) holds lines rb*128 .. +127 and scales kc*4 .. +3, line l at byte
+// (l % 32) * 16 + (l / 32) * 4, scale s at + s.  Lines and scales past the operand
+// are zero (a zero scale times the zero-filled codes there adds 0).
+__global__ void __launch_bounds__(256) k_sf_chunks(const uint8_t* __restrict__ sc, int64_t rows,
+                                                   int64_t k16, int64_t n_kc, int64_t n_words,
+                                                   uint32_t* __restrict__ out) {
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n_words;
        w += (int64_t)gridDim.x * blockDim.x) {
     const int64_t chunk = w >> 7;
@@ -183,7 +207,7 @@ __global__ void __launch_bounds__(256) k_sf_block(const uint8_t* __restrict__ sc
 // ---------------------------------------------------------------- the GEMM
 
 struct GemmParams {
-  const uint8_t* sfa;  // chunked scales of A, n_kc chunks per 128-line block
+  const uint8_t* sfa;  // A's scales in the kernel's layout
   const uint8_t* sfb;
   const float* a_amax;
   const float* b_amax;
@@ -192,7 +216,6 @@ struct GemmParams {
   float a_finv, b_finv;  // fl(1 / (bound * 6)) of each operand
   int M, N;
   int k_tiles;  // ceil(K / 256)
-  int n_kc;     // 4 * k_tiles
   int tiles_m, tiles_n;
   void* d;
   bool d_bf16;
@@ -202,35 +225,44 @@ struct GemmParams {
 
 constexpr int kRasterGroup = 16;  // M tiles walked together so their A tiles stay in L2
 
+__device__ __forceinline__ void tile_coords(int idx, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int group = idx / (kRasterGroup * tiles_n);
+  const int first_m = group * kRasterGroup;
+  const int gm = min(tiles_m - first_m, kRasterGroup);
+  const int rem = idx - group * kRasterGroup * tiles_n;
+  tm = first_m + rem % gm;
+  tn = rem / gm;
+}
+
+// Persistent: CTA c computes tiles c, c + gridDim.x, ...  The load ring runs on
+// across tile boundaries; the epilogue copies the accumulator to registers,
+// hands TMEM back (acc_empty) and stores while the MMAs of the next tile run.
+template <class SF>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_nvf4(const __grid_constant__ CUtensorMap map_a,
                 const __grid_constant__ CUtensorMap map_b, const GemmParams p) {
+  using G = GemmGeom<SF>;
+  constexpr int S = SF::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   int* err = reinterpret_cast<int*>(tmem_slot + 1);
-  float* s_beta = reinterpret_cast<float*>(smem + kStages * kStageBytes + 1024);  // [kBN]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // tile of this CTA: groups of kRasterGroup M tiles, M fastest inside a group
-  const int idx = blockIdx.x;
-  const int group = idx / (kRasterGroup * p.tiles_n);
-  const int first_m = group * kRasterGroup;
-  const int gm = min(p.tiles_m - first_m, kRasterGroup);
-  const int rem = idx - group * kRasterGroup * p.tiles_n;
-  const int tm = first_m + rem % gm, tn = rem / gm;
+  const int num_tiles = p.tiles_m * p.tiles_n;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpilogueWarps);
     *err = 0;
     fence_mbar_init();
     prefetch_tmap(&map_a);
@@ -249,129 +281,177 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- producer
     const uint64_t pol_a = policy_evict_last();
     const uint64_t pol_b = policy_evict_normal();
-    int issued = 0;
-    for (int kt = 0; kt < p.k_tiles; ++kt) {
-      const int s = kt % kStages;
-      if (kt >= kStages && !mbar_wait_bounded(&empty[s], ((kt / kStages) - 1) & 1)) {
-        *err = 1;
-        break;
+    uint32_t it = 0;  // K tiles issued, over all tiles of this CTA
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      int tm, tn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+        const uint32_t s = it % S;
+        if (it >= (uint32_t)S && !mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1)) {
+          *err = 1;
+          ok = false;
+          break;
+        }
+        if (*(volatile int*)err) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * G::kStageBytes;
+        uint8_t* st_sf = st + kABytes + kBBytes;
+        mbar_expect_tx(&full[s], G::kStageBytes);
+        tma_load_2d(st, &map_a, &full[s], kt * kBKBytes, tm * kBM, pol_a);
+        tma_load_2d(st + kABytes, &map_b, &full[s], kt * kBKBytes, tn * kBN, pol_b);
+        const int64_t n_kc = (int64_t)p.k_tiles * kKSteps;
+        bulk_load(st_sf, p.sfa + ((int64_t)tm * n_kc + kt * kKSteps) * 512, SF::kSfaBytes,
+                  &full[s], pol_a);
+        for (int h = 0; h < 2; ++h)
+          bulk_load(st_sf + SF::kSfaBytes + h * kKSteps * 512,
+                    p.sfb + ((int64_t)(tn * 2 + h) * n_kc + kt * kKSteps) * 512, kKSteps * 512,
+                    &full[s], pol_b);
       }
-      if (*(volatile int*)err) break;
-      uint8_t* st = smem + s * kStageBytes;
-      mbar_expect_tx(&full[s], kStageBytes);
-      tma_load_2d(st, &map_a, &full[s], kt * kBKBytes, tm * kBM, pol_a);
-      tma_load_2d(st + kABytes, &map_b, &full[s], kt * kBKBytes, tn * kBN, pol_b);
-      const uint8_t* sa = p.sfa + ((int64_t)tm * p.n_kc + kt * kKSteps) * kSfChunk;
-      bulk_load(st + kABytes + kBBytes, sa, kSfaBytes, &full[s], pol_a);
-      for (int h = 0; h < kHalves; ++h) {
-        const uint8_t* sb =
-            p.sfb + ((int64_t)(tn * kHalves + h) * p.n_kc + kt * kKSteps) * kSfChunk;
-        bulk_load(st + kABytes + kBBytes + kSfaBytes + h * kKSteps * kSfChunk, sb,
-                  kKSteps * kSfChunk, &full[s], pol_b);
-      }
-      issued = kt + 1;
     }
     // drain: every copy issued must have landed before the CTA may exit
-    for (int kt = max(0, issued - kStages); kt < issued; ++kt)
-      if (!mbar_wait_bounded(&full[kt % kStages], (kt / kStages) & 1)) *err = 1;
+    for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; ++j)
+      if (!mbar_wait_bounded(&full[j % S], (j / S) & 1)) *err = 1;
   } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    int issued = 0;
-    for (int kt = 0; kt < p.k_tiles; ++kt) {
-      const int s = kt % kStages;
-      if (!mbar_wait_bounded(&full[s], (kt / kStages) & 1)) {
+    // ---------------- MMA issuer: per K tile, the stage's scales to TMEM, then
+    // the four MMAs (K = 64 each) that read them
+    auto copy_scales = [&](uint32_t j) {
+      const uint32_t s = j % S;
+      const uint32_t st_sfa = smem_addr(smem + s * G::kStageBytes) + kABytes + kBBytes;
+      const uint32_t st_sfb = st_sfa + SF::kSfaBytes;
+      const uint32_t sfa_col = tmem + kSfCol0 + s * G::kSfColsPerStage;
+      const uint32_t sfb_col = sfa_col + SF::kSfaCols;
+#pragma unroll
+      for (int ks = 0; ks < kKSteps; ++ks) {
+        tc_cp_32x128b_x4(sfa_col + 4 * ks, desc_plain(st_sfa + ks * 512, 0, 128));
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tc_cp_32x128b_x4(sfb_col + 8 * ks + 4 * h,
+                           desc_plain(st_sfb + (h * kKSteps + ks) * 512, 0, 128));
+      }
+    };
+    uint32_t it = 0, t = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++t) {
+      // the epilogue of the previous tile has copied the accumulator out
+      if (t > 0 && !mbar_wait_bounded(acc_empty, (t - 1) & 1)) {
         *err = 1;
         break;
       }
-      if (*(volatile int*)err) break;
       tc_fence_after();
-      const uint32_t st = smem_addr(smem + s * kStageBytes);
-      const uint32_t st_sfa = st + kABytes + kBBytes;
-      const uint32_t st_sfb = st_sfa + kSfaBytes;
-      const uint32_t sf_col = tmem + kSfCol0 + s * kSfColsPerStage;
-#pragma unroll
-      for (int ks = 0; ks < kKSteps; ++ks) {
-        tc_cp_sf(sf_col + ks * 4, desc_sf_chunk(st_sfa + ks * kSfChunk));
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tc_cp_sf(sf_col + kKSteps * 4 + (ks * kHalves + h) * 4,
-                   desc_sf_chunk(st_sfb + (h * kKSteps + ks) * kSfChunk));
-      }
-#pragma unroll
-      for (int ks = 0; ks < kKSteps; ++ks) {
-        const uint64_t adesc = desc_sw128(st + ks * kUmmaKBytes);
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h) {
-          const uint64_t bdesc = desc_sw128(st + kABytes + h * kUmmaN * kBKBytes + ks * kUmmaKBytes);
-          tc_mma_nvf4(tmem + h * kUmmaN, adesc, bdesc, p.idesc, sf_col + ks * 4,
-                      sf_col + kKSteps * 4 + (ks * kHalves + h) * 4, (kt | ks) != 0);
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+        const uint32_t s = it % S;
+        if (!mbar_wait_bounded(&full[s], (it / S) & 1)) {
+          *err = 1;
+          ok = false;
+          break;
         }
+        if (*(volatile int*)err) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        copy_scales(it);
+        const uint32_t st = smem_addr(smem + s * G::kStageBytes);
+        const uint32_t sfa_col = tmem + kSfCol0 + s * G::kSfColsPerStage;
+        const uint32_t sfb_col = sfa_col + SF::kSfaCols;
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ++ks)
+          tc_mma_nvf4(tmem, desc_sw128(st + ks * kUmmaKBytes),
+                      desc_sw128(st + kABytes + ks * kUmmaKBytes), p.idesc, sfa_col + 4 * ks,
+                      sfb_col + 8 * ks, (kt | ks) != 0);
+        tc_commit(&empty[s]);
       }
-      tc_commit(&empty[s]);
-      issued = kt + 1;
+      // the accumulator of this tile is complete (or abandoned) once all issued MMAs are
+      tc_commit(acc_full);
     }
-    // the accumulator is complete (or abandoned) once everything issued is done
-    if (issued > 0) tc_commit(acc_full);
-    else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(acc_full)) : "memory");
-    if (!mbar_wait_bounded(acc_full, 0)) *err = 1;
+    // everything issued must be done before TMEM is freed
+    if (t > 0 && !mbar_wait_bounded(acc_full, (t - 1) & 1)) *err = 1;
   } else if (warp >= 2) {
-    // ---------------- epilogue: lane quarter q = rows 32q .. 32q+31 of the tile
+    // ---------------- epilogue: lane quarter q (rows 32q ..), column half `half`
     const int q = warp & 3;
-    for (int t = threadIdx.x - 64; t < kBN; t += 128) {
-      const int col = tn * kBN + t;
-      s_beta[t] = col < p.N ? __fmul_rn(p.b_amax[(int64_t)col * p.b_amax_stride], p.b_finv) : 0.0f;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
-    const bool ready = mbar_wait_bounded(acc_full, 0);
-    tc_fence_after();
-    const int row = tm * kBM + q * 32 + lane;
-    const bool row_ok = row < p.M;
-    const float alpha =
-        row_ok ? __fmul_rn(p.a_amax[(int64_t)row * p.a_amax_stride], p.a_finv) : 0.0f;
-    const bool write = ready && *(volatile int*)err == 0;
-    if (!ready) *err = 1;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, v);
+    const int half = (warp - 2) >> 2;
+    const bool b_vec = p.b_amax_stride != 0 && (reinterpret_cast<uintptr_t>(p.b_amax) & 15) == 0;
+    uint32_t t = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
+      int tm, tn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+      const bool ready = mbar_wait_bounded(acc_full, t & 1);
+      if (!ready) *err = 1;
+      tc_fence_after();
+      uint32_t v[kEpiCols];
+#pragma unroll
+      for (int c = 0; c < kEpiCols / 32; ++c)
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + half * kEpiCols + c * 32, v + c * 32);
       tmem_ld_wait();
-      const int col0 = tn * kBN + c * 32;
-      if (!write || !row_ok || col0 >= p.N) continue;
-      float o[32];
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);  // TMEM may take the next tile's MMAs
+      if (!ready || *(volatile int*)err) break;
+
+      const int row = tm * kBM + q * 32 + lane;
+      const int col_base = tn * kBN + half * kEpiCols;
+      if (row >= p.M || col_base >= p.N) continue;
+      const float alpha = __fmul_rn(p.a_amax[(int64_t)row * p.a_amax_stride], p.a_finv);
+      const int nvalid = min(kEpiCols, p.N - col_base);
+      const int64_t off = (int64_t)row * p.N + col_base;
+      const bool vec = nvalid == kEpiCols &&
+                       ((reinterpret_cast<uintptr_t>(p.d) + off * (p.d_bf16 ? 2 : 4)) & 15) == 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        o[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), alpha), s_beta[c * 32 + j]);
-      const int64_t off = (int64_t)row * p.N + col0;
-      const int nvalid = min(32, p.N - col0);
-      if (p.d_bf16) {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.d) + off;
-        if (nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-          uint32_t w[16];
+      for (int c = 0; c < kEpiCols / 32; ++c) {
+        const int col0 = col_base + c * 32;
+        uint32_t* vc = v + c * 32;
+        // d = fl(fl(acc * alpha) * beta), beta = fl(amax_b[col] * fl(1/F_b))
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-            w[j] = *reinterpret_cast<uint32_t*>(&h2);
+        for (int j4 = 0; j4 < 8; ++j4) {
+          float b4[4];
+          if (b_vec && col0 + 32 <= p.N) {
+            const float4 t4 = __ldg(reinterpret_cast<const float4*>(p.b_amax + col0) + j4);
+            b4[0] = t4.x, b4[1] = t4.y, b4[2] = t4.z, b4[3] = t4.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              b4[j] = __ldg(p.b_amax + (int64_t)min(col0 + 4 * j4 + j, p.N - 1) * p.b_amax_stride);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(dst + 8 * j) =
-                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nvalid) dst[j] = __float2bfloat16_rn(o[j]);
+            vc[4 * j4 + j] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(vc[4 * j4 + j]), alpha),
+                                                       __fmul_rn(b4[j], p.b_finv)));
         }
-      } else {
-        float* dst = static_cast<float*>(p.d) + off;
-        if (nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        if (p.d_bf16) {
+          uint16_t* dst = static_cast<uint16_t*>(p.d) + off + c * 32;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(dst + 4 * j) =
-                make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(vc[8 * g + 2 * j]),
+                                                        __uint_as_float(vc[8 * g + 2 * j + 1]));
+              w[j] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            if (vec) {
+              *reinterpret_cast<uint4*>(dst + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (c * 32 + 8 * g + j < nvalid) dst[8 * g + j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+            }
+          }
         } else {
+          uint32_t* dst = static_cast<uint32_t*>(p.d) + off + c * 32;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nvalid) dst[j] = o[j];
+          for (int g = 0; g < 8; ++g) {
+            if (vec) {
+              *reinterpret_cast<uint4*>(dst + 4 * g) =
+                  make_uint4(vc[4 * g], vc[4 * g + 1], vc[4 * g + 2], vc[4 * g + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (c * 32 + 4 * g + j < nvalid) dst[4 * g + j] = vc[4 * g + j];
+            }
+          }
         }
       }
     }
@@ -400,26 +480,29 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K) {
   GemmLayout L;
   L.k_tiles = ceil_div(K, 2 * kBKBytes);
-  L.n_kc = L.k_tiles * kKSteps;
   L.tiles_m = ceil_div(M, kBM);
   L.tiles_n = ceil_div(N, kBN);
-  L.sfa_bytes = L.tiles_m * L.n_kc * kSfChunk;
-  L.sfb_bytes = L.tiles_n * kHalves * L.n_kc * kSfChunk;
+  L.sfa_bytes = L.tiles_m * L.k_tiles * ChunkSf::kSfaBytes;
+  L.sfb_bytes = L.tiles_n * L.k_tiles * ChunkSf::kSfbBytes;
   L.sfb_offset = (L.sfa_bytes + 255) / 256 * 256;
   L.workspace_bytes = L.sfb_offset + L.sfb_bytes;
   return L;
 }
 
-cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  const GemmLayout L = gemm_layout(a.M, a.N, a.K);
+template <class SF>
+static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const DeviceInfo& dev,
+                                 cudaStream_t stream) {
+  using G = GemmGeom<SF>;
   uint8_t* sfa = a.workspace;
   uint8_t* sfb = a.workspace + L.sfb_offset;
-  const int64_t words_a = L.sfa_bytes / 4, words_b = L.sfb_bytes / 4;
+  const int64_t words_a = L.tiles_m * L.k_tiles * SF::kSfaBytes / 4;
+  const int64_t words_b = L.tiles_n * L.k_tiles * SF::kSfbBytes / 4;
   const int pre_grid = (int)std::min<int64_t>(ceil_div(words_a + words_b, 256), 8 * dev.num_sms);
-  k_sf_block<<<pre_grid, 256, 0, stream>>>(a.a_scales, a.M, a.K / 16, L.n_kc, words_a,
-                                           reinterpret_cast<uint32_t*>(sfa));
-  k_sf_block<<<pre_grid, 256, 0, stream>>>(a.b_scales, a.N, a.K / 16, L.n_kc, words_b,
-                                           reinterpret_cast<uint32_t*>(sfb));
+  const int64_t n_kc = L.k_tiles * kKSteps;
+  k_sf_chunks<<<pre_grid, 256, 0, stream>>>(a.a_scales, a.M, a.K / 16, n_kc, words_a,
+                                            reinterpret_cast<uint32_t*>(sfa));
+  k_sf_chunks<<<pre_grid, 256, 0, stream>>>(a.b_scales, a.N, a.K / 16, n_kc, words_b,
+                                            reinterpret_cast<uint32_t*>(sfb));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -430,7 +513,8 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
 
   static bool attr_set[64] = {};
   if (dev.device < 64 && !attr_set[dev.device]) {
-    e = cudaFuncSetAttribute(k_gemm_nvf4, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(k_gemm_nvf4<SF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             G::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev.device] = true;
   }
@@ -446,16 +530,20 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
   p.M = (int)a.M;
   p.N = (int)a.N;
   p.k_tiles = (int)L.k_tiles;
-  p.n_kc = (int)L.n_kc;
   p.tiles_m = (int)L.tiles_m;
   p.tiles_n = (int)L.tiles_n;
   p.d = a.d;
   p.d_bf16 = a.d_bf16;
-  p.idesc = make_idesc_nvf4(kBM, kUmmaN);
+  p.idesc = make_idesc_nvf4(kBM, kBN);
   p.status = dev.status;
-  const int64_t tiles = L.tiles_m * L.tiles_n;
-  k_gemm_nvf4<<<(unsigned)tiles, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
+  const int grid = (int)std::min<int64_t>(L.tiles_m * L.tiles_n, dev.num_sms);
+  k_gemm_nvf4<SF><<<grid, kThreads, G::kSmemBytes, stream>>>(map_a, map_b, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  const GemmLayout L = gemm_layout(a.M, a.N, a.K);
+  return launch_gemm_t<ChunkSf>(a, L, dev, stream);
 }
 
 }  // namespace nvfp4
