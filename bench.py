@@ -663,8 +663,11 @@ def run_gemm(args):
     stream = torch.cuda.current_stream()
     nv.load_library()
     calls, flops = [], 0
-    for i, (name, b_rs) in enumerate((("fprop", False), ("wgrad", True))):
-        m, n, k = workloads.GEMM_SHAPES[name]
+    jobs = [("fprop", False), ("wgrad", True)]
+    if args.gemm_shape:  # one GEMM of the given shape, both operands row-scaled
+        jobs = [(tuple(args.gemm_shape), True)]
+    for i, (name, b_rs) in enumerate(jobs):
+        m, n, k = name if isinstance(name, tuple) else workloads.GEMM_SHAPES[name]
         ca, sa, aa = workloads.nvfp4_operand(m, k, 31 + 2 * i, row_scaled=True, device=dev)
         cb, sb, ab = workloads.nvfp4_operand(n, k, 32 + 2 * i, row_scaled=b_rs, device=dev)
         a = nv.Operand(ca, sa, aa, nv.NVFP4_ROW_SCALED, 448.0)
@@ -676,7 +679,7 @@ def run_gemm(args):
 
     def step(ev):
         for j, (a, b, d, ws, _) in enumerate(calls):
-            if j == 1:
+            if j == len(calls) - 1:
                 ev[0].record(stream)
             nv.nvfp4_gemm(a, b, d, ws, stream=stream)
 
@@ -710,22 +713,24 @@ def run_gemm(args):
     t_total, rate = job_throughput(sum(step_ms) / 1e3, world, flops, K_, dev)
     kern_ms = statistics.mean(m[0].elapsed_time(e) for m, e in zip(mids, ends_))
     peak, peak_src = tensor_peak()
-    achieved = calls[1][4] / (kern_ms / 1e3) / 1e12
+    achieved = calls[-1][4] / (kern_ms / 1e3) / 1e12
     if rank == 0:
         print(json.dumps({
-            "metric": "NVFP4 GEMM consumer TFLOP/s (fprop + wgrad of the linear layer)",
+            "metric": "NVFP4 GEMM consumer TFLOP/s" + ("" if args.gemm_shape else
+                                                      " (fprop + wgrad of the linear layer)"),
             "value": rate / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K_,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K_, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32 acc, bf16 out",
             "data": "synthetic",
-            "config": {"workload": SUPPLEMENTARY["gemm"],
+            "config": {"workload": SUPPLEMENTARY["gemm"] if not args.gemm_shape else
+                       "one NVFP4 GEMM %dx%dx%d, both operands row-scaled" % tuple(args.gemm_shape),
                        "l2": "a 256 MB L2 flush before each step",
                        "flops_per_step": flops, "peak_tflops": peak, "peak_source": peak_src,
                        "pct_of_tensor_peak": 100.0 * rate / 1e12 / world / peak},
-            "roofline": {"kernel": "nvfp4_gemm wgrad call (scale pre-pass + k_gemm_nvf4)",
+            "roofline": {"kernel": "nvfp4_gemm, last call of the step (scale pre-pass + k_gemm_nvf4)",
                          "bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": None, "algorithmic_flops": calls[1][4]},
+                         "traffic": None, "algorithmic_flops": calls[-1][4]},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": 3 * len(calls) * K_,
             "clocks": clocks}))
     if world > 1:
@@ -745,6 +750,9 @@ def main():
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows of X and dY (default 16384; smaller only for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-shape", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
+                    help="--workload gemm: one GEMM of this shape per step instead of the "
+                         "linear layer's two (smaller only for profiling captures)")
     ap.add_argument("--workload", default="linear",
                     choices=["linear", "linear-fos", *SUPPLEMENTARY],
                     help="linear (default): the headline workload; the others measure the "
