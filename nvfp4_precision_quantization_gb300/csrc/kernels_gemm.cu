@@ -18,9 +18,9 @@
 // Structure (persistent: one CTA per SM walks 128 x 256 output tiles, tile c,
 // c + gridDim.x, ..., groups of 16 M tiles side by side so their A tiles stay in L2):
 //   warp 0    producer: TMA loads of the A and B code tiles (128 B of K per row,
-//             128B swizzle) and 1D bulk copies of their scale chunks, into a
-//             4-stage shared-memory ring guarded by mbarriers, running on across
-//             tile boundaries;
+//             128B swizzle) and 1D bulk copies of their scales, into a 3-stage
+//             shared-memory ring (72 KB a stage) guarded by mbarriers, running on
+//             across tile boundaries;
 //   warp 1    allocates TMEM (512 columns) and, from one thread, copies each
 //             stage's scales to TMEM (tcgen05.cp) and issues the MMAs (M = 128,
 //             N = 256, K = 64, four per stage), releasing each stage with
@@ -29,10 +29,9 @@
 //             accumulator to registers (tcgen05.ld), hand TMEM back to the MMA
 //             warp at once (the next tile's MMAs overlap the rest), then apply
 //             alpha_i * beta_j, convert and store D.
-// Scales reach the kernel in the tensor core's chunk layout: a pre-pass
-// (k_sf_chunks) rewrites the compact [lines][k/16] scales into 512-byte chunks of
-// 128 lines x 4 scales, byte (l % 32) * 16 + (l / 32) * 4 + s, which one
-// tcgen05.cp .32x128b.warpx4 moves into four TMEM columns.
+// Scales reach the kernel in the layout their TMEM copies want (see SfLayout): a
+// pre-pass (k_sf_layout) rewrites the compact [lines][k/16] scales of both operands
+// into the caller's workspace.
 //
 // Every wait is bounded (about 2 s): on a timeout the kernel records
 // NVFP4_DEVICE_TIMEOUT, stops issuing work, waits (bounded) for what it already
@@ -62,17 +61,20 @@ constexpr int kSfCol0 = kBN;                          // scale columns follow th
 constexpr int kMetaBytes = 1024;                      // barriers, TMEM address, error flag
 
 // Where the tensor core reads the scales of a block-scaled MMA with M = 128 and
-// scale_vec::4X: the four scales (one 32-bit TMEM word) of line l of A for the
-// MMA's K = 64 sit in TMEM lane l at column base + l / 32; for B (N = 256) line n
-// sits in lane n % 128 at column base + n / 32, base a multiple of 4 columns.  They
-// get there as 512-byte chunks of 128 lines x 4 scales, byte (l % 32) * 16 +
-// (l / 32) * 4 + s, each moved by one tcgen05.cp .32x128b.warpx4 (replicated into
-// all four lane quarters): 4 copies for A and 8 for B per stage, base columns 4
-// (A) and 8 (B) apart per K step.
-struct ChunkSf {
-  static constexpr int kStages = 4;
-  static constexpr int kSfaBytes = kKSteps * 512;
-  static constexpr int kSfbBytes = 2 * kKSteps * 512;
+// scale_vec::4X (one 32-bit TMEM word = the four scales of a line for the MMA's
+// K = 64; base columns on multiples of 4): A's line l from its accumulator lane l
+// at column base + l / 32; B's line n (N = 256) by each lane quarter q of the tensor
+// core from its own lanes, lane 32q + n % 32, at column base + n / 32 -- B's scales
+// must be present in all four quarters.  They get there by tcgen05.cp .128x256b
+// (lane l <- a 32-byte row of shared memory, 8 columns): one copy holds two K steps
+// of A (row l: the words of K steps 2c and 2c + 1 at bytes 4q and 16 + 4q, q = l /
+// 32, zero elsewhere) or one K step of all 256 lines of B (row l: line 32c + l % 32
+// at bytes 4c).  Per K tile of 256: 2 + 4 copies, 8 + 16 KB of shared memory, 16 +
+// 32 TMEM columns (A's K step ks at base + 4ks, B's at base + 8ks).
+struct SfLayout {
+  static constexpr int kStages = 3;
+  static constexpr int kSfaBytes = 2 * 4096;
+  static constexpr int kSfbBytes = kKSteps * 4096;
   static constexpr int kSfaCols = 4 * kKSteps, kSfbCols = 8 * kKSteps;
 };
 template <class SF>
@@ -113,9 +115,9 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                    smem_addr(bar))
                : "memory");
 }
-// 32 lanes x 128 bits from shared memory, replicated into all four lane quarters.
-__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+// 128 lanes x 256 bits from shared memory: lane l, column c <- row l, bytes 4c .. 4c+3.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
 }
 // D (+)= (A x scaleA) * (B x scaleB)^T, E2M1 operands with one E4M3 scale per 16 values.
@@ -178,26 +180,38 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 // ---------------------------------------------------------------- scale pre-pass
 
-// Compact scales [rows][k16] -> chunks [n_rb][n_kc][512 bytes]:
-// chunk (rb, kc) holds lines rb*128 .. +127 and scales kc*4 .. +3, line l at byte
-// (l % 32) * 16 + (l / 32) * 4, scale s at + s.  Lines and scales past the operand
-// are zero (a zero scale times the zero-filled codes there adds 0).
-__global__ void __launch_bounds__(256) k_sf_chunks(const uint8_t* __restrict__ sc, int64_t rows,
-                                                   int64_t k16, int64_t n_kc, int64_t n_words,
-                                                   uint32_t* __restrict__ out) {
+// Scale pre-pass.  Compact scales [rows][k16] -> [n_blk][k_tiles][copies][4096] for
+// blocks of 128 * P lines (P = 1: A, two copies per K tile; P = 2: B, four).  In
+// copy c, lane l owns a 32-byte row of eight 4-byte words (the four scales of one
+// line and K step each, zero where unused):
+//   A (P = 1): word 4u + q (q = l / 32) of row l = line blk * 128 + l, K step 2c + u;
+//   B (P = 2): word cc of row l = line blk * 256 + 32 cc + l % 32, K step c.
+// Stored as one tcgen05.cp .128x256b reads it: 16-byte half u at 2048 u, row l at
+// 16 l.  One thread writes one 32-bit word.
+__global__ void __launch_bounds__(256) k_sf_layout(const uint8_t* __restrict__ sc, int64_t rows,
+                                                  int64_t k16, int64_t k_tiles, int P,
+                                                  int64_t n_words, uint32_t* __restrict__ out) {
+  const int copies = P == 1 ? kKSteps / 2 : kKSteps;
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n_words;
        w += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t chunk = w >> 7;
-    const int inner = (int)(w & 127);
-    const int64_t rb = chunk / n_kc, kc = chunk - rb * n_kc;
-    const int64_t line = rb * 128 + (inner & 3) * 32 + (inner >> 2);
+    const int inner = (int)(w & 1023);  // word within one 4096-byte copy
+    const int64_t cpy = w >> 10;
+    const int c = (int)(cpy % copies);
+    const int64_t bk = cpy / copies;
+    const int64_t kt = bk % k_tiles, blk = bk / k_tiles;
+    const int u = inner >> 9;
+    const int l = (inner >> 2) & 127;
+    const int wb = inner & 3;
     uint32_t word = 0;
-    if (line < rows) {
-      const uint8_t* p = sc + line * k16;
+    const bool used = P == 1 ? wb == (l >> 5) : true;
+    if (used) {
+      const int64_t line = P == 1 ? blk * 128 + l : blk * 256 + 32 * (4 * u + wb) + (l & 31);
+      const int ks = P == 1 ? 2 * c + u : c;
+      const int64_t s0 = kt * 16 + ks * 4;
+      if (line < rows) {
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int64_t s = kc * 4 + b;
-        if (s < k16) word |= (uint32_t)p[s] << (8 * b);
+        for (int j = 0; j < 4; ++j)
+          if (s0 + j < k16) word |= (uint32_t)sc[line * k16 + s0 + j] << (8 * j);
       }
     }
     out[w] = word;
@@ -302,13 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&full[s], G::kStageBytes);
         tma_load_2d(st, &map_a, &full[s], kt * kBKBytes, tm * kBM, pol_a);
         tma_load_2d(st + kABytes, &map_b, &full[s], kt * kBKBytes, tn * kBN, pol_b);
-        const int64_t n_kc = (int64_t)p.k_tiles * kKSteps;
-        bulk_load(st_sf, p.sfa + ((int64_t)tm * n_kc + kt * kKSteps) * 512, SF::kSfaBytes,
+        bulk_load(st_sf, p.sfa + ((int64_t)tm * p.k_tiles + kt) * SF::kSfaBytes, SF::kSfaBytes,
                   &full[s], pol_a);
-        for (int h = 0; h < 2; ++h)
-          bulk_load(st_sf + SF::kSfaBytes + h * kKSteps * 512,
-                    p.sfb + ((int64_t)(tn * 2 + h) * n_kc + kt * kKSteps) * 512, kKSteps * 512,
-                    &full[s], pol_b);
+        bulk_load(st_sf + SF::kSfaBytes, p.sfb + ((int64_t)tn * p.k_tiles + kt) * SF::kSfbBytes,
+                  SF::kSfbBytes, &full[s], pol_b);
       }
     }
     // drain: every copy issued must have landed before the CTA may exit
@@ -323,14 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st_sfb = st_sfa + SF::kSfaBytes;
       const uint32_t sfa_col = tmem + kSfCol0 + s * G::kSfColsPerStage;
       const uint32_t sfb_col = sfa_col + SF::kSfaCols;
+      // 128 rows x 32 bytes per copy: 16-byte halves 2048 bytes apart, rows 16 apart
 #pragma unroll
-      for (int ks = 0; ks < kKSteps; ++ks) {
-        tc_cp_32x128b_x4(sfa_col + 4 * ks, desc_plain(st_sfa + ks * 512, 0, 128));
+      for (int c = 0; c < kKSteps / 2; ++c)
+        tc_cp_128x256b(sfa_col + 8 * c, desc_plain(st_sfa + c * 4096, 2048, 128));
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tc_cp_32x128b_x4(sfb_col + 8 * ks + 4 * h,
-                           desc_plain(st_sfb + (h * kKSteps + ks) * 512, 0, 128));
-      }
+      for (int ks = 0; ks < kKSteps; ++ks)
+        tc_cp_128x256b(sfb_col + 8 * ks, desc_plain(st_sfb + ks * 4096, 2048, 128));
     };
     uint32_t it = 0, t = 0;
     bool ok = true;
@@ -482,8 +492,8 @@ GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K) {
   L.k_tiles = ceil_div(K, 2 * kBKBytes);
   L.tiles_m = ceil_div(M, kBM);
   L.tiles_n = ceil_div(N, kBN);
-  L.sfa_bytes = L.tiles_m * L.k_tiles * ChunkSf::kSfaBytes;
-  L.sfb_bytes = L.tiles_n * L.k_tiles * ChunkSf::kSfbBytes;
+  L.sfa_bytes = L.tiles_m * L.k_tiles * SfLayout::kSfaBytes;
+  L.sfb_bytes = L.tiles_n * L.k_tiles * SfLayout::kSfbBytes;
   L.sfb_offset = (L.sfa_bytes + 255) / 256 * 256;
   L.workspace_bytes = L.sfb_offset + L.sfb_bytes;
   return L;
@@ -498,11 +508,10 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const D
   const int64_t words_a = L.tiles_m * L.k_tiles * SF::kSfaBytes / 4;
   const int64_t words_b = L.tiles_n * L.k_tiles * SF::kSfbBytes / 4;
   const int pre_grid = (int)std::min<int64_t>(ceil_div(words_a + words_b, 256), 8 * dev.num_sms);
-  const int64_t n_kc = L.k_tiles * kKSteps;
-  k_sf_chunks<<<pre_grid, 256, 0, stream>>>(a.a_scales, a.M, a.K / 16, n_kc, words_a,
-                                            reinterpret_cast<uint32_t*>(sfa));
-  k_sf_chunks<<<pre_grid, 256, 0, stream>>>(a.b_scales, a.N, a.K / 16, n_kc, words_b,
-                                            reinterpret_cast<uint32_t*>(sfb));
+  k_sf_layout<<<pre_grid, 256, 0, stream>>>(a.a_scales, a.M, a.K / 16, L.k_tiles, 1, words_a,
+                                           reinterpret_cast<uint32_t*>(sfa));
+  k_sf_layout<<<pre_grid, 256, 0, stream>>>(a.b_scales, a.N, a.K / 16, L.k_tiles, 2, words_b,
+                                           reinterpret_cast<uint32_t*>(sfb));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -543,7 +552,7 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const D
 
 cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   const GemmLayout L = gemm_layout(a.M, a.N, a.K);
-  return launch_gemm_t<ChunkSf>(a, L, dev, stream);
+  return launch_gemm_t<SfLayout>(a, L, dev, stream);
 }
 
 }  // namespace nvfp4

@@ -87,9 +87,9 @@ def test_gemm_host_validation_without_gpu(lib_path):
     """nvfp4_gemm's argument checks and workspace size are host-only."""
     import nvfp4_precision_quantization_gb300 as nv
     L = nv.load_library()
-    # scales in the tensor core's chunk layout: 2 KB per 128 lines of A and 4 KB per 256
-    # lines of B, per K tile of 256 (3 and 2 tiles, 32 K tiles)
-    assert nv.nvfp4_gemm_workspace_size(300, 500, 8192) == 3 * 32 * 2048 + 2 * 32 * 4096
+    # scales in the layout of their TMEM copies: 8 KB per 128 lines of A and 16 KB per
+    # 256 lines of B, per K tile of 256 (3 and 2 tiles, 32 K tiles)
+    assert nv.nvfp4_gemm_workspace_size(300, 500, 8192) == 3 * 32 * 8192 + 2 * 32 * 16384
     assert nv.nvfp4_gemm_workspace_size(0, 500, 8192) == 0
     ok = nv._COperand(256, 256, 256, nv.NVFP4_ROW_SCALED, 448.0)
     bad_bound = nv._COperand(256, 256, 256, nv.NVFP4_ROW_SCALED, 500.0)
