@@ -46,10 +46,12 @@
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers on the current CUDA device; the
- *     caller allocates and owns every buffer.  The library allocates nothing,
+ *     caller allocates and owns every buffer.  The library allocates nothing
+ *     (its own device memory, the status word and the static GEMM workspace, is
+ *     reserved when its device code loads),
  *     never synchronizes and never reads device memory on the host, so a call
  *     can be captured in a CUDA graph (after the first call on a device, which
- *     loads the kernels).
+ *     loads the kernels; nothing is claimed here for nvfp4_gemm_static_ws).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) on the current device.
  *   - noop: optional device float; if non-NULL and *noop == 1.0f at run time,
@@ -274,6 +276,22 @@ NVFP4_API nvfp4_status nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k
 NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_operand *a, const nvfp4_operand *b, int64_t m,
                         int64_t n, int64_t k, void *d, int32_t out_dtype, void *workspace,
                         uint64_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm_static_ws -- nvfp4_gemm with its workspace in the library's own static
+ * device memory instead of a caller buffer: NVFP4_GEMM_STATIC_WS_BYTES per device,
+ * reserved when the library's device code is loaded, so the call allocates nothing.
+ * The pages have no counterpart for it (an interface for callers that cannot pass a
+ * workspace); it computes exactly what nvfp4_gemm computes, byte for byte.
+ *   A shape whose nvfp4_gemm_workspace_size exceeds NVFP4_GEMM_STATIC_WS_BYTES returns
+ *   NVFP4_ERR_UNSUPPORTED and enqueues nothing.
+ *   Every call on a device uses the same workspace: calls must not overlap in time
+ *   (issue them on one stream or order them otherwise).
+ */
+#define NVFP4_GEMM_STATIC_WS_BYTES (64ull << 20)
+NVFP4_API nvfp4_status nvfp4_gemm_static_ws(const nvfp4_operand *a, const nvfp4_operand *b,
+                                  int64_t m, int64_t n, int64_t k, void *d,
+                                  int32_t out_dtype, nvfp4_stream_t stream);
 
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 NVFP4_API const char *nvfp4_last_error(void);

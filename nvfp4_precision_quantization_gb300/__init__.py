@@ -26,8 +26,8 @@ __all__ = [
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
-    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "Operand",
-    "alloc_out", "EXPORTED_SYMBOLS",
+    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws", "Operand",
+    "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS",
 ]
 
 NVFP4_OK = 0
@@ -43,13 +43,14 @@ NVFP4_PER_TENSOR = 0
 NVFP4_ROW_SCALED = 1
 NVFP4_DEVICE_TIMEOUT = 1
 NVFP4_DEVICE_BAD_GROUPS = 2
+NVFP4_GEMM_STATIC_WS_BYTES = 64 << 20
 
 EXPORTED_SYMBOLS = (
     "nvfp4_amax", "nvfp4_quantize_rowwise", "nvfp4_quantize_columnwise", "nvfp4_quantize_both",
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
-    "nvfp4_gemm_workspace_size", "nvfp4_gemm",
+    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -122,6 +123,7 @@ def load_library():
         "nvfp4_selftest_convert": [vp, i64, vp, vp, vp],
         "nvfp4_gemm_workspace_size": [i64, i64, i64, C.POINTER(C.c_uint64)],
         "nvfp4_gemm": [vp, vp, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
+        "nvfp4_gemm_static_ws": [vp, vp, i64, i64, i64, vp, i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -319,6 +321,25 @@ def nvfp4_gemm(a: Operand, b: Operand, d: torch.Tensor, workspace: Optional[torc
     ca, cb = a._c(), b._c()
     _check(load_library().nvfp4_gemm(C.byref(ca), C.byref(cb), m, n, k, _ptr(d), od,
                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def nvfp4_gemm_static_ws(a: Operand, b: Operand, d: torch.Tensor, stream=None) -> None:
+    """nvfp4_gemm with the library's static device workspace (no workspace argument)."""
+    if d.dim() != 2 or not d.is_contiguous():
+        raise ValueError("d must be a contiguous 2-D tensor")
+    if d.dtype == torch.bfloat16:
+        od = NVFP4_OUT_BF16
+    elif d.dtype == torch.float32:
+        od = NVFP4_OUT_FP32
+    else:
+        raise TypeError("d must be bfloat16 or float32")
+    m, n = d.shape
+    k = a.codes.shape[1] * 2
+    if a.codes.shape[0] != m or b.codes.shape[0] != n or b.codes.shape[1] * 2 != k:
+        raise ValueError("operand shapes do not match d")
+    ca, cb = a._c(), b._c()
+    _check(load_library().nvfp4_gemm_static_ws(C.byref(ca), C.byref(cb), m, n, k, _ptr(d), od,
+                                                _stream(stream)))
 
 
 def alloc_out(lines: int, n: int, amax_len: int, device="cuda", fill=None) -> Out:

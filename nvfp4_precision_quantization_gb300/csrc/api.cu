@@ -26,6 +26,10 @@ namespace nvfp4 {
 // when they find invalid device-resident input or give up a bounded wait.
 __device__ int g_status_word;
 
+// Workspace of nvfp4_gemm_static_ws: file-scope device memory reserved when the module
+// loads, so that call allocates nothing.
+static __device__ __align__(256) uint8_t g_gemm_static_ws[NVFP4_GEMM_STATIC_WS_BYTES];
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -43,6 +47,7 @@ struct DevCacheEntry {
   bool ready = false;
   int num_sms = 0;
   int* status = nullptr;
+  uint8_t* gemm_static_ws = nullptr;  // device address of g_gemm_static_ws
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -62,13 +67,18 @@ nvfp4_status current_device(DeviceInfo* out) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_status_word);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    void* ws = nullptr;
+    e = cudaGetSymbolAddress(&ws, g_gemm_static_ws);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static GEMM workspace)");
     c.num_sms = sms;
     c.status = static_cast<int*>(p);
+    c.gemm_static_ws = static_cast<uint8_t*>(ws);
     c.ready = true;
   }
   out->device = dev;
   out->num_sms = c.num_sms;
   out->status = c.status;
+  out->gemm_static_ws = c.gemm_static_ws;
   return NVFP4_OK;
 }
 
@@ -409,9 +419,11 @@ nvfp4_status nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint64_t
   return NVFP4_OK;
 }
 
-nvfp4_status nvfp4_gemm(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m, int64_t n,
-                        int64_t k, void* d, int32_t out_dtype, void* workspace,
-                        uint64_t workspace_bytes, nvfp4_stream_t stream) {
+namespace {
+// workspace == NULL: the static workspace of the current device (nvfp4_gemm_static_ws)
+nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m, int64_t n,
+                       int64_t k, void* d, int32_t out_dtype, void* workspace,
+                       uint64_t workspace_bytes, nvfp4_stream_t stream, bool static_ws) {
   nvfp4_status st;
   if ((st = check_sizes(m, n)) != NVFP4_OK) return st;
   if ((st = check_sizes(k, 0)) != NVFP4_OK) return st;
@@ -440,10 +452,17 @@ nvfp4_status nvfp4_gemm(const nvfp4_operand* a, const nvfp4_operand* b, int64_t 
   }
   const GemmLayout L = gemm_layout(m, n, k);
   if (L.tiles_m * L.tiles_n >= (1LL << 31)) return fail(NVFP4_ERR_UNSUPPORTED, "too many tiles");
-  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
-    return fail(NVFP4_ERR_INVALID, "workspace must be non-NULL and 256-byte aligned");
-  if (workspace_bytes < (uint64_t)L.workspace_bytes)
-    return fail(NVFP4_ERR_INVALID, "workspace smaller than nvfp4_gemm_workspace_size");
+  if (static_ws) {
+    if ((uint64_t)L.workspace_bytes > (uint64_t)NVFP4_GEMM_STATIC_WS_BYTES)
+      return fail(NVFP4_ERR_UNSUPPORTED,
+                  "the shape needs " + std::to_string(L.workspace_bytes) +
+                      " bytes of workspace, more than the static workspace holds");
+  } else {
+    if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+      return fail(NVFP4_ERR_INVALID, "workspace must be non-NULL and 256-byte aligned");
+    if (workspace_bytes < (uint64_t)L.workspace_bytes)
+      return fail(NVFP4_ERR_INVALID, "workspace smaller than nvfp4_gemm_workspace_size");
+  }
   DeviceInfo dev;
   if ((st = current_device(&dev)) != NVFP4_OK) return st;
   GemmArgs g{};
@@ -462,10 +481,23 @@ nvfp4_status nvfp4_gemm(const nvfp4_operand* a, const nvfp4_operand* b, int64_t 
   g.K = k;
   g.d = d;
   g.d_bf16 = out_dtype == NVFP4_OUT_BF16;
-  g.workspace = static_cast<uint8_t*>(workspace);
+  g.workspace = static_ws ? dev.gemm_static_ws : static_cast<uint8_t*>(workspace);
   cudaError_t e = launch_gemm(g, dev, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return NVFP4_OK;
+}
+}  // namespace
+
+nvfp4_status nvfp4_gemm(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m, int64_t n,
+                        int64_t k, void* d, int32_t out_dtype, void* workspace,
+                        uint64_t workspace_bytes, nvfp4_stream_t stream) {
+  return gemm_impl(a, b, m, n, k, d, out_dtype, workspace, workspace_bytes, stream, false);
+}
+
+nvfp4_status nvfp4_gemm_static_ws(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m,
+                                  int64_t n, int64_t k, void* d, int32_t out_dtype,
+                                  nvfp4_stream_t stream) {
+  return gemm_impl(a, b, m, n, k, d, out_dtype, nullptr, 0, stream, true);
 }
 
 nvfp4_status nvfp4_grouped_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,

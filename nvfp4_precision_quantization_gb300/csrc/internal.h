@@ -14,6 +14,7 @@ struct DeviceInfo {
   int device;
   int num_sms;
   int* status;  // device address of the library status word
+  uint8_t* gemm_static_ws;  // device address of the static GEMM workspace
 };
 
 // Zero up to four float arrays and copy up to two (dst <- src), unless noop.

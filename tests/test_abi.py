@@ -107,3 +107,13 @@ def test_gemm_host_validation_without_gpu(lib_path):
     assert st == nv.NVFP4_ERR_INVALID and "out_dtype" in nv.nvfp4_last_error()
     st = L.nvfp4_gemm(None, R(ok), 4, 4, 64, 256, nv.NVFP4_OUT_FP32, 256, 1 << 20, None)
     assert st == nv.NVFP4_ERR_INVALID
+
+
+def test_gemm_static_ws_rejects_oversize_without_gpu(lib_path):
+    import nvfp4_precision_quantization_gb300 as nv
+    L = nv.load_library()
+    ok = nv._COperand(256, 256, 256, nv.NVFP4_ROW_SCALED, 448.0)
+    R = ctypes.byref
+    assert nv.nvfp4_gemm_workspace_size(65536, 65536, 65536) > nv.NVFP4_GEMM_STATIC_WS_BYTES
+    st = L.nvfp4_gemm_static_ws(R(ok), R(ok), 65536, 65536, 65536, 256, nv.NVFP4_OUT_BF16, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "static workspace" in nv.nvfp4_last_error()
