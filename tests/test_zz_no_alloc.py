@@ -50,9 +50,15 @@ def test_static_workspace_allocates_nothing():
 
 
 def test_oversize_shape_is_rejected_and_writes_nothing():
-    m, n, k = 16384, 28672, 8192  # needs about 91 MB of workspace
+    m, n, k = 65536, 8192, 16384  # needs 72 MiB of workspace
     assert nv.nvfp4_gemm_workspace_size(m, n, k) > nv.NVFP4_GEMM_STATIC_WS_BYTES
-    a, b = _op(m, k, 52, RS), _op(n, k, 53, PT)
+    # rejected on the host before any device access: the operand bytes are never read
+    a = nv.Operand(torch.empty(m, k // 2, dtype=torch.uint8, device=DEV),
+                   torch.empty(m, k // 16, dtype=torch.uint8, device=DEV),
+                   torch.ones(m, device=DEV), RS, 448.0)
+    b = nv.Operand(torch.empty(n, k // 2, dtype=torch.uint8, device=DEV),
+                   torch.empty(n, k // 16, dtype=torch.uint8, device=DEV),
+                   torch.ones(1, device=DEV), PT, 448.0)
     d = torch.full((m, n), 3.0, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(nv.NVFP4Error) as ei:
         nv.nvfp4_gemm_static_ws(a, b, d)
