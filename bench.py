@@ -613,6 +613,12 @@ def measure_e2e(nv, ops, outs, cfg, stream, dev, steps):
             "overlap": "H2D, quantize and D2H on separate streams"}
 
 
+# DRAM bytes (read + write) of the k_gemm_nvf4 launch of the wgrad call, from the
+# full-size capture in profiles/launches_gemm_fprop16384x28672x8192_wgrad28672x8192x16384.md;
+# to be taken again whenever the GEMM kernel changes.
+GEMM_TRAFFIC_BYTES = 1842.99e6 + 506.35e6
+
+
 def tensor_peak():
     """FP4 dense tensor peak: the measured BF16 burst GEMM rate times the nominal
     FP4 / BF16 ratio (13.5 / 2.25 = 6)."""
@@ -727,10 +733,13 @@ def run_gemm(args):
                        "l2": "a 256 MB L2 flush before each step",
                        "flops_per_step": flops, "peak_tflops": peak, "peak_source": peak_src,
                        "pct_of_tensor_peak": 100.0 * rate / 1e12 / world / peak},
-            "roofline": {"kernel": "nvfp4_gemm, last call of the step (scale pre-pass + k_gemm_nvf4)",
+            "roofline": {"kernel": "k_gemm_nvf4, last call of the step (its event time includes "
+                                   "the call's scale pre-pass)",
                          "bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": None, "algorithmic_flops": calls[-1][4]},
+                         "traffic": None if args.gemm_shape else GEMM_TRAFFIC_BYTES,
+                         "traffic_unit": "DRAM bytes per launch of k_gemm_nvf4",
+                         "algorithmic_flops": calls[-1][4]},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": 3 * len(calls) * K_,
             "clocks": clocks}))
     if world > 1:

@@ -187,34 +187,47 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 //   A (P = 1): word 4u + q (q = l / 32) of row l = line blk * 128 + l, K step 2c + u;
 //   B (P = 2): word cc of row l = line blk * 256 + 32 cc + l % 32, K step c.
 // Stored as one tcgen05.cp .128x256b reads it: 16-byte half u at 2048 u, row l at
-// 16 l.  One thread writes one 32-bit word.
+// 16 l.  One CTA per (block, K tile): it stages the block's 16 scales per line of
+// that K tile in shared memory (16-byte loads where the rows allow), then writes
+// the block's copies as coalesced 16-byte stores, one 16-byte row half per thread.
 __global__ void __launch_bounds__(256) k_sf_layout(const uint8_t* __restrict__ sc, int64_t rows,
                                                   int64_t k16, int64_t k_tiles, int P,
-                                                  int64_t n_words, uint32_t* __restrict__ out) {
+                                                  uint8_t* __restrict__ out) {
+  __shared__ uint4 cs[256];  // [line of the block][16 scales]
+  const int L = 128 * P;
   const int copies = P == 1 ? kKSteps / 2 : kKSteps;
-  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n_words;
-       w += (int64_t)gridDim.x * blockDim.x) {
-    const int inner = (int)(w & 1023);  // word within one 4096-byte copy
-    const int64_t cpy = w >> 10;
-    const int c = (int)(cpy % copies);
-    const int64_t bk = cpy / copies;
-    const int64_t kt = bk % k_tiles, blk = bk / k_tiles;
-    const int u = inner >> 9;
-    const int l = (inner >> 2) & 127;
-    const int wb = inner & 3;
-    uint32_t word = 0;
-    const bool used = P == 1 ? wb == (l >> 5) : true;
-    if (used) {
-      const int64_t line = P == 1 ? blk * 128 + l : blk * 256 + 32 * (4 * u + wb) + (l & 31);
-      const int ks = P == 1 ? 2 * c + u : c;
-      const int64_t s0 = kt * 16 + ks * 4;
-      if (line < rows) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (s0 + j < k16) word |= (uint32_t)sc[line * k16 + s0 + j] << (8 * j);
+  const int64_t kt = blockIdx.x % k_tiles, blk = blockIdx.x / k_tiles;
+  const int64_t s0 = kt * 16;
+  const bool vec = k16 % 16 == 0 && (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
+  for (int i = threadIdx.x; i < L; i += blockDim.x) {
+    const int64_t line = blk * L + i;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (line < rows) {
+      const uint8_t* p = sc + line * k16 + s0;
+      if (vec) {
+        v = __ldg(reinterpret_cast<const uint4*>(p));
+      } else {
+        uint32_t w[4] = {0, 0, 0, 0};
+        for (int j = 0; j < 16 && s0 + j < k16; ++j) w[j >> 2] |= (uint32_t)p[j] << (8 * (j & 3));
+        v = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    out[w] = word;
+    cs[i] = v;
+  }
+  __syncthreads();
+  const uint32_t* cw = reinterpret_cast<const uint32_t*>(cs);  // cw[4 * line + ks]
+  uint4* dst = reinterpret_cast<uint4*>(out + blockIdx.x * (int64_t)copies * 4096);
+  for (int v = threadIdx.x; v < copies * 256; v += blockDim.x) {
+    const int c = v >> 8, u = (v >> 7) & 1, l = v & 127;  // copy, half, row
+    uint32_t w[4];
+    if (P == 1) {  // line l, K step 2c + u, at word l / 32
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = j == (l >> 5) ? cw[4 * l + 2 * c + u] : 0u;
+    } else {  // words 4u .. 4u + 3: lines 32 (4u + j) + l % 32, K step c
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = cw[4 * (32 * (4 * u + j) + (l & 31)) + c];
+    }
+    dst[u * 128 + l + c * 256] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -505,13 +518,10 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const D
   using G = GemmGeom<SF>;
   uint8_t* sfa = a.workspace;
   uint8_t* sfb = a.workspace + L.sfb_offset;
-  const int64_t words_a = L.tiles_m * L.k_tiles * SF::kSfaBytes / 4;
-  const int64_t words_b = L.tiles_n * L.k_tiles * SF::kSfbBytes / 4;
-  const int pre_grid = (int)std::min<int64_t>(ceil_div(words_a + words_b, 256), 8 * dev.num_sms);
-  k_sf_layout<<<pre_grid, 256, 0, stream>>>(a.a_scales, a.M, a.K / 16, L.k_tiles, 1, words_a,
-                                           reinterpret_cast<uint32_t*>(sfa));
-  k_sf_layout<<<pre_grid, 256, 0, stream>>>(a.b_scales, a.N, a.K / 16, L.k_tiles, 2, words_b,
-                                           reinterpret_cast<uint32_t*>(sfb));
+  k_sf_layout<<<(unsigned)(L.tiles_m * L.k_tiles), 256, 0, stream>>>(a.a_scales, a.M, a.K / 16,
+                                                                     L.k_tiles, 1, sfa);
+  k_sf_layout<<<(unsigned)(L.tiles_n * L.k_tiles), 256, 0, stream>>>(a.b_scales, a.N, a.K / 16,
+                                                                     L.k_tiles, 2, sfb);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
