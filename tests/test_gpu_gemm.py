@@ -180,3 +180,31 @@ def test_repeated_calls_agree_and_overwrite():
     nv.nvfp4_gemm(a, b, d2, ws)
     torch.cuda.synchronize()
     assert torch.equal(d1, d2)
+
+
+@pytest.mark.parametrize("shape", [(256, 512, 1024), (129, 300, 544)])
+def test_accumulation_is_exact_on_representable_operands(shape):
+    """Operands whose every partial sum is exactly representable in FP32: code
+    magnitudes in {0, .5, ..., 6} (multiples of 0.5, at most 6) times power-of-two
+    scales 0.5 .. 4, amax = F (value = code * scale): each product is a multiple of
+    2^-4 below 2^10, and any partial sum of at most 1024 of them is below 2^20 -- 24
+    significant bits -- so the tensor core's FP32 accumulation is exact in any order.
+    Then d = fl(fl(acc * alpha) * beta) with acc the exact product, alpha = fl(F *
+    fl(1/F)), beta likewise: the GPU must match that bit for bit."""
+    m, n, k = shape
+    rng = np.random.default_rng(17)
+    F = 448.0 * 6.0
+
+    def op(lines):
+        codes = rng.integers(0, 256, (lines, k // 2), dtype=np.uint8)
+        scales = rng.choice(np.array([0x30, 0x38, 0x40, 0x48], np.uint8), (lines, k // 16))
+        return _host_op(codes, scales, np.full(lines, F, np.float32), RS, 448.0)
+
+    a_h, b_h = op(m), op(n)
+    got = _run(_dev_op(a_h, RS), _dev_op(b_h, RS), m, n, torch.float32)
+    exact = oracle.gemm(a_h, b_h)  # amax / F = 1: the plain sum of code * scale products
+    assert np.all(np.abs(exact) < 2.0 ** 20) and np.all(exact * 16 == np.round(exact * 16))
+    f32 = np.float32
+    alpha = f32(f32(F) * (f32(1.0) / f32(F)))
+    want = (exact.astype(f32) * alpha).astype(f32) * alpha
+    assert np.array_equal(got.astype(f32).view(np.uint32), want.astype(f32).view(np.uint32))
