@@ -208,3 +208,21 @@ def test_accumulation_is_exact_on_representable_operands(shape):
     alpha = f32(f32(F) * (f32(1.0) / f32(F)))
     want = (exact.astype(f32) * alpha).astype(f32) * alpha
     assert np.array_equal(got.astype(f32).view(np.uint32), want.astype(f32).view(np.uint32))
+
+
+def test_fprop_with_16x16_block_weight():
+    """A 16x16-block weight (per-tensor, "Add backward overrides and 1x16 weights to
+    NVFP4 four-over-six", torchao PR #8) is a valid B operand as the quantize entry
+    points write it: its rowwise scales carry each tile's scale on all 16 lines."""
+    rng = np.random.default_rng(12)
+    tokens, d_in, d_out = 200, 256, 272
+    x = (rng.standard_normal((tokens, d_in)) * np.exp(rng.uniform(-2, 2, (tokens, 1)))).astype(np.float32)
+    w = (rng.standard_normal((d_out, d_in)) * 0.05).astype(np.float32)
+    qx = oracle.quantize(x, "fp32", mode=oracle.ROW_SCALED, columnwise=False)
+    qw = oracle.quantize(w, "fp32", mode=oracle.PER_TENSOR, block_2d=True, columnwise=False)
+    sw = qw["row"][1]
+    assert np.array_equal(sw[0::16], sw[15::16])  # the tile's scale on each of its lines
+    a_h = _host_op(*qx["row"], RS, 448.0)
+    b_h = _host_op(*qw["row"], PT, 448.0)
+    y = _run(_dev_op(a_h, RS), _dev_op(b_h, PT), tokens, d_out, torch.bfloat16)
+    _compare(y, a_h, b_h, torch.bfloat16, "fprop 16x16 weight")
