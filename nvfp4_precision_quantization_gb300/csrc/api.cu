@@ -306,6 +306,7 @@ bool make_byte_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pit
 bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pitch,
                       int box_bytes, int box_rows) {
   if (rows <= 0 || pitch <= 0) return false;
+  if (box_bytes != 128 && box_bytes != 64) return false;
   if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || pitch % 16 != 0) return false;
   if (rows >= (1LL << 31) || pitch >= (1LL << 31)) return false;
   EncodeTiledFn fn = encode_tiled();
@@ -316,8 +317,8 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
   const cuuint32_t estride[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

@@ -163,8 +163,8 @@ int pipe_grid_size(int64_t num_tiles, int num_sms);
 // Host helpers (api.cu): encode 2D tiled tensor maps; false if TMA cannot be used.
 bool make_tile_map(CUtensorMap* map, const void* base, InType in, int64_t rows, int64_t cols,
                    int box_cols, int box_rows);
-// K-major code matrix [rows][pitch] read by the GEMM: box of box_bytes (128) x box_rows,
-// 128B swizzle, zero fill outside the matrix
+// K-major code matrix [rows][pitch] read by the GEMM: box of box_bytes (128 or 64) x
+// box_rows, the swizzle of that width (128B / 64B), zero fill outside the matrix
 bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t pitch,
                       int box_bytes, int box_rows);
 // byte matrix [rows][pitch] (an output of codes), box of box_bytes x box_rows

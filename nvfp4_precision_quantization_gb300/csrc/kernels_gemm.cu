@@ -48,9 +48,15 @@ namespace {
 
 constexpr int kBM = 128;                   // tile rows of A = MMA M
 constexpr int kBN = 256;                   // tile rows of B = output columns per tile = MMA N
-constexpr int kBKBytes = 128;              // K bytes per stage and row: 256 E2M1 values
+// K bytes per stage and row: 256 E2M1 values.  (64 -- six stages of 36 KB with the
+// 64B swizzle -- is correct too but measured 17 % slower.)
+constexpr int kBKBytes = 128;
 constexpr int kUmmaKBytes = 32;            // K = 64 values per MMA
-constexpr int kKSteps = kBKBytes / kUmmaKBytes;  // 4
+constexpr int kKSteps = kBKBytes / kUmmaKBytes;  // MMAs per stage
+constexpr int kTileScales = kBKBytes / 8;        // scales per line and K tile
+// the operand tiles' shared-memory swizzle: one 8-row atom of kBKBytes-byte rows
+constexpr int kSwizzleMode = kBKBytes == 128 ? 2 : 4;  // descriptor code: 128B / 64B
+static_assert(kBKBytes == 128 || kBKBytes == 64, "K tile of 128 or 64 bytes per row");
 constexpr int kABytes = kBM * kBKBytes;    // 16 KB
 constexpr int kBBytes = kBN * kBKBytes;    // 32 KB
 constexpr int kEpilogueWarps = 8;                    // two per TMEM lane quarter
@@ -72,8 +78,8 @@ constexpr int kMetaBytes = 1024;                      // barriers, TMEM address,
 // at bytes 4c).  Per K tile of 256: 2 + 4 copies, 8 + 16 KB of shared memory, 16 +
 // 32 TMEM columns (A's K step ks at base + 4ks, B's at base + 8ks).
 struct SfLayout {
-  static constexpr int kStages = 3;
-  static constexpr int kSfaBytes = 2 * 4096;
+  static constexpr int kStages = kBKBytes == 128 ? 3 : 6;
+  static constexpr int kSfaBytes = kKSteps / 2 * 4096;
   static constexpr int kSfbBytes = kKSteps * 4096;
   static constexpr int kSfaCols = 4 * kKSteps, kSfbCols = 8 * kKSteps;
 };
@@ -151,12 +157,13 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major operand tile with 128-byte rows in
-// the 128B swizzle: 8-row groups 1024 bytes apart (stride byte offset), the
-// leading byte offset unused for this layout, bits 46-48 = 0b001, swizzle mode 2.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major operand tile with kBKBytes-byte rows
+// in the matching swizzle: 8-row groups 8 * kBKBytes bytes apart (stride byte
+// offset), the leading byte offset unused for this layout, bits 46-48 = 0b001.
+__device__ __forceinline__ uint64_t desc_swz(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
-         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+         ((uint64_t)(8 * kBKBytes >> 4) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)kSwizzleMode << 61);
 }
 // Descriptor of a no-swizzle K-major scale matrix: 8-row x 16-byte core matrices
 // `sbo` bytes apart along the lines and `lbo` bytes apart along the row.
@@ -193,39 +200,41 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __global__ void __launch_bounds__(256) k_sf_layout(const uint8_t* __restrict__ sc, int64_t rows,
                                                   int64_t k16, int64_t k_tiles, int P,
                                                   uint8_t* __restrict__ out) {
-  __shared__ uint4 cs[256];  // [line of the block][16 scales]
+  __shared__ uint32_t cw[256 * kKSteps];  // cw[kKSteps * line + ks]: the line's K step ks
   const int L = 128 * P;
   const int copies = P == 1 ? kKSteps / 2 : kKSteps;
   const int64_t kt = blockIdx.x % k_tiles, blk = blockIdx.x / k_tiles;
-  const int64_t s0 = kt * 16;
-  const bool vec = k16 % 16 == 0 && (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
+  const int64_t s0 = kt * kTileScales;
+  const bool vec = k16 % kTileScales == 0 && (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
   for (int i = threadIdx.x; i < L; i += blockDim.x) {
     const int64_t line = blk * L + i;
-    uint4 v = make_uint4(0, 0, 0, 0);
+    uint32_t w[kKSteps];
+#pragma unroll
+    for (int j = 0; j < kKSteps; ++j) w[j] = 0;
     if (line < rows) {
       const uint8_t* p = sc + line * k16 + s0;
       if (vec) {
-        v = __ldg(reinterpret_cast<const uint4*>(p));
+#pragma unroll
+        for (int j = 0; j < kKSteps; ++j) w[j] = __ldg(reinterpret_cast<const uint32_t*>(p) + j);
       } else {
-        uint32_t w[4] = {0, 0, 0, 0};
-        for (int j = 0; j < 16 && s0 + j < k16; ++j) w[j >> 2] |= (uint32_t)p[j] << (8 * (j & 3));
-        v = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int j = 0; j < kTileScales && s0 + j < k16; ++j)
+          w[j >> 2] |= (uint32_t)p[j] << (8 * (j & 3));
       }
     }
-    cs[i] = v;
+#pragma unroll
+    for (int j = 0; j < kKSteps; ++j) cw[kKSteps * i + j] = w[j];
   }
   __syncthreads();
-  const uint32_t* cw = reinterpret_cast<const uint32_t*>(cs);  // cw[4 * line + ks]
   uint4* dst = reinterpret_cast<uint4*>(out + blockIdx.x * (int64_t)copies * 4096);
   for (int v = threadIdx.x; v < copies * 256; v += blockDim.x) {
     const int c = v >> 8, u = (v >> 7) & 1, l = v & 127;  // copy, half, row
     uint32_t w[4];
     if (P == 1) {  // line l, K step 2c + u, at word l / 32
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = j == (l >> 5) ? cw[4 * l + 2 * c + u] : 0u;
+      for (int j = 0; j < 4; ++j) w[j] = j == (l >> 5) ? cw[kKSteps * l + 2 * c + u] : 0u;
     } else {  // words 4u .. 4u + 3: lines 32 (4u + j) + l % 32, K step c
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = cw[4 * (32 * (4 * u + j) + (l & 31)) + c];
+      for (int j = 0; j < 4; ++j) w[j] = cw[kKSteps * (32 * (4 * u + j) + (l & 31)) + c];
     }
     dst[u * 128 + l + c * 256] = make_uint4(w[0], w[1], w[2], w[3]);
   }
@@ -250,7 +259,7 @@ struct GemmParams {
   int* status;
 };
 
-constexpr int kRasterGroup = 16;  // M tiles walked together so their A tiles stay in L2
+constexpr int kRasterGroup = 32;  // M tiles walked together so their A tiles stay in L2
 
 __device__ __forceinline__ void tile_coords(int idx, int tiles_m, int tiles_n, int& tm, int& tn) {
   const int group = idx / (kRasterGroup * tiles_n);
@@ -382,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sfb_col = sfa_col + SF::kSfaCols;
 #pragma unroll
         for (int ks = 0; ks < kKSteps; ++ks)
-          tc_mma_nvf4(tmem, desc_sw128(st + ks * kUmmaKBytes),
-                      desc_sw128(st + kABytes + ks * kUmmaKBytes), p.idesc, sfa_col + 4 * ks,
+          tc_mma_nvf4(tmem, desc_swz(st + ks * kUmmaKBytes),
+                      desc_swz(st + kABytes + ks * kUmmaKBytes), p.idesc, sfa_col + 4 * ks,
                       sfb_col + 8 * ks, (kt | ks) != 0);
         tc_commit(&empty[s]);
       }
