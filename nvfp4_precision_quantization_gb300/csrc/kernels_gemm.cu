@@ -16,7 +16,7 @@
 // accumulator never goes to HBM.
 //
 // Structure (persistent: one CTA per SM walks 128 x 256 output tiles, tile c,
-// c + gridDim.x, ..., groups of 16 M tiles side by side so their A tiles stay in L2):
+// c + gridDim.x, ..., groups of 32 M tiles side by side so their A tiles stay in L2):
 //   warp 0    producer: TMA loads of the A and B code tiles (128 B of K per row,
 //             128B swizzle) and 1D bulk copies of their scales, into a 3-stage
 //             shared-memory ring (72 KB a stage) guarded by mbarriers, running on
