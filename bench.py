@@ -223,7 +223,7 @@ def run_ours(args):
         col = nv.alloc_out(c, r, c, dev)
         row.amax_in, col.amax_in = row.amax, col.amax
         outs.append((row, col))
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > 129 MB L2
+    flush = l2_flush_buffer(dev)
 
     def step(ev=None):
         for i, (t, (row, col)) in enumerate(zip(ops, outs)):
@@ -297,7 +297,8 @@ def run_ours(args):
             "config": {
                 "workload": WORKLOAD + (", four-over-six (T in {6, 4} by squared error)"
                                         if fos else ""),
-                "l2": "inputs larger than L2 (268 MB, 940 MB) and a 256 MB L2 flush before each step",
+                "l2": "inputs larger than L2 (268 MB, 940 MB) and " + flush_note(flush),
+                "input_sha256_first_64MiB": input_digest(x, dy),
                 "bytes_io_per_step": bio, "bytes_min_per_step": bmin,
                 "elements_per_step": elems,
                 "gbps_bytes_min": world * bmin * K / t_total / 1e9,
@@ -395,7 +396,7 @@ def supplementary_oracle_sample(w: str, sample_rows: int):
 
 def run_supplementary(args):
     """One JSON line for a row of the path other than the headline workload: same
-    timing rules (warm-up, 256 MB L2 flush before each step, CUDA events on the
+    timing rules (warm-up, an L2 flush of twice the L2 before each step, CUDA events on the
     launching stream, clocks sampled during the timed region)."""
     import torch
 
@@ -511,7 +512,7 @@ def run_supplementary(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = supplementary_oracle_sample(w, args.oracle_rows or 256)
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = l2_flush_buffer(dev)
     for _ in range(args.warmup):
         flush.zero_()
         step([torch.cuda.Event(enable_timing=True)])
@@ -547,7 +548,7 @@ def run_supplementary(args):
             "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
             "pct_of_hbm_peak": 100.0 * rate / 1e9 / world / peak,
             "config": {"workload": SUPPLEMENTARY[w],
-                       "l2": "a 256 MB L2 flush before each step",
+                       "l2": flush_note(flush),
                        "bytes_io_per_step": bio, "bytes_min_per_step": bmin,
                        "gbps_bytes_min": world * bmin * K_ / t_total / 1e9,
                        "pct_of_hbm_peak_bytes_min": 100.0 * bmin * K_ / t_total / 1e9 / peak,
@@ -617,6 +618,31 @@ def measure_e2e(nv, ops, outs, cfg, stream, dev, steps):
 # full-size capture in profiles/launches_gemm_fprop16384x28672x8192_wgrad28672x8192x16384.md;
 # to be taken again whenever the GEMM kernel changes.
 GEMM_TRAFFIC_BYTES = 2120.7e6 + 514.8e6
+
+
+def l2_flush_buffer(dev):
+    """A buffer twice the device's L2 (from its properties), written before each timed
+    step so that no step starts with the previous one's data in L2."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
+    return torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+
+def flush_note(flush) -> str:
+    return f"a {flush.numel() / 2**20:.0f} MiB L2 flush (2x the device's L2) before each step"
+
+
+def input_digest(*tensors, limit: int = 64 << 20) -> str:
+    """SHA-256 of the first `limit` bytes of each synthetic input, concatenated (a
+    fingerprint that the inputs are the seeded ones)."""
+    import hashlib
+
+    import torch
+    h = hashlib.sha256()
+    for t in tensors:
+        b = t.reshape(-1).view(torch.uint8)[:limit]
+        h.update(b.cpu().numpy().tobytes())
+    return h.hexdigest()
 
 
 def tensor_peak():
@@ -692,7 +718,7 @@ def run_gemm(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = gemm_oracle_sample(args.oracle_rows or 64)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = l2_flush_buffer(dev)
     for _ in range(args.warmup):
         flush.zero_()
         step([torch.cuda.Event(enable_timing=True)])
@@ -730,7 +756,7 @@ def run_gemm(args):
             "data": "synthetic",
             "config": {"workload": SUPPLEMENTARY["gemm"] if not args.gemm_shape else
                        "one NVFP4 GEMM %dx%dx%d, both operands row-scaled" % tuple(args.gemm_shape),
-                       "l2": "a 256 MB L2 flush before each step",
+                       "l2": flush_note(flush),
                        "flops_per_step": flops, "peak_tflops": peak, "peak_source": peak_src,
                        "pct_of_tensor_peak": 100.0 * rate / 1e12 / world / peak},
             "roofline": {"kernel": "k_gemm_nvf4, last call of the step (its event time includes "
