@@ -339,6 +339,9 @@ SUPPLEMENTARY = {
     "moe-ragged": "MoE tokens as above, quantized straight from the unpadded tokens into the "
                   "padded layout (padding rows not read): per-group amax, four-over-six, "
                   "bound 256, rowwise",
+    "moe-gemm": "grouped NVFP4 GEMM of the MoE layout: the 32 groups' padded tokens "
+                "(67456 rows incl. padding, K 7168, row-scaled) times 32 expert weights "
+                "(N 2048 each, one amax per expert), BF16 out; FLOPs over the padded rows",
     "gemm": "NVFP4 GEMM consumer of the linear layer: fprop Y[16384x28672] = X[16384x8192] "
             "W[28672x8192]^T (X row-scaled, W per-tensor) and wgrad dW[28672x8192] = "
             "dY^T[28672x16384] X (both row-scaled: bilateral post-scale); random NVFP4 operand "
@@ -654,14 +657,13 @@ def tensor_peak():
     return 6.0 * 1900.0, "of fallback bf16 x 6"
 
 
-def gemm_oracle_sample(lines: int):
-    """The oracle's FP64 GEMM (single thread) on lines x lines outputs of the fprop
-    shape's K, in TFLOP/s of the products it forms."""
+def gemm_oracle_sample(lines: int, k: int):
+    """The oracle's FP64 GEMM (single thread) on lines x lines outputs of depth k, in
+    TFLOP/s of the products it forms."""
     import numpy as np
 
     import oracle
     import workloads
-    k = workloads.GEMM_SHAPES["fprop"][2]
     ops = []
     for seed, rs in ((21, True), (22, False)):
         c, sc, a = workloads.nvfp4_operand(lines, k, seed, row_scaled=rs)
@@ -672,7 +674,7 @@ def gemm_oracle_sample(lines: int):
     dt = time.perf_counter() - t0
     return {"value": 2.0 * lines * lines * k / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
             "kind": "oracle", "seconds": dt,
-            "sample": f"{lines} x {lines} outputs of the fprop GEMM (k = {k}), FP64"}
+            "sample": f"{lines} x {lines} outputs of depth k = {k}, FP64"}
 
 
 def run_gemm(args):
@@ -695,9 +697,23 @@ def run_gemm(args):
     stream = torch.cuda.current_stream()
     nv.load_library()
     calls, flops = [], 0
+    grouped = args.workload == "moe-gemm"
     jobs = [("fprop", False), ("wgrad", True)]
     if args.gemm_shape:  # one GEMM of the given shape, both operands row-scaled
         jobs = [(tuple(args.gemm_shape), True)]
+    if grouped:  # the padded MoE tokens times 32 experts, one amax per expert
+        _, _, pad_ends = workloads.moe_layout()
+        groups, m, n, k = len(pad_ends), int(pad_ends[-1]), 2048, 7168
+        ca, sa, aa = workloads.nvfp4_operand(m, k, 41, row_scaled=True, device=dev)
+        cb, sb, ab = workloads.nvfp4_operand(groups * n, k, 42, row_scaled=True, device=dev)
+        a = nv.Operand(ca, sa, aa, nv.NVFP4_ROW_SCALED, 448.0)
+        b = nv.Operand(cb, sb, ab[:groups].contiguous(), nv.NVFP4_PER_TENSOR, 448.0)
+        d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(nv.nvfp4_grouped_gemm_workspace_size(m, n, k, groups), dtype=torch.uint8,
+                         device=dev)
+        calls.append((a, b, d, ws, 2.0 * m * n * k, pad_ends.to(dev)))
+        flops += 2.0 * m * n * k
+        jobs = []
     for i, (name, b_rs) in enumerate(jobs):
         m, n, k = name if isinstance(name, tuple) else workloads.GEMM_SHAPES[name]
         ca, sa, aa = workloads.nvfp4_operand(m, k, 31 + 2 * i, row_scaled=True, device=dev)
@@ -706,18 +722,22 @@ def run_gemm(args):
         b = nv.Operand(cb, sb, ab, nv.NVFP4_ROW_SCALED if b_rs else nv.NVFP4_PER_TENSOR, 448.0)
         d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(nv.nvfp4_gemm_workspace_size(m, n, k), dtype=torch.uint8, device=dev)
-        calls.append((a, b, d, ws, 2.0 * m * n * k))
+        calls.append((a, b, d, ws, 2.0 * m * n * k, None))
         flops += 2.0 * m * n * k
 
     def step(ev):
-        for j, (a, b, d, ws, _) in enumerate(calls):
+        for j, (a, b, d, ws, _, ends) in enumerate(calls):
             if j == len(calls) - 1:
                 ev[0].record(stream)
-            nv.nvfp4_gemm(a, b, d, ws, stream=stream)
+            if ends is not None:
+                nv.nvfp4_grouped_gemm(a, b, ends, d, ws, stream=stream)
+            else:
+                nv.nvfp4_gemm(a, b, d, ws, stream=stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = gemm_oracle_sample(args.oracle_rows or 64)
+        cpu = gemm_oracle_sample(args.oracle_rows or 64, 7168 if grouped else
+                                 workloads.GEMM_SHAPES["fprop"][2])
     flush = l2_flush_buffer(dev)
     for _ in range(args.warmup):
         flush.zero_()
@@ -748,13 +768,14 @@ def run_gemm(args):
     achieved = calls[-1][4] / (kern_ms / 1e3) / 1e12
     if rank == 0:
         print(json.dumps({
-            "metric": "NVFP4 GEMM consumer TFLOP/s" + ("" if args.gemm_shape else
-                                                      " (fprop + wgrad of the linear layer)"),
+            "metric": "NVFP4 GEMM consumer TFLOP/s" + (
+                " (grouped, MoE experts)" if grouped else
+                "" if args.gemm_shape else " (fprop + wgrad of the linear layer)"),
             "value": rate / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K_,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K_, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32 acc, bf16 out",
             "data": "synthetic",
-            "config": {"workload": SUPPLEMENTARY["gemm"] if not args.gemm_shape else
+            "config": {"workload": SUPPLEMENTARY[args.workload] if not args.gemm_shape else
                        "one NVFP4 GEMM %dx%dx%d, both operands row-scaled" % tuple(args.gemm_shape),
                        "l2": flush_note(flush),
                        "flops_per_step": flops, "peak_tflops": peak, "peak_source": peak_src,
@@ -763,7 +784,7 @@ def run_gemm(args):
                                    "the call's scale pre-pass)",
                          "bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": None if args.gemm_shape else GEMM_TRAFFIC_BYTES,
+                         "traffic": None if (args.gemm_shape or grouped) else GEMM_TRAFFIC_BYTES,
                          "traffic_unit": "DRAM bytes per launch of k_gemm_nvf4",
                          "algorithmic_flops": calls[-1][4]},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": 3 * len(calls) * K_,
@@ -796,7 +817,7 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload == "gemm":
+    elif args.workload in ("gemm", "moe-gemm"):
         run_gemm(args)
     elif args.workload in SUPPLEMENTARY:
         run_supplementary(args)

@@ -278,6 +278,33 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_operand *a, const nvfp4_operand *b
                         uint64_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_grouped_gemm -- the per-expert GEMM of "Add NVFP4 four-over-six grouped GEMM
+ * for MoE training" (torchao PR #9, description: token groups A (rows, k) times
+ * expert weights B (groups, n, k) with group-end offsets), with the same bilateral
+ * post-scale as nvfp4_gemm: for group g with rows [s_g, e_g) of a,
+ *   d[i][j] = sum_c value_a(i, c) * value_b(g * n + j, c),  s_g <= i < e_g,
+ * i.e. nvfp4_gemm of a's rows of the group with b's rows [g*n, (g+1)*n).
+ *   a: rows lines (the padded MoE tokens, as the grouped quantize entry points write
+ *      them), amax [rows] (NVFP4_ROW_SCALED: per row, e.g. the group amax expanded
+ *      to its rows) or [1];
+ *   b: num_groups * n lines, amax [num_groups * n] (NVFP4_ROW_SCALED) or
+ *      [num_groups] (NVFP4_PER_TENSOR: one amax per expert);
+ *   group_ends: device int64 [num_groups], cumulative, non-decreasing, every end a
+ *      multiple of 128, last == rows (empty groups allowed); num_groups <= 4096;
+ *   n: a multiple of 256 (NVFP4_ERR_UNSUPPORTED otherwise); d [rows][n].
+ *   Invalid or unaligned ends set NVFP4_DEVICE_BAD_GROUPS and write nothing.
+ *   workspace: at least nvfp4_grouped_gemm_workspace_size(rows, n, k, num_groups)
+ *   bytes, as for nvfp4_gemm.
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_gemm_workspace_size(int64_t rows, int64_t n, int64_t k,
+                                               int32_t num_groups, uint64_t *bytes);
+NVFP4_API nvfp4_status nvfp4_grouped_gemm(const nvfp4_operand *a, const nvfp4_operand *b,
+                                const int64_t *group_ends, int32_t num_groups, int64_t rows,
+                                int64_t n, int64_t k, void *d, int32_t out_dtype,
+                                void *workspace, uint64_t workspace_bytes,
+                                nvfp4_stream_t stream);
+
+/*
  * nvfp4_gemm_static_ws -- nvfp4_gemm with its workspace in the library's own static
  * device memory instead of a caller buffer: NVFP4_GEMM_STATIC_WS_BYTES per device,
  * reserved when the library's device code is loaded, so the call allocates nothing.

@@ -27,6 +27,7 @@ __all__ = [
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws", "Operand",
+    "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm",
     "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS",
 ]
 
@@ -51,6 +52,7 @@ EXPORTED_SYMBOLS = (
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws",
+    "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -124,6 +126,8 @@ def load_library():
         "nvfp4_gemm_workspace_size": [i64, i64, i64, C.POINTER(C.c_uint64)],
         "nvfp4_gemm": [vp, vp, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
         "nvfp4_gemm_static_ws": [vp, vp, i64, i64, i64, vp, i32, vp],
+        "nvfp4_grouped_gemm_workspace_size": [i64, i64, i64, i32, C.POINTER(C.c_uint64)],
+        "nvfp4_grouped_gemm": [vp, vp, vp, i32, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -321,6 +325,38 @@ def nvfp4_gemm(a: Operand, b: Operand, d: torch.Tensor, workspace: Optional[torc
     ca, cb = a._c(), b._c()
     _check(load_library().nvfp4_gemm(C.byref(ca), C.byref(cb), m, n, k, _ptr(d), od,
                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def nvfp4_grouped_gemm_workspace_size(rows: int, n: int, k: int, num_groups: int) -> int:
+    v = C.c_uint64(0)
+    _check(load_library().nvfp4_grouped_gemm_workspace_size(rows, n, k, num_groups, C.byref(v)))
+    return v.value
+
+
+def nvfp4_grouped_gemm(a: Operand, b: Operand, group_ends: torch.Tensor, d: torch.Tensor,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """d [rows][n] = per group g: dequant(a rows of g) x dequant(b rows [g*n, (g+1)*n))^T.
+    group_ends: device int64 [groups]; b.codes has groups * n rows."""
+    if d.dim() != 2 or not d.is_contiguous():
+        raise ValueError("d must be a contiguous 2-D tensor")
+    if d.dtype == torch.bfloat16:
+        od = NVFP4_OUT_BF16
+    elif d.dtype == torch.float32:
+        od = NVFP4_OUT_FP32
+    else:
+        raise TypeError("d must be bfloat16 or float32")
+    rows, n = d.shape
+    groups = int(group_ends.numel())
+    k = a.codes.shape[1] * 2
+    if a.codes.shape[0] != rows or b.codes.shape[0] != groups * n or b.codes.shape[1] * 2 != k:
+        raise ValueError("operand shapes do not match d and the group count")
+    need = nvfp4_grouped_gemm_workspace_size(rows, n, k, groups)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=d.device)
+    ca, cb = a._c(), b._c()
+    _check(load_library().nvfp4_grouped_gemm(C.byref(ca), C.byref(cb), _ptr(group_ends), groups,
+                                              rows, n, k, _ptr(d), od, _ptr(workspace),
+                                              workspace.numel(), _stream(stream)))
 
 
 def nvfp4_gemm_static_ws(a: Operand, b: Operand, d: torch.Tensor, stream=None) -> None:

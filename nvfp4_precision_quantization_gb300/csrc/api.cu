@@ -416,15 +416,17 @@ nvfp4_status nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint64_t
   nvfp4_status st;
   if ((st = check_sizes(m, n)) != NVFP4_OK) return st;
   if ((st = check_sizes(k, 0)) != NVFP4_OK) return st;
-  *bytes = (m == 0 || n == 0 || k == 0) ? 0 : (uint64_t)gemm_layout(m, n, k).workspace_bytes;
+  *bytes = (m == 0 || n == 0 || k == 0) ? 0 : (uint64_t)gemm_layout(m, n, k, n).workspace_bytes;
   return NVFP4_OK;
 }
 
 namespace {
 // workspace == NULL: the static workspace of the current device (nvfp4_gemm_static_ws)
-nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m, int64_t n,
-                       int64_t k, void* d, int32_t out_dtype, void* workspace,
-                       uint64_t workspace_bytes, nvfp4_stream_t stream, bool static_ws) {
+// group_ends != NULL: the grouped GEMM (num_groups groups of A's rows, B = [groups*n][k])
+nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, const int64_t* group_ends,
+                       int32_t num_groups, int64_t m, int64_t n, int64_t k, void* d,
+                       int32_t out_dtype, void* workspace, uint64_t workspace_bytes,
+                       nvfp4_stream_t stream, bool static_ws) {
   nvfp4_status st;
   if ((st = check_sizes(m, n)) != NVFP4_OK) return st;
   if ((st = check_sizes(k, 0)) != NVFP4_OK) return st;
@@ -451,7 +453,9 @@ nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m
     if (reinterpret_cast<uintptr_t>(o->codes) % 16 != 0)
       return fail(NVFP4_ERR_UNSUPPORTED, "operand codes must be 16-byte aligned");
   }
-  const GemmLayout L = gemm_layout(m, n, k);
+  if (group_ends != nullptr && n % 256 != 0)
+    return fail(NVFP4_ERR_UNSUPPORTED, "grouped GEMM: n must be a multiple of 256");
+  const GemmLayout L = gemm_layout(m, n, k, group_ends ? (int64_t)num_groups * n : n);
   if (L.tiles_m * L.tiles_n >= (1LL << 31)) return fail(NVFP4_ERR_UNSUPPORTED, "too many tiles");
   if (static_ws) {
     if ((uint64_t)L.workspace_bytes > (uint64_t)NVFP4_GEMM_STATIC_WS_BYTES)
@@ -483,6 +487,8 @@ nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m
   g.d = d;
   g.d_bf16 = out_dtype == NVFP4_OUT_BF16;
   g.workspace = static_ws ? dev.gemm_static_ws : static_cast<uint8_t*>(workspace);
+  g.group_ends = group_ends;
+  g.num_groups = num_groups;
   cudaError_t e = launch_gemm(g, dev, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return NVFP4_OK;
@@ -492,13 +498,39 @@ nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m
 nvfp4_status nvfp4_gemm(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m, int64_t n,
                         int64_t k, void* d, int32_t out_dtype, void* workspace,
                         uint64_t workspace_bytes, nvfp4_stream_t stream) {
-  return gemm_impl(a, b, m, n, k, d, out_dtype, workspace, workspace_bytes, stream, false);
+  return gemm_impl(a, b, nullptr, 0, m, n, k, d, out_dtype, workspace, workspace_bytes, stream,
+                   false);
+}
+
+nvfp4_status nvfp4_grouped_gemm_workspace_size(int64_t rows, int64_t n, int64_t k,
+                                               int32_t num_groups, uint64_t* bytes) {
+  if (bytes == nullptr) return fail(NVFP4_ERR_INVALID, "bytes is NULL");
+  nvfp4_status st;
+  if ((st = check_sizes(rows, n)) != NVFP4_OK) return st;
+  if ((st = check_sizes(k, 0)) != NVFP4_OK) return st;
+  if (num_groups < 1 || num_groups > 4096)
+    return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
+  *bytes = (rows == 0 || n == 0 || k == 0)
+               ? 0
+               : (uint64_t)gemm_layout(rows, n, k, (int64_t)num_groups * n).workspace_bytes;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_grouped_gemm(const nvfp4_operand* a, const nvfp4_operand* b,
+                                const int64_t* group_ends, int32_t num_groups, int64_t rows,
+                                int64_t n, int64_t k, void* d, int32_t out_dtype, void* workspace,
+                                uint64_t workspace_bytes, nvfp4_stream_t stream) {
+  if (group_ends == nullptr) return fail(NVFP4_ERR_INVALID, "group_ends is NULL");
+  if (num_groups < 1 || num_groups > 4096)
+    return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
+  return gemm_impl(a, b, group_ends, num_groups, rows, n, k, d, out_dtype, workspace,
+                   workspace_bytes, stream, false);
 }
 
 nvfp4_status nvfp4_gemm_static_ws(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m,
                                   int64_t n, int64_t k, void* d, int32_t out_dtype,
                                   nvfp4_stream_t stream) {
-  return gemm_impl(a, b, m, n, k, d, out_dtype, nullptr, 0, stream, true);
+  return gemm_impl(a, b, nullptr, 0, m, n, k, d, out_dtype, nullptr, 0, stream, true);
 }
 
 nvfp4_status nvfp4_grouped_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,

@@ -148,13 +148,19 @@ struct GemmArgs {
   int64_t M, N, K;  // M, N >= 1; K >= 32 and a multiple of 32
   void* d;
   bool d_bf16;
-  uint8_t* workspace;  // >= gemm_layout(M, N, K).workspace_bytes, 256-byte aligned
+  uint8_t* workspace;  // >= gemm_layout(M, N, K, b_lines).workspace_bytes, 256-byte aligned
+  // grouped GEMM (NULL otherwise): A's rows in num_groups groups ending at group_ends
+  // (device, multiples of 128); group g multiplies B's rows [g*N, (g+1)*N), N a
+  // multiple of 256; b_amax [num_groups*N] (row-scaled) or [num_groups]
+  const int64_t* group_ends;
+  int num_groups;
 };
 struct GemmLayout {
   int64_t k_tiles, tiles_m, tiles_n;
   int64_t sfa_bytes, sfb_bytes, sfb_offset, workspace_bytes;
 };
-GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K);
+// b_lines: rows of B (N, or num_groups * N for the grouped GEMM)
+GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int64_t b_lines);
 cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // Grid size shared by the TMA amax and encode kernels (same tile -> CTA mapping).

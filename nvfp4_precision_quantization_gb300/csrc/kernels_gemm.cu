@@ -257,7 +257,26 @@ struct GemmParams {
   bool d_bf16;
   uint32_t idesc;
   int* status;
+  // grouped (per-expert) GEMM: rows of A in groups ending at group_ends (multiples of
+  // 128), group g multiplying rows g * b_group_rows .. of B; NULL for one GEMM
+  const int64_t* group_ends;
+  int num_groups;
+  int b_group_rows;         // N in the grouped GEMM, 0 otherwise
+  int b_amax_group_stride;  // where group g's amax starts in b_amax (N, 1 or 0)
 };
+
+// The group of the A tile starting at row r: the first g with group_ends[g] > r
+// (empty groups are skipped); 0 when the GEMM is not grouped.
+__device__ __forceinline__ int group_of_row(const GemmParams& p, int64_t r) {
+  if (p.group_ends == nullptr) return 0;
+  int lo = 0, hi = p.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.group_ends[mid] > r) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
 
 constexpr int kRasterGroup = 32;  // M tiles walked together so their A tiles stay in L2
 
@@ -292,6 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.tiles_m * p.tiles_n;
 
+  if (p.group_ends != nullptr) {  // every thread takes part; nothing is written if invalid
+    const bool ok = groups_valid(p.group_ends, p.num_groups, p.M) &&
+                    ends_aligned(p.group_ends, p.num_groups, kBM);
+    if (!ok) {
+      if (threadIdx.x == 0) raise_status(p.status, kStatusBadGroups);
+      return;
+    }
+  }
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -322,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       int tm, tn;
       tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+      const int b_tile0 = group_of_row(p, (int64_t)tm * kBM) * (p.b_group_rows / kBN);
       for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
         const uint32_t s = it % S;
         if (it >= (uint32_t)S && !mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1)) {
@@ -336,11 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + s * G::kStageBytes;
         uint8_t* st_sf = st + kABytes + kBBytes;
         mbar_expect_tx(&full[s], G::kStageBytes);
+        const int bt = b_tile0 + tn;  // B's 256-row tile (of its group)
         tma_load_2d(st, &map_a, &full[s], kt * kBKBytes, tm * kBM, pol_a);
-        tma_load_2d(st + kABytes, &map_b, &full[s], kt * kBKBytes, tn * kBN, pol_b);
+        tma_load_2d(st + kABytes, &map_b, &full[s], kt * kBKBytes, bt * kBN, pol_b);
         bulk_load(st_sf, p.sfa + ((int64_t)tm * p.k_tiles + kt) * SF::kSfaBytes, SF::kSfaBytes,
                   &full[s], pol_a);
-        bulk_load(st_sf + SF::kSfaBytes, p.sfb + ((int64_t)tn * p.k_tiles + kt) * SF::kSfbBytes,
+        bulk_load(st_sf + SF::kSfaBytes, p.sfb + ((int64_t)bt * p.k_tiles + kt) * SF::kSfbBytes,
                   SF::kSfbBytes, &full[s], pol_b);
       }
     }
@@ -427,6 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int col_base = tn * kBN + half * kEpiCols;
       if (row >= p.M || col_base >= p.N) continue;
       const float alpha = __fmul_rn(p.a_amax[(int64_t)row * p.a_amax_stride], p.a_finv);
+      const float* b_amax =
+          p.b_amax + (int64_t)group_of_row(p, (int64_t)tm * kBM) * p.b_amax_group_stride;
       const int nvalid = min(kEpiCols, p.N - col_base);
       const int64_t off = (int64_t)row * p.N + col_base;
       const bool vec = nvalid == kEpiCols &&
@@ -440,12 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j4 = 0; j4 < 8; ++j4) {
           float b4[4];
           if (b_vec && col0 + 32 <= p.N) {
-            const float4 t4 = __ldg(reinterpret_cast<const float4*>(p.b_amax + col0) + j4);
+            const float4 t4 = __ldg(reinterpret_cast<const float4*>(b_amax + col0) + j4);
             b4[0] = t4.x, b4[1] = t4.y, b4[2] = t4.z, b4[3] = t4.w;
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              b4[j] = __ldg(p.b_amax + (int64_t)min(col0 + 4 * j4 + j, p.N - 1) * p.b_amax_stride);
+              b4[j] = __ldg(b_amax + (int64_t)min(col0 + 4 * j4 + j, p.N - 1) * p.b_amax_stride);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -509,13 +541,13 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K) {
+GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int64_t b_lines) {
   GemmLayout L;
   L.k_tiles = ceil_div(K, 2 * kBKBytes);
   L.tiles_m = ceil_div(M, kBM);
   L.tiles_n = ceil_div(N, kBN);
   L.sfa_bytes = L.tiles_m * L.k_tiles * SfLayout::kSfaBytes;
-  L.sfb_bytes = L.tiles_n * L.k_tiles * SfLayout::kSfbBytes;
+  L.sfb_bytes = ceil_div(b_lines, kBN) * L.k_tiles * SfLayout::kSfbBytes;
   L.sfb_offset = (L.sfa_bytes + 255) / 256 * 256;
   L.workspace_bytes = L.sfb_offset + L.sfb_bytes;
   return L;
@@ -529,14 +561,15 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const D
   uint8_t* sfb = a.workspace + L.sfb_offset;
   k_sf_layout<<<(unsigned)(L.tiles_m * L.k_tiles), 256, 0, stream>>>(a.a_scales, a.M, a.K / 16,
                                                                      L.k_tiles, 1, sfa);
-  k_sf_layout<<<(unsigned)(L.tiles_n * L.k_tiles), 256, 0, stream>>>(a.b_scales, a.N, a.K / 16,
-                                                                     L.k_tiles, 2, sfb);
+  const int64_t b_lines = a.group_ends ? (int64_t)a.num_groups * a.N : a.N;
+  k_sf_layout<<<(unsigned)(ceil_div(b_lines, kBN) * L.k_tiles), 256, 0, stream>>>(
+      a.b_scales, b_lines, a.K / 16, L.k_tiles, 2, sfb);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   CUtensorMap map_a, map_b;
   if (!make_operand_map(&map_a, a.a_codes, a.M, a.K / 2, kBKBytes, kBM) ||
-      !make_operand_map(&map_b, a.b_codes, a.N, a.K / 2, kBKBytes, kBN))
+      !make_operand_map(&map_b, a.b_codes, b_lines, a.K / 2, kBKBytes, kBN))
     return cudaErrorInvalidValue;
 
   static bool attr_set[64] = {};
@@ -564,13 +597,18 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const D
   p.d_bf16 = a.d_bf16;
   p.idesc = make_idesc_nvf4(kBM, kBN);
   p.status = dev.status;
+  p.group_ends = a.group_ends;
+  p.num_groups = a.group_ends ? a.num_groups : 0;
+  p.b_group_rows = a.group_ends ? (int)a.N : 0;
+  p.b_amax_group_stride = a.group_ends ? (a.b_row_scaled ? (int)a.N : 1) : 0;
   const int grid = (int)std::min<int64_t>(L.tiles_m * L.tiles_n, dev.num_sms);
   k_gemm_nvf4<SF><<<grid, kThreads, G::kSmemBytes, stream>>>(map_a, map_b, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  const GemmLayout L = gemm_layout(a.M, a.N, a.K);
+  const GemmLayout L =
+      gemm_layout(a.M, a.N, a.K, a.group_ends ? (int64_t)a.num_groups * a.N : a.N);
   return launch_gemm_t<SfLayout>(a, L, dev, stream);
 }
 

@@ -266,3 +266,30 @@ def gemm(a, b, *, with_abs: bool = False):
                       _f32(b["amax"]).reshape(-1), int(b["row_scaled"]), float(b["bound"]),
                       m, n, k, d, _ptr(da))
     return (d, da) if with_abs else d
+
+
+def grouped_gemm(a, b, group_ends, n: int, *, with_abs: bool = False):
+    """The per-expert GEMM of grouped tokens ("Add NVFP4 four-over-six grouped GEMM for
+    MoE training", torchao PR #9, description): group g's rows of a, [e_{g-1}, e_g),
+    times b's rows [g*n, (g+1)*n)^T, each block computed by gemm() above (no new
+    arithmetic: only the slicing of the operands and of their amax).  b["amax"] holds
+    [groups*n] per-line values (row_scaled) or [groups] per-expert values."""
+    ends = np.asarray(group_ends, np.int64)
+    rows = a["codes"].shape[0]
+    d = np.zeros((rows, n), np.float64)
+    da = np.zeros((rows, n), np.float64) if with_abs else None
+    start = 0
+    for g, e in enumerate(ends.tolist()):
+        if e > start:
+            ag = dict(a, codes=a["codes"][start:e], scales=a["scales"][start:e],
+                      amax=a["amax"][start:e] if a["row_scaled"] else a["amax"])
+            bam = b["amax"][g * n:(g + 1) * n] if b["row_scaled"] else b["amax"][g:g + 1]
+            bg = dict(b, codes=b["codes"][g * n:(g + 1) * n], scales=b["scales"][g * n:(g + 1) * n],
+                      amax=bam)
+            r = gemm(ag, bg, with_abs=with_abs)
+            if with_abs:
+                d[start:e], da[start:e] = r
+            else:
+                d[start:e] = r
+        start = e
+    return (d, da) if with_abs else d

@@ -121,3 +121,29 @@ def test_matches_product_of_dequantized_operands(row_scaled):
                            cols=128, bound=256.0).astype(np.float64)
     assert np.all(np.abs(da @ db.T - d) <= 2.0 ** -21 * dabs)
     assert np.all(dabs >= np.abs(d))
+
+
+def test_grouped_gemm_is_the_per_group_product():
+    """oracle.grouped_gemm against facts independent of its slicing: each group's rows
+    equal the dense GEMM with its own expert (an empty group in between takes no
+    rows and no expert rows); an expert's per-tensor amax scales exactly its group's
+    rows; a single group is the dense GEMM."""
+    k, n = 64, 8
+    a = _random_operand(384, k, seed=21, row_scaled=True)
+    experts = [_random_operand(n, k, seed=30 + g, row_scaled=False) for g in range(3)]
+    b = _op(np.concatenate([e["codes"] for e in experts]),
+            np.concatenate([e["scales"] for e in experts]),
+            np.array([e["amax"][0] for e in experts], np.float32), False)
+    ends = [128, 128, 384]  # group 1 empty
+    d = oracle.grouped_gemm(a, b, ends, n)
+    rows0 = dict(a, codes=a["codes"][:128], scales=a["scales"][:128], amax=a["amax"][:128])
+    assert np.array_equal(d[:128], oracle.gemm(rows0, experts[0]))
+    rows2 = dict(a, codes=a["codes"][128:], scales=a["scales"][128:], amax=a["amax"][128:])
+    assert np.array_equal(d[128:], oracle.gemm(rows2, experts[2]))
+    # doubling expert 2's amax doubles exactly rows 128..383
+    b2 = dict(b, amax=b["amax"].copy())
+    b2["amax"][2] *= 2.0
+    d2 = oracle.grouped_gemm(a, b2, ends, n)
+    assert np.array_equal(d2[128:], 2.0 * d[128:]) and np.array_equal(d2[:128], d[:128])
+    # a single group is the dense GEMM with expert 0
+    assert np.array_equal(oracle.grouped_gemm(a, b, [384], n), oracle.gemm(a, experts[0]))

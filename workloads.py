@@ -16,6 +16,9 @@ operands they describe):
               each group zero-padded to a multiple of 128 rows, K = 7168, N(0,1).
   edge        4000 x 5000 N(0,1) in BF16 and FP32, 8192 x 8192 N(0, 0.02),
               4096 x 4096 with every 8th row zero, an all-zero tensor (seed 4).
+  moe-gemm    the grouped GEMM of the MoE layout above: the padded tokens' NVFP4 bytes
+              (K 7168) times 32 experts' weights (N 2048), drawn like `gemm` below,
+              one per-tensor amax per expert (seed 5 and up).
   gemm        NVFP4 operand bytes for the GEMM consumer, drawn directly: code bytes
               uniform over all 256 values (every pair of E2M1 codes, both signs),
               scale bytes uniform over the normal positive E4M3 codes 0x08..0x7E,
@@ -81,6 +84,14 @@ def moe_counts(num_groups: int = 32, tokens: int = 65536, device="cpu") -> torch
     g = generator(SEEDS["moe"], "cpu")
     draws = torch.randint(0, num_groups, (tokens,), generator=g)
     return torch.bincount(draws, minlength=num_groups).to(torch.int64)
+
+
+def moe_layout(num_groups: int = 32, tokens: int = 65536, align: int = 128):
+    """The MoE token counts, their padded counts and the padded group ends (CPU int64),
+    without generating any tokens."""
+    counts = moe_counts(num_groups, tokens)
+    padded = ((counts + align - 1) // align) * align
+    return counts, padded, torch.cumsum(padded, 0)
 
 
 def moe(device="cpu", num_groups: int = 32, tokens: int = 65536, cols: int = 7168,
