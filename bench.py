@@ -339,9 +339,12 @@ SUPPLEMENTARY = {
     "moe-ragged": "MoE tokens as above, quantized straight from the unpadded tokens into the "
                   "padded layout (padding rows not read): per-group amax, four-over-six, "
                   "bound 256, rowwise",
-    "moe-gemm": "grouped NVFP4 GEMM of the MoE layout: the 32 groups' padded tokens "
-                "(67456 rows incl. padding, K 7168, row-scaled) times 32 expert weights "
-                "(N 2048 each, one amax per expert), BF16 out; FLOPs over the padded rows",
+    "moe-gemm": "grouped NVFP4 GEMMs of the MoE layout (32 groups of Multinomial(65536) "
+                "tokens, each padded to a multiple of 256 rows): per-expert fprop (tokens x "
+                "K 7168, row-scaled, times 32 expert weights of N 2048, one amax per expert) "
+                "and per-expert wgrad (dY^T [2048 x tokens] times X^T [7168 x tokens], "
+                "columnwise, per-group column amax, K = each group's tokens); BF16 out; "
+                "FLOPs over the padded rows",
     "gemm": "NVFP4 GEMM consumer of the linear layer: fprop Y[16384x28672] = X[16384x8192] "
             "W[28672x8192]^T (X row-scaled, W per-tensor) and wgrad dW[28672x8192] = "
             "dY^T[28672x16384] X (both row-scaled: bilateral post-scale); random NVFP4 operand "
@@ -701,9 +704,11 @@ def run_gemm(args):
     jobs = [("fprop", False), ("wgrad", True)]
     if args.gemm_shape:  # one GEMM of the given shape, both operands row-scaled
         jobs = [(tuple(args.gemm_shape), True)]
-    if grouped:  # the padded MoE tokens times 32 experts, one amax per expert
-        _, _, pad_ends = workloads.moe_layout()
+    if grouped:  # the MoE tokens (padded to 256 per group) and 32 experts
+        _, _, pad_ends = workloads.moe_layout(align=256)
         groups, m, n, k = len(pad_ends), int(pad_ends[-1]), 2048, 7168
+        ends = pad_ends.to(dev)
+        # fprop: tokens [m][k] row-scaled x expert weights [groups*n][k], one amax per expert
         ca, sa, aa = workloads.nvfp4_operand(m, k, 41, row_scaled=True, device=dev)
         cb, sb, ab = workloads.nvfp4_operand(groups * n, k, 42, row_scaled=True, device=dev)
         a = nv.Operand(ca, sa, aa, nv.NVFP4_ROW_SCALED, 448.0)
@@ -711,8 +716,20 @@ def run_gemm(args):
         d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(nv.nvfp4_grouped_gemm_workspace_size(m, n, k, groups), dtype=torch.uint8,
                          device=dev)
-        calls.append((a, b, d, ws, 2.0 * m * n * k, pad_ends.to(dev)))
-        flops += 2.0 * m * n * k
+        calls.append((a, b, d, ws, 2.0 * m * n * k, ("fprop", ends)))
+        # wgrad: dY^T [n][tokens] x X^T [k][tokens], both columnwise, per-group column amax
+        cg, sg, ag = workloads.nvfp4_operand(n, m, 43, row_scaled=True, device=dev)
+        cx, sx, ax = workloads.nvfp4_operand(k, m, 44, row_scaled=True, device=dev)
+        rng = torch.Generator(device=dev)
+        rng.manual_seed(45)
+        a2 = nv.Operand(cg, sg, torch.rand(groups * n, generator=rng, device=dev) + 0.5,
+                        nv.NVFP4_ROW_SCALED, 448.0)
+        b2 = nv.Operand(cx, sx, torch.rand(groups * k, generator=rng, device=dev) + 0.5,
+                        nv.NVFP4_ROW_SCALED, 448.0)
+        d2 = torch.empty(groups, n, k, dtype=torch.bfloat16, device=dev)
+        ws2 = torch.empty(nv.nvfp4_gemm_workspace_size(n, k, m), dtype=torch.uint8, device=dev)
+        calls.append((a2, b2, d2, ws2, 2.0 * n * k * m, ("wgrad", ends)))
+        flops += 2.0 * m * n * k * 2
         jobs = []
     for i, (name, b_rs) in enumerate(jobs):
         m, n, k = name if isinstance(name, tuple) else workloads.GEMM_SHAPES[name]
@@ -726,13 +743,15 @@ def run_gemm(args):
         flops += 2.0 * m * n * k
 
     def step(ev):
-        for j, (a, b, d, ws, _, ends) in enumerate(calls):
+        for j, (a, b, d, ws, _, grp) in enumerate(calls):
             if j == len(calls) - 1:
                 ev[0].record(stream)
-            if ends is not None:
-                nv.nvfp4_grouped_gemm(a, b, ends, d, ws, stream=stream)
-            else:
+            if grp is None:
                 nv.nvfp4_gemm(a, b, d, ws, stream=stream)
+            elif grp[0] == "fprop":
+                nv.nvfp4_grouped_gemm(a, b, grp[1], d, ws, stream=stream)
+            else:
+                nv.nvfp4_grouped_gemm_wgrad(a, b, grp[1], d, ws, stream=stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -769,7 +788,7 @@ def run_gemm(args):
     if rank == 0:
         print(json.dumps({
             "metric": "NVFP4 GEMM consumer TFLOP/s" + (
-                " (grouped, MoE experts)" if grouped else
+                " (grouped MoE fprop + wgrad)" if grouped else
                 "" if args.gemm_shape else " (fprop + wgrad of the linear layer)"),
             "value": rate / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K_,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K_, "higher_is_better": True,

@@ -305,6 +305,27 @@ NVFP4_API nvfp4_status nvfp4_grouped_gemm(const nvfp4_operand *a, const nvfp4_op
                                 nvfp4_stream_t stream);
 
 /*
+ * nvfp4_grouped_gemm_wgrad -- the per-expert weight-gradient GEMM of the same MoE
+ * layout: group g's token range [s_g, e_g) is the reduction dimension,
+ *   d[g][i][j] = sum_{s_g <= c < e_g} value_a(i, c) * value_b(j, c),
+ * with the bilateral post-scale of nvfp4_gemm using group g's amax.  The operands
+ * are columnwise outputs of nvfp4_grouped_quantize_columnwise (lines = features, the
+ * tokens along K): a = dY^T (m lines), b = X^T (n lines), each [lines][tokens/2];
+ * a->amax [num_groups * m] (NVFP4_ROW_SCALED: group g's per-line amax at g*m) or
+ * [num_groups] (NVFP4_PER_TENSOR: one per group); b->amax likewise with n.
+ *   group_ends: device int64 [num_groups], cumulative token ends, every end a
+ *   multiple of 256 (so that no 256-token K tile spans two groups), last == tokens;
+ *   an empty group gets a zero block.  d: [num_groups][m][n].
+ *   Invalid or unaligned ends set NVFP4_DEVICE_BAD_GROUPS and write nothing.
+ *   workspace: nvfp4_gemm_workspace_size(m, n, tokens) bytes.
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_gemm_wgrad(const nvfp4_operand *a, const nvfp4_operand *b,
+                                      const int64_t *group_ends, int32_t num_groups, int64_t m,
+                                      int64_t n, int64_t tokens, void *d, int32_t out_dtype,
+                                      void *workspace, uint64_t workspace_bytes,
+                                      nvfp4_stream_t stream);
+
+/*
  * nvfp4_gemm_static_ws -- nvfp4_gemm with its workspace in the library's own static
  * device memory instead of a caller buffer: NVFP4_GEMM_STATIC_WS_BYTES per device,
  * reserved when the library's device code is loaded, so the call allocates nothing.

@@ -27,7 +27,7 @@ __all__ = [
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws", "Operand",
-    "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm",
+    "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
     "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS",
 ]
 
@@ -52,7 +52,7 @@ EXPORTED_SYMBOLS = (
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws",
-    "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm",
+    "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -128,6 +128,8 @@ def load_library():
         "nvfp4_gemm_static_ws": [vp, vp, i64, i64, i64, vp, i32, vp],
         "nvfp4_grouped_gemm_workspace_size": [i64, i64, i64, i32, C.POINTER(C.c_uint64)],
         "nvfp4_grouped_gemm": [vp, vp, vp, i32, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
+        "nvfp4_grouped_gemm_wgrad": [vp, vp, vp, i32, i64, i64, i64, vp, i32, vp, C.c_uint64,
+                                     vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -357,6 +359,33 @@ def nvfp4_grouped_gemm(a: Operand, b: Operand, group_ends: torch.Tensor, d: torc
     _check(load_library().nvfp4_grouped_gemm(C.byref(ca), C.byref(cb), _ptr(group_ends), groups,
                                               rows, n, k, _ptr(d), od, _ptr(workspace),
                                               workspace.numel(), _stream(stream)))
+
+
+def nvfp4_grouped_gemm_wgrad(a: Operand, b: Operand, group_ends: torch.Tensor, d: torch.Tensor,
+                             workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """d [groups][m][n]: per group g, dequant(a) x dequant(b)^T over g's token range of K.
+    a [m][tokens/2], b [n][tokens/2] (columnwise outputs); group_ends device int64."""
+    if d.dim() != 3 or not d.is_contiguous():
+        raise ValueError("d must be a contiguous 3-D tensor [groups][m][n]")
+    if d.dtype == torch.bfloat16:
+        od = NVFP4_OUT_BF16
+    elif d.dtype == torch.float32:
+        od = NVFP4_OUT_FP32
+    else:
+        raise TypeError("d must be bfloat16 or float32")
+    groups, m, n = d.shape
+    tokens = a.codes.shape[1] * 2
+    if (groups != group_ends.numel() or a.codes.shape[0] != m or b.codes.shape[0] != n
+            or b.codes.shape[1] * 2 != tokens):
+        raise ValueError("operand shapes do not match d and the group count")
+    need = nvfp4_gemm_workspace_size(m, n, tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=d.device)
+    ca, cb = a._c(), b._c()
+    _check(load_library().nvfp4_grouped_gemm_wgrad(C.byref(ca), C.byref(cb), _ptr(group_ends),
+                                                    groups, m, n, tokens, _ptr(d), od,
+                                                    _ptr(workspace), workspace.numel(),
+                                                    _stream(stream)))
 
 
 def nvfp4_gemm_static_ws(a: Operand, b: Operand, d: torch.Tensor, stream=None) -> None:

@@ -426,7 +426,7 @@ namespace {
 nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, const int64_t* group_ends,
                        int32_t num_groups, int64_t m, int64_t n, int64_t k, void* d,
                        int32_t out_dtype, void* workspace, uint64_t workspace_bytes,
-                       nvfp4_stream_t stream, bool static_ws) {
+                       nvfp4_stream_t stream, bool static_ws, bool k_grouped = false) {
   nvfp4_status st;
   if ((st = check_sizes(m, n)) != NVFP4_OK) return st;
   if ((st = check_sizes(k, 0)) != NVFP4_OK) return st;
@@ -443,7 +443,8 @@ nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, const int
   if (d == nullptr) return fail(NVFP4_ERR_INVALID, "d is NULL");
   const size_t esize = out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
   if (k == 0) {  // the empty sum
-    cudaError_t e = cudaMemsetAsync(d, 0, (size_t)m * (size_t)n * esize, stream);
+    const size_t blocks = k_grouped ? (size_t)num_groups : 1;
+    cudaError_t e = cudaMemsetAsync(d, 0, blocks * (size_t)m * (size_t)n * esize, stream);
     return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "cudaMemsetAsync");
   }
   if (k % 32 != 0) return fail(NVFP4_ERR_UNSUPPORTED, "k must be a multiple of 32");
@@ -453,9 +454,12 @@ nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, const int
     if (reinterpret_cast<uintptr_t>(o->codes) % 16 != 0)
       return fail(NVFP4_ERR_UNSUPPORTED, "operand codes must be 16-byte aligned");
   }
-  if (group_ends != nullptr && n % 256 != 0)
+  if (group_ends != nullptr && !k_grouped && n % 256 != 0)
     return fail(NVFP4_ERR_UNSUPPORTED, "grouped GEMM: n must be a multiple of 256");
-  const GemmLayout L = gemm_layout(m, n, k, group_ends ? (int64_t)num_groups * n : n);
+  if (k_grouped && k % 256 != 0)
+    return fail(NVFP4_ERR_UNSUPPORTED, "grouped wgrad GEMM: tokens must be a multiple of 256");
+  const GemmLayout L =
+      gemm_layout(m, n, k, group_ends && !k_grouped ? (int64_t)num_groups * n : n);
   if (L.tiles_m * L.tiles_n >= (1LL << 31)) return fail(NVFP4_ERR_UNSUPPORTED, "too many tiles");
   if (static_ws) {
     if ((uint64_t)L.workspace_bytes > (uint64_t)NVFP4_GEMM_STATIC_WS_BYTES)
@@ -489,6 +493,7 @@ nvfp4_status gemm_impl(const nvfp4_operand* a, const nvfp4_operand* b, const int
   g.workspace = static_ws ? dev.gemm_static_ws : static_cast<uint8_t*>(workspace);
   g.group_ends = group_ends;
   g.num_groups = num_groups;
+  g.k_grouped = k_grouped;
   cudaError_t e = launch_gemm(g, dev, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return NVFP4_OK;
@@ -525,6 +530,18 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_operand* a, const nvfp4_operand* b,
     return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
   return gemm_impl(a, b, group_ends, num_groups, rows, n, k, d, out_dtype, workspace,
                    workspace_bytes, stream, false);
+}
+
+nvfp4_status nvfp4_grouped_gemm_wgrad(const nvfp4_operand* a, const nvfp4_operand* b,
+                                      const int64_t* group_ends, int32_t num_groups, int64_t m,
+                                      int64_t n, int64_t tokens, void* d, int32_t out_dtype,
+                                      void* workspace, uint64_t workspace_bytes,
+                                      nvfp4_stream_t stream) {
+  if (group_ends == nullptr) return fail(NVFP4_ERR_INVALID, "group_ends is NULL");
+  if (num_groups < 1 || num_groups > 4096)
+    return fail(NVFP4_ERR_INVALID, "num_groups must be in [1, 4096]");
+  return gemm_impl(a, b, group_ends, num_groups, m, n, tokens, d, out_dtype, workspace,
+                   workspace_bytes, stream, false, true);
 }
 
 nvfp4_status nvfp4_gemm_static_ws(const nvfp4_operand* a, const nvfp4_operand* b, int64_t m,

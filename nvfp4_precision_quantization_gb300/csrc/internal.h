@@ -154,6 +154,10 @@ struct GemmArgs {
   // multiple of 256; b_amax [num_groups*N] (row-scaled) or [num_groups]
   const int64_t* group_ends;
   int num_groups;
+  // with group_ends: false -- groups of A's rows (per-expert fprop); true -- groups of
+  // K (tokens, ends multiples of 256): group g writes d + g*M*N from its K range,
+  // a_amax [num_groups*M] or [num_groups], b_amax [num_groups*N] or [num_groups]
+  bool k_grouped;
 };
 struct GemmLayout {
   int64_t k_tiles, tiles_m, tiles_n;

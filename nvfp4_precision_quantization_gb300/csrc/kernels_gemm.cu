@@ -263,12 +263,22 @@ struct GemmParams {
   int num_groups;
   int b_group_rows;         // N in the grouped GEMM, 0 otherwise
   int b_amax_group_stride;  // where group g's amax starts in b_amax (N, 1 or 0)
+  // K-grouped (the per-expert wgrad GEMM): group_ends cut K (tokens, multiples of 256)
+  // and group g writes its own [M][N] block of d, d + g * M * N
+  bool k_grouped;
+  int64_t group_total;      // what the last group end must equal (rows of A, or K)
+  int a_amax_group_stride;  // where group g's amax starts in a_amax (K-grouped: M, 1)
+};
+
+// One output tile of this CTA's walk: its group, tile coordinates and K tiles.
+struct TileJob {
+  int g, tm, tn, kt0, kt1;
 };
 
 // The group of the A tile starting at row r: the first g with group_ends[g] > r
-// (empty groups are skipped); 0 when the GEMM is not grouped.
+// (empty groups are skipped); 0 when the GEMM is not grouped by rows.
 __device__ __forceinline__ int group_of_row(const GemmParams& p, int64_t r) {
-  if (p.group_ends == nullptr) return 0;
+  if (p.group_ends == nullptr || p.k_grouped) return 0;
   int lo = 0, hi = p.num_groups - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
@@ -279,6 +289,27 @@ __device__ __forceinline__ int group_of_row(const GemmParams& p, int64_t r) {
 }
 
 constexpr int kRasterGroup = 32;  // M tiles walked together so their A tiles stay in L2
+
+__device__ __forceinline__ void tile_coords(int idx, int tiles_m, int tiles_n, int& tm, int& tn);
+__device__ __forceinline__ int group_of_row(const GemmParams& p, int64_t r);
+
+__device__ __forceinline__ TileJob tile_job(const GemmParams& p, int tile) {
+  TileJob j;
+  j.g = 0;
+  j.kt0 = 0;
+  j.kt1 = p.k_tiles;
+  if (p.k_grouped) {
+    const int per = p.tiles_m * p.tiles_n;
+    j.g = tile / per;
+    tile_coords(tile - j.g * per, p.tiles_m, p.tiles_n, j.tm, j.tn);
+    j.kt0 = (int)((j.g ? p.group_ends[j.g - 1] : 0) / (2 * kBKBytes));
+    j.kt1 = (int)(p.group_ends[j.g] / (2 * kBKBytes));
+  } else {
+    tile_coords(tile, p.tiles_m, p.tiles_n, j.tm, j.tn);
+    if (p.group_ends != nullptr) j.g = group_of_row(p, (int64_t)j.tm * kBM);
+  }
+  return j;
+}
 
 __device__ __forceinline__ void tile_coords(int idx, int tiles_m, int tiles_n, int& tm, int& tn) {
   const int group = idx / (kRasterGroup * tiles_n);
@@ -309,11 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* err = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int num_tiles = (p.k_grouped ? p.num_groups : 1) * p.tiles_m * p.tiles_n;
 
   if (p.group_ends != nullptr) {  // every thread takes part; nothing is written if invalid
-    const bool ok = groups_valid(p.group_ends, p.num_groups, p.M) &&
-                    ends_aligned(p.group_ends, p.num_groups, kBM);
+    const bool ok = groups_valid(p.group_ends, p.num_groups, p.group_total) &&
+                    ends_aligned(p.group_ends, p.num_groups, p.k_grouped ? 2 * kBKBytes : kBM);
     if (!ok) {
       if (threadIdx.x == 0) raise_status(p.status, kStatusBadGroups);
       return;
@@ -348,10 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;  // K tiles issued, over all tiles of this CTA
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      int tm, tn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
-      const int b_tile0 = group_of_row(p, (int64_t)tm * kBM) * (p.b_group_rows / kBN);
-      for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+      const TileJob job = tile_job(p, tile);
+      const int tm = job.tm, tn = job.tn;
+      const int b_tile0 = job.g * (p.b_group_rows / kBN);  // the expert's rows of B
+      for (int kt = job.kt0; kt < job.kt1; ++kt, ++it) {
         const uint32_t s = it % S;
         if (it >= (uint32_t)S && !mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1)) {
           *err = 1;
@@ -403,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+      const TileJob job = tile_job(p, tile);
+      for (int kt = job.kt0; kt < job.kt1; ++kt, ++it) {
         const uint32_t s = it % S;
         if (!mbar_wait_bounded(&full[s], (it / S) & 1)) {
           *err = 1;
@@ -423,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < kKSteps; ++ks)
           tc_mma_nvf4(tmem, desc_swz(st + ks * kUmmaKBytes),
                       desc_swz(st + kABytes + ks * kUmmaKBytes), p.idesc, sfa_col + 4 * ks,
-                      sfb_col + 8 * ks, (kt | ks) != 0);
+                      sfb_col + 8 * ks, (kt != job.kt0) || ks != 0);
         tc_commit(&empty[s]);
       }
       // the accumulator of this tile is complete (or abandoned) once all issued MMAs are
@@ -435,11 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue: lane quarter q (rows 32q ..), column half `half`
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
-    const bool b_vec = p.b_amax_stride != 0 && (reinterpret_cast<uintptr_t>(p.b_amax) & 15) == 0;
+    const bool b_lines = p.b_amax_stride != 0;  // one amax per line of B
     uint32_t t = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
-      int tm, tn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+      const TileJob job = tile_job(p, tile);
+      const int tm = job.tm, tn = job.tn;
       const bool ready = mbar_wait_bounded(acc_full, t & 1);
       if (!ready) *err = 1;
       tc_fence_after();
@@ -452,15 +484,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);  // TMEM may take the next tile's MMAs
       if (!ready || *(volatile int*)err) break;
+      if (job.kt1 == job.kt0) {  // an empty K range (an empty group): the sum is 0
+#pragma unroll
+        for (int i = 0; i < kEpiCols; ++i) v[i] = 0u;
+      }
 
       const int row = tm * kBM + q * 32 + lane;
       const int col_base = tn * kBN + half * kEpiCols;
       if (row >= p.M || col_base >= p.N) continue;
-      const float alpha = __fmul_rn(p.a_amax[(int64_t)row * p.a_amax_stride], p.a_finv);
-      const float* b_amax =
-          p.b_amax + (int64_t)group_of_row(p, (int64_t)tm * kBM) * p.b_amax_group_stride;
+      const float alpha = __fmul_rn(
+          p.a_amax[(int64_t)job.g * p.a_amax_group_stride + (int64_t)row * p.a_amax_stride],
+          p.a_finv);
+      const float* b_amax = p.b_amax + (int64_t)job.g * p.b_amax_group_stride;
+      // 16-byte loads of beta only where this group's amax row is 16-byte aligned
+      const bool b_vec = b_lines && (reinterpret_cast<uintptr_t>(b_amax) & 15) == 0;
       const int nvalid = min(kEpiCols, p.N - col_base);
-      const int64_t off = (int64_t)row * p.N + col_base;
+      const int64_t off = (p.k_grouped ? (int64_t)job.g * p.M * p.N : 0) +
+                          (int64_t)row * p.N + col_base;
       const bool vec = nvalid == kEpiCols &&
                        ((reinterpret_cast<uintptr_t>(p.d) + off * (p.d_bf16 ? 2 : 4)) & 15) == 0;
 #pragma unroll
@@ -561,7 +601,7 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const D
   uint8_t* sfb = a.workspace + L.sfb_offset;
   k_sf_layout<<<(unsigned)(L.tiles_m * L.k_tiles), 256, 0, stream>>>(a.a_scales, a.M, a.K / 16,
                                                                      L.k_tiles, 1, sfa);
-  const int64_t b_lines = a.group_ends ? (int64_t)a.num_groups * a.N : a.N;
+  const int64_t b_lines = a.group_ends && !a.k_grouped ? (int64_t)a.num_groups * a.N : a.N;
   k_sf_layout<<<(unsigned)(ceil_div(b_lines, kBN) * L.k_tiles), 256, 0, stream>>>(
       a.b_scales, b_lines, a.K / 16, L.k_tiles, 2, sfb);
   cudaError_t e = cudaGetLastError();
@@ -599,16 +639,20 @@ static cudaError_t launch_gemm_t(const GemmArgs& a, const GemmLayout& L, const D
   p.status = dev.status;
   p.group_ends = a.group_ends;
   p.num_groups = a.group_ends ? a.num_groups : 0;
-  p.b_group_rows = a.group_ends ? (int)a.N : 0;
+  p.k_grouped = a.group_ends != nullptr && a.k_grouped;
+  p.b_group_rows = a.group_ends && !a.k_grouped ? (int)a.N : 0;
   p.b_amax_group_stride = a.group_ends ? (a.b_row_scaled ? (int)a.N : 1) : 0;
-  const int grid = (int)std::min<int64_t>(L.tiles_m * L.tiles_n, dev.num_sms);
+  p.a_amax_group_stride = p.k_grouped ? (a.a_row_scaled ? (int)a.M : 1) : 0;
+  p.group_total = p.k_grouped ? a.K : a.M;
+  const int64_t tiles = (a.group_ends && a.k_grouped ? a.num_groups : 1) * L.tiles_m * L.tiles_n;
+  const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
   k_gemm_nvf4<SF><<<grid, kThreads, G::kSmemBytes, stream>>>(map_a, map_b, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  const GemmLayout L =
-      gemm_layout(a.M, a.N, a.K, a.group_ends ? (int64_t)a.num_groups * a.N : a.N);
+  const GemmLayout L = gemm_layout(
+      a.M, a.N, a.K, a.group_ends && !a.k_grouped ? (int64_t)a.num_groups * a.N : a.N);
   return launch_gemm_t<SfLayout>(a, L, dev, stream);
 }
 

@@ -293,3 +293,31 @@ def grouped_gemm(a, b, group_ends, n: int, *, with_abs: bool = False):
                 d[start:e] = r
         start = e
     return (d, da) if with_abs else d
+
+
+def grouped_gemm_wgrad(a, b, group_ends, *, with_abs: bool = False):
+    """The per-expert weight-gradient GEMM: for group g, the token range [e_{g-1}, e_g)
+    of K, d[g] = gemm() of a's and b's columns in that range (their codes, scales and
+    group g's amax: [groups*lines] per line or [groups] per group).  Composition of the
+    pinned gemm() above; no new arithmetic."""
+    ends = np.asarray(group_ends, np.int64)
+    m, n = a["codes"].shape[0], b["codes"].shape[0]
+    G = len(ends)
+    d = np.zeros((G, m, n), np.float64)
+    da = np.zeros((G, m, n), np.float64) if with_abs else None
+
+    def part(op, lines, g, s, e):
+        am = op["amax"][g * lines:(g + 1) * lines] if op["row_scaled"] else op["amax"][g:g + 1]
+        return dict(op, codes=op["codes"][:, s // 2:e // 2], scales=op["scales"][:, s // 16:e // 16],
+                    amax=am)
+
+    start = 0
+    for g, e in enumerate(ends.tolist()):
+        if e > start:
+            r = gemm(part(a, m, g, start, e), part(b, n, g, start, e), with_abs=with_abs)
+            if with_abs:
+                d[g], da[g] = r
+            else:
+                d[g] = r
+        start = e
+    return (d, da) if with_abs else d

@@ -104,3 +104,93 @@ def test_moe_grouped_gemm_sampled():
         exp, dabs = oracle.gemm(a_h, b_h, with_abs=True)
         got = d[ri][:, ci].float().cpu().numpy().astype(np.float64)
         assert np.all(np.abs(got - exp) <= _bound(k, dabs, exp, True)), g
+
+
+# ---------------------------------------------------------------- wgrad (K grouped)
+
+def _wgrad_run(a_h, b_h, ends, a_mode, b_mode, dtype, fill=float("nan")):
+    G, m, n = len(ends), a_h["codes"].shape[0], b_h["codes"].shape[0]
+    d = torch.full((G, m, n), fill, dtype=dtype, device=DEV)
+    nv.nvfp4_device_status(reset=True)
+    nv.nvfp4_grouped_gemm_wgrad(_dev(a_h, a_mode), _dev(b_h, b_mode),
+                                torch.tensor(ends, dtype=torch.int64, device=DEV), d)
+    torch.cuda.synchronize()
+    return d
+
+
+@pytest.mark.parametrize("modes", [(RS, RS), (PT, PT), (RS, PT)])
+def test_grouped_wgrad_matches_oracle(modes):
+    ends = [256, 256, 768, 1024]  # an empty group
+    G, m, n, tokens = len(ends), 200, 300, ends[-1]
+    ca, sa, _ = workloads.nvfp4_operand(m, tokens, 80, row_scaled=True)
+    cb, sb, _ = workloads.nvfp4_operand(n, tokens, 81, row_scaled=True)
+    rng = np.random.default_rng(9)
+    aa = np.exp(rng.uniform(-2, 2, G * m if modes[0] == RS else G)).astype(np.float32)
+    ab = np.exp(rng.uniform(-2, 2, G * n if modes[1] == RS else G)).astype(np.float32)
+    a_h = _host_op(ca.numpy(), sa.numpy(), aa, modes[0], 448.0)
+    b_h = _host_op(cb.numpy(), sb.numpy(), ab, modes[1], 256.0)
+    dtype = torch.float32 if modes[0] == modes[1] else torch.bfloat16
+    d = _wgrad_run(a_h, b_h, ends, modes[0], modes[1], dtype)
+    assert nv.nvfp4_device_status(reset=True) == 0
+    got = d.float().cpu().numpy().astype(np.float64)
+    exp, dabs = oracle.grouped_gemm_wgrad(a_h, b_h, ends, with_abs=True)
+    assert np.all(got[1] == 0)  # the empty group
+    bad = np.argwhere(~(np.abs(got - exp) <= _bound(512, dabs, exp, dtype == torch.bfloat16)))
+    assert bad.size == 0, f"{len(bad)} outside the bound, first {bad[:4].tolist()}"
+
+
+def test_grouped_wgrad_on_grouped_columnwise_operands():
+    """The MoE backward chain: dY and X of two token groups quantized columnwise per
+    group (row-scaled: each group's column amax; the oracle's quantize, group by group),
+    then dW_g = dY_g^T X_g on the tensor cores against the oracle."""
+    rng = np.random.default_rng(10)
+    ends = [256, 768]
+    d_out, d_in, tokens = 256, 192, ends[-1]
+    dy = (rng.standard_normal((tokens, d_out)) * 0.5).astype(np.float32)
+    x = (rng.standard_normal((tokens, d_in)) * np.exp(rng.uniform(-1, 1, (tokens, 1)))).astype(np.float32)
+
+    def per_group_columnwise(t):
+        cols = t.shape[1]
+        codes = np.zeros((cols, tokens // 2), np.uint8)
+        scales = np.zeros((cols, tokens // 16), np.uint8)
+        amax = np.zeros((len(ends), cols), np.float32)
+        s = 0
+        for g, e in enumerate(ends):
+            o = oracle.quantize(t[s:e], "fp32", mode=oracle.ROW_SCALED, rowwise=False)["col"]
+            codes[:, s // 2:e // 2], scales[:, s // 16:e // 16], amax[g] = o
+            s = e
+        return _host_op(codes, scales, amax.reshape(-1), RS, 448.0)
+
+    a_h, b_h = per_group_columnwise(dy), per_group_columnwise(x)
+    d = _wgrad_run(a_h, b_h, ends, RS, RS, torch.float32)
+    assert nv.nvfp4_device_status(reset=True) == 0
+    got = d.cpu().numpy().astype(np.float64)
+    exp, dabs = oracle.grouped_gemm_wgrad(a_h, b_h, ends, with_abs=True)
+    assert np.all(np.abs(got - exp) <= _bound(512, dabs, exp, False))
+    s = 0
+    for g, e in enumerate(ends):  # close to the unquantized per-group product
+        ref = dy[s:e].T.astype(np.float64) @ x[s:e].astype(np.float64)
+        assert np.linalg.norm(got[g] - ref) < 0.2 * np.linalg.norm(ref), g
+        s = e
+
+
+def test_grouped_wgrad_invalid_ends_write_nothing():
+    m = n = 128
+    tokens = 512
+    ca, sa, _ = workloads.nvfp4_operand(m, tokens, 90, row_scaled=True)
+    cb, sb, _ = workloads.nvfp4_operand(n, tokens, 91, row_scaled=True)
+    for ends in ([128, 512], [512, 256], [256]):  # unaligned, decreasing, short
+        G = len(ends)
+        a_h = _host_op(ca.numpy(), sa.numpy(), np.ones(G * m, np.float32), RS, 448.0)
+        b_h = _host_op(cb.numpy(), sb.numpy(), np.ones(G * n, np.float32), RS, 448.0)
+        d = _wgrad_run(a_h, b_h, ends, RS, RS, torch.float32, fill=7.0)
+        assert nv.nvfp4_device_status(reset=True) & nv.NVFP4_DEVICE_BAD_GROUPS, ends
+        assert bool((d == 7.0).all()), ends
+
+
+def test_grouped_wgrad_tokens_not_multiple_of_256_is_unsupported():
+    ca, sa, _ = workloads.nvfp4_operand(128, 384, 92, row_scaled=True)
+    a_h = _host_op(ca.numpy(), sa.numpy(), np.ones(128, np.float32), RS, 448.0)
+    with pytest.raises(nv.NVFP4Error) as ei:
+        _wgrad_run(a_h, a_h, [384], RS, RS, torch.float32)
+    assert ei.value.status == nv.NVFP4_ERR_UNSUPPORTED

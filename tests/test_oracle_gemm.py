@@ -147,3 +147,20 @@ def test_grouped_gemm_is_the_per_group_product():
     assert np.array_equal(d2[128:], 2.0 * d[128:]) and np.array_equal(d2[:128], d[:128])
     # a single group is the dense GEMM with expert 0
     assert np.array_equal(oracle.grouped_gemm(a, b, [384], n), oracle.gemm(a, experts[0]))
+
+
+def test_grouped_wgrad_sums_to_the_dense_product():
+    """With one shared amax per line for every group (the same per-group values), the
+    per-group K ranges add up to the dense GEMM over all of K (linearity in K), and an
+    empty group's block is zero."""
+    k = 96
+    a = _random_operand(5, k, seed=41, row_scaled=True)
+    b = _random_operand(6, k, seed=42, row_scaled=True)
+    ends = [32, 32, 96]
+    G = len(ends)
+    ag = dict(a, amax=np.tile(a["amax"], G))
+    bg = dict(b, amax=np.tile(b["amax"], G))
+    d, dabs = oracle.grouped_gemm_wgrad(ag, bg, ends, with_abs=True)
+    full, fabs = oracle.gemm(a, b, with_abs=True)
+    assert np.all(d[1] == 0)
+    assert np.all(np.abs(d.sum(0) - full) <= 2.0 ** -48 * fabs)
