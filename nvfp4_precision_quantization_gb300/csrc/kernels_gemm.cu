@@ -65,6 +65,7 @@ constexpr int kThreads = 64 + 32 * kEpilogueWarps;    // producer, MMA, epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSfCol0 = kBN;                          // scale columns follow the accumulator
 constexpr int kMetaBytes = 1024;                      // barriers, TMEM address, error flag
+constexpr int kSmemEnds = 1024;                       // group ends staged in shared memory
 
 // Where the tensor core reads the scales of a block-scaled MMA with M = 128 and
 // scale_vec::4X (one 32-bit TMEM word = the four scales of a line for the MMA's
@@ -87,7 +88,8 @@ template <class SF>
 struct GemmGeom {
   static constexpr int kStageBytes = kABytes + kBBytes + SF::kSfaBytes + SF::kSfbBytes;
   static constexpr int kSfColsPerStage = SF::kSfaCols + SF::kSfbCols;
-  static constexpr int kSmemBytes = SF::kStages * kStageBytes + kMetaBytes + 1024 /* alignment */;
+  static constexpr int kSmemBytes = SF::kStages * kStageBytes + kMetaBytes +
+                                    kSmemEnds * 8 /* group ends */ + 1024 /* alignment */;
   static_assert(kSfCol0 + SF::kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM columns");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128B swizzle");
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -277,12 +279,12 @@ struct TileJob {
 
 // The group of the A tile starting at row r: the first g with group_ends[g] > r
 // (empty groups are skipped); 0 when the GEMM is not grouped by rows.
-__device__ __forceinline__ int group_of_row(const GemmParams& p, int64_t r) {
+__device__ __forceinline__ int group_of_row(const GemmParams& p, const int64_t* ends, int64_t r) {
   if (p.group_ends == nullptr || p.k_grouped) return 0;
   int lo = 0, hi = p.num_groups - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (p.group_ends[mid] > r) hi = mid;
+    if (ends[mid] > r) hi = mid;
     else lo = mid + 1;
   }
   return lo;
@@ -291,9 +293,10 @@ __device__ __forceinline__ int group_of_row(const GemmParams& p, int64_t r) {
 constexpr int kRasterGroup = 32;  // M tiles walked together so their A tiles stay in L2
 
 __device__ __forceinline__ void tile_coords(int idx, int tiles_m, int tiles_n, int& tm, int& tn);
-__device__ __forceinline__ int group_of_row(const GemmParams& p, int64_t r);
+__device__ __forceinline__ int group_of_row(const GemmParams& p, const int64_t* ends, int64_t r);
 
-__device__ __forceinline__ TileJob tile_job(const GemmParams& p, int tile) {
+// ends: the group ends (a shared-memory copy when they fit)
+__device__ __forceinline__ TileJob tile_job(const GemmParams& p, const int64_t* ends, int tile) {
   TileJob j;
   j.g = 0;
   j.kt0 = 0;
@@ -302,11 +305,11 @@ __device__ __forceinline__ TileJob tile_job(const GemmParams& p, int tile) {
     const int per = p.tiles_m * p.tiles_n;
     j.g = tile / per;
     tile_coords(tile - j.g * per, p.tiles_m, p.tiles_n, j.tm, j.tn);
-    j.kt0 = (int)((j.g ? p.group_ends[j.g - 1] : 0) / (2 * kBKBytes));
-    j.kt1 = (int)(p.group_ends[j.g] / (2 * kBKBytes));
+    j.kt0 = (int)((j.g ? ends[j.g - 1] : 0) / (2 * kBKBytes));
+    j.kt1 = (int)(ends[j.g] / (2 * kBKBytes));
   } else {
     tile_coords(tile, p.tiles_m, p.tiles_n, j.tm, j.tn);
-    if (p.group_ends != nullptr) j.g = group_of_row(p, (int64_t)j.tm * kBM);
+    if (p.group_ends != nullptr) j.g = group_of_row(p, ends, (int64_t)j.tm * kBM);
   }
   return j;
 }
@@ -338,6 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   int* err = reinterpret_cast<int*>(tmem_slot + 1);
+  int64_t* s_ends = reinterpret_cast<int64_t*>(smem + S * G::kStageBytes + kMetaBytes);
+  // every tile looks its group up: from shared memory when the ends fit
+  const int64_t* ends = p.num_groups <= kSmemEnds ? s_ends : p.group_ends;
+  if (p.group_ends != nullptr && p.num_groups <= kSmemEnds)
+    for (int g = threadIdx.x; g < p.num_groups; g += blockDim.x) s_ends[g] = p.group_ends[g];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = (p.k_grouped ? p.num_groups : 1) * p.tiles_m * p.tiles_n;
@@ -379,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;  // K tiles issued, over all tiles of this CTA
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const TileJob job = tile_job(p, tile);
+      const TileJob job = tile_job(p, ends, tile);
       const int tm = job.tm, tn = job.tn;
       const int b_tile0 = job.g * (p.b_group_rows / kBN);  // the expert's rows of B
       for (int kt = job.kt0; kt < job.kt1; ++kt, ++it) {
@@ -434,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const TileJob job = tile_job(p, tile);
+      const TileJob job = tile_job(p, ends, tile);
       for (int kt = job.kt0; kt < job.kt1; ++kt, ++it) {
         const uint32_t s = it % S;
         if (!mbar_wait_bounded(&full[s], (it / S) & 1)) {
@@ -470,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool b_lines = p.b_amax_stride != 0;  // one amax per line of B
     uint32_t t = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
-      const TileJob job = tile_job(p, tile);
+      const TileJob job = tile_job(p, ends, tile);
       const int tm = job.tm, tn = job.tn;
       const bool ready = mbar_wait_bounded(acc_full, t & 1);
       if (!ready) *err = 1;
