@@ -385,6 +385,13 @@ __device__ __forceinline__ uint4 ldg_v4_policy(const void* p, uint64_t policy) {
   return v;
 }
 
+// One 32-byte store (a whole L2 sector); p must be 32-byte aligned.
+__device__ __forceinline__ void stg_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Streaming stores for outputs that are not read again by this kernel.
 __device__ __forceinline__ void stg_v4_cs(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),

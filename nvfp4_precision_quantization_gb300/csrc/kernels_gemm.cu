@@ -509,8 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nvalid = min(kEpiCols, p.N - col_base);
       const int64_t off = (p.k_grouped ? (int64_t)job.g * p.M * p.N : 0) +
                           (int64_t)row * p.N + col_base;
-      const bool vec = nvalid == kEpiCols &&
-                       ((reinterpret_cast<uintptr_t>(p.d) + off * (p.d_bf16 ? 2 : 4)) & 15) == 0;
+      // whole 32-byte sectors per store where the row's run is 32-byte aligned,
+      // else 16-byte stores, else (ragged N or odd alignment) element stores
+      const uintptr_t d_addr = reinterpret_cast<uintptr_t>(p.d) + off * (p.d_bf16 ? 2 : 4);
+      const bool vec = nvalid == kEpiCols && (d_addr & 15) == 0;
+      const bool vec32 = vec && (d_addr & 31) == 0;
 #pragma unroll
       for (int c = 0; c < kEpiCols / 32; ++c) {
         const int col0 = col_base + c * 32;
@@ -534,28 +537,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (p.d_bf16) {
           uint16_t* dst = static_cast<uint16_t*>(p.d) + off + c * 32;
+          uint32_t w[16];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t w[4];
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(vc[2 * j]),
+                                                      __uint_as_float(vc[2 * j + 1]));
+            w[j] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          if (vec32) {
+            stg_v8(dst, w);
+            stg_v8(dst + 16, w + 8);
+          } else if (vec) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(vc[8 * g + 2 * j]),
-                                                        __uint_as_float(vc[8 * g + 2 * j + 1]));
-              w[j] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            if (vec) {
-              *reinterpret_cast<uint4*>(dst + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
+            for (int g = 0; g < 4; ++g)
+              *reinterpret_cast<uint4*>(dst + 8 * g) =
+                  make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+          } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                if (c * 32 + 8 * g + j < nvalid) dst[8 * g + j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
-            }
+            for (int j = 0; j < 32; ++j)
+              if (c * 32 + j < nvalid) dst[j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
           }
         } else {
           uint32_t* dst = static_cast<uint32_t*>(p.d) + off + c * 32;
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
-            if (vec) {
+            if (vec32) {
+              if ((g & 1) == 0) stg_v8(dst + 4 * g, vc + 4 * g);
+            } else if (vec) {
               *reinterpret_cast<uint4*>(dst + 4 * g) =
                   make_uint4(vc[4 * g], vc[4 * g + 1], vc[4 * g + 2], vc[4 * g + 3]);
             } else {
