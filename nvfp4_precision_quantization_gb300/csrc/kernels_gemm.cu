@@ -65,7 +65,8 @@ constexpr int kThreads = 64 + 32 * kEpilogueWarps;    // producer, MMA, epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSfCol0 = kBN;                          // scale columns follow the accumulator
 constexpr int kMetaBytes = 1024;                      // barriers, TMEM address, error flag
-constexpr int kSmemEnds = 1024;                       // group ends staged in shared memory
+constexpr int kSmemEnds = 512;                        // group ends staged in shared memory
+constexpr int kBetaBytes = kEpilogueWarps * kEpiCols * 4;  // per-warp column factors
 
 // Where the tensor core reads the scales of a block-scaled MMA with M = 128 and
 // scale_vec::4X (one 32-bit TMEM word = the four scales of a line for the MMA's
@@ -89,7 +90,8 @@ struct GemmGeom {
   static constexpr int kStageBytes = kABytes + kBBytes + SF::kSfaBytes + SF::kSfbBytes;
   static constexpr int kSfColsPerStage = SF::kSfaCols + SF::kSfbCols;
   static constexpr int kSmemBytes = SF::kStages * kStageBytes + kMetaBytes +
-                                    kSmemEnds * 8 /* group ends */ + 1024 /* alignment */;
+                                    kSmemEnds * 8 /* group ends */ + kBetaBytes +
+                                    1024 /* alignment */;
   static_assert(kSfCol0 + SF::kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM columns");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128B swizzle");
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -342,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   int* err = reinterpret_cast<int*>(tmem_slot + 1);
   int64_t* s_ends = reinterpret_cast<int64_t*>(smem + S * G::kStageBytes + kMetaBytes);
+  float* s_beta = reinterpret_cast<float*>(s_ends + kSmemEnds);
   // every tile looks its group up: from shared memory when the ends fit
   const int64_t* ends = p.num_groups <= kSmemEnds ? s_ends : p.group_ends;
   if (p.group_ends != nullptr && p.num_groups <= kSmemEnds)
@@ -477,9 +480,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     const bool b_lines = p.b_amax_stride != 0;  // one amax per line of B
     uint32_t t = 0;
+    float* beta = s_beta + (warp - 2) * kEpiCols;  // this warp's column factors
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
       const TileJob job = tile_job(p, ends, tile);
       const int tm = job.tm, tn = job.tn;
+      const int row = tm * kBM + q * 32 + lane;
+      const int col_base = tn * kBN + half * kEpiCols;
+      const bool live = row < p.M && col_base < p.N;
+      // Before the accumulator is ready: alpha = fl(amax_a[row] * fl(1/F_a)) and this
+      // warp's 128 column factors beta = fl(amax_b[col] * fl(1/F_b)), lane l computing
+      // columns 4l .. 4l+3 into shared memory, so that no global load waits behind
+      // the accumulator.
+      const float alpha =
+          live ? __fmul_rn(p.a_amax[(int64_t)job.g * p.a_amax_group_stride +
+                                    (int64_t)row * p.a_amax_stride],
+                           p.a_finv)
+               : 0.f;
+      {
+        const float* b_amax = p.b_amax + (int64_t)job.g * p.b_amax_group_stride;
+        const int c4 = col_base + 4 * lane;
+        float b4[4];
+        // 16-byte loads only where this group's amax row is 16-byte aligned
+        if (b_lines && (reinterpret_cast<uintptr_t>(b_amax) & 15) == 0 && c4 + 4 <= p.N) {
+          const float4 t4 = __ldg(reinterpret_cast<const float4*>(b_amax + c4));
+          b4[0] = t4.x, b4[1] = t4.y, b4[2] = t4.z, b4[3] = t4.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            b4[j] = __ldg(b_amax + (int64_t)max(0, min(c4 + j, p.N - 1)) * p.b_amax_stride);
+        }
+        __syncwarp();  // every lane has read the previous tile's factors
+        sts_v4(beta + 4 * lane, __float_as_uint(__fmul_rn(b4[0], p.b_finv)),
+               __float_as_uint(__fmul_rn(b4[1], p.b_finv)),
+               __float_as_uint(__fmul_rn(b4[2], p.b_finv)),
+               __float_as_uint(__fmul_rn(b4[3], p.b_finv)));
+        __syncwarp();
+      }
       const bool ready = mbar_wait_bounded(acc_full, t & 1);
       if (!ready) *err = 1;
       tc_fence_after();
@@ -496,16 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kEpiCols; ++i) v[i] = 0u;
       }
-
-      const int row = tm * kBM + q * 32 + lane;
-      const int col_base = tn * kBN + half * kEpiCols;
-      if (row >= p.M || col_base >= p.N) continue;
-      const float alpha = __fmul_rn(
-          p.a_amax[(int64_t)job.g * p.a_amax_group_stride + (int64_t)row * p.a_amax_stride],
-          p.a_finv);
-      const float* b_amax = p.b_amax + (int64_t)job.g * p.b_amax_group_stride;
-      // 16-byte loads of beta only where this group's amax row is 16-byte aligned
-      const bool b_vec = b_lines && (reinterpret_cast<uintptr_t>(b_amax) & 15) == 0;
+      if (!live) continue;
       const int nvalid = min(kEpiCols, p.N - col_base);
       const int64_t off = (p.k_grouped ? (int64_t)job.g * p.M * p.N : 0) +
                           (int64_t)row * p.N + col_base;
@@ -516,24 +543,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool vec32 = vec && (d_addr & 31) == 0;
 #pragma unroll
       for (int c = 0; c < kEpiCols / 32; ++c) {
-        const int col0 = col_base + c * 32;
         uint32_t* vc = v + c * 32;
-        // d = fl(fl(acc * alpha) * beta), beta = fl(amax_b[col] * fl(1/F_b))
+        // d = fl(fl(acc * alpha) * beta)
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          float b4[4];
-          if (b_vec && col0 + 32 <= p.N) {
-            const float4 t4 = __ldg(reinterpret_cast<const float4*>(b_amax + col0) + j4);
-            b4[0] = t4.x, b4[1] = t4.y, b4[2] = t4.z, b4[3] = t4.w;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              b4[j] = __ldg(b_amax + (int64_t)min(col0 + 4 * j4 + j, p.N - 1) * p.b_amax_stride);
-          }
+          const float4 b4 = *reinterpret_cast<const float4*>(beta + c * 32 + 4 * j4);
+          const float bj[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            vc[4 * j4 + j] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(vc[4 * j4 + j]), alpha),
-                                                       __fmul_rn(b4[j], p.b_finv)));
+            vc[4 * j4 + j] =
+                __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(vc[4 * j4 + j]), alpha), bj[j]));
         }
         if (p.d_bf16) {
           uint16_t* dst = static_cast<uint16_t*>(p.d) + off + c * 32;

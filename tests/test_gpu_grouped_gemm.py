@@ -194,3 +194,32 @@ def test_grouped_wgrad_tokens_not_multiple_of_256_is_unsupported():
     with pytest.raises(nv.NVFP4Error) as ei:
         _wgrad_run(a_h, a_h, [384], RS, RS, torch.float32)
     assert ei.value.status == nv.NVFP4_ERR_UNSUPPORTED
+
+
+def test_more_groups_than_staged_in_shared_memory():
+    """600 groups (more than the kernel stages in shared memory, so every tile looks
+    its group up in global memory), nearly all empty, in both grouped modes."""
+    n, k = 256, 64
+    ends = [0] * 299 + [128] * 299 + [384, 512]
+    a_h, b_h = _operands(ends[-1], len(ends), n, k, 100, RS)
+    d = _run(a_h, b_h, ends, n, torch.float32, RS)
+    assert nv.nvfp4_device_status(reset=True) == 0
+    exp, dabs = oracle.grouped_gemm(a_h, b_h, ends, n, with_abs=True)
+    got = d.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - exp) <= _bound(k, dabs, exp, False))
+
+    ends = [0] * 300 + [256] * 200 + [768] * 99 + [1024]
+    G, m, n, tokens = len(ends), 128, 256, ends[-1]
+    ca, sa, _ = workloads.nvfp4_operand(m, tokens, 102, row_scaled=True)
+    cb, sb, _ = workloads.nvfp4_operand(n, tokens, 103, row_scaled=True)
+    rng = np.random.default_rng(12)
+    a_h = _host_op(ca.numpy(), sa.numpy(), np.exp(rng.uniform(-2, 2, G * m)).astype(np.float32),
+                   RS, 448.0)
+    b_h = _host_op(cb.numpy(), sb.numpy(), np.exp(rng.uniform(-2, 2, G * n)).astype(np.float32),
+                   RS, 448.0)
+    d = _wgrad_run(a_h, b_h, ends, RS, RS, torch.float32)
+    assert nv.nvfp4_device_status(reset=True) == 0
+    got = d.cpu().numpy().astype(np.float64)
+    exp, dabs = oracle.grouped_gemm_wgrad(a_h, b_h, ends, with_abs=True)
+    assert np.all(got[:300] == 0) and np.all(got[301:500] == 0) and np.all(got[501:599] == 0)
+    assert np.all(np.abs(got - exp) <= _bound(512, dabs, exp, False))
