@@ -283,7 +283,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, what = oracle_sample(args.oracle_rows or 768)
+        v, dt, what = oracle_sample(args.oracle_rows or 2560)
         cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": what,
                "seconds": dt}
 
@@ -623,7 +623,7 @@ def measure_e2e(nv, ops, outs, cfg, stream, dev, steps):
 # DRAM bytes (read + write) of the k_gemm_nvf4 launch of the wgrad call, from the
 # full-size capture in profiles/launches_gemm_fprop16384x28672x8192_wgrad28672x8192x16384.md;
 # to be taken again whenever the GEMM kernel changes.
-GEMM_TRAFFIC_BYTES = 2150.3e6 + 515.0e6
+GEMM_TRAFFIC_BYTES = 1962.3e6 + 516.5e6
 
 
 def l2_flush_buffer(dev):
@@ -755,7 +755,7 @@ def run_gemm(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = gemm_oracle_sample(args.oracle_rows or 64, 7168 if grouped else
+        cpu = gemm_oracle_sample(args.oracle_rows or 512, 7168 if grouped else
                                  workloads.GEMM_SHAPES["fprop"][2])
     flush = l2_flush_buffer(dev)
     for _ in range(args.warmup):
@@ -819,8 +819,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-rows", type=int, default=None,
-                    help="rows of X and dY in the oracle sample (default 768 for the CPU "
-                         "baseline, 128 per step for --impl reference)")
+                    help="rows of X and dY in the oracle sample (default 2560 for the CPU "
+                         "baseline, about 10 s of one Grace core; 128 per step for "
+                         "--impl reference; GEMM workloads: lines of each operand, "
+                         "default 512)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows of X and dY (default 16384; smaller only for profiling captures)")
