@@ -75,6 +75,8 @@ def lib():
         L.oracle_gemm.restype = None
         L.oracle_gemm.argtypes = [u8p, u8p, f32p, C.c_int, C.c_float, u8p, u8p, f32p, C.c_int,
                                   C.c_float, i64, i64, i64, f64p, vp]
+        L.oracle_rht16.restype = C.c_int
+        L.oracle_rht16.argtypes = [f32p, i64, i64, C.c_uint32, f32p]
         _lib = L
     return _lib
 
@@ -321,3 +323,27 @@ def grouped_gemm_wgrad(a, b, group_ends, *, with_abs: bool = False):
                 d[g] = r
         start = e
     return (d, da) if with_abs else d
+
+
+# --------------------------------------------------------------------------
+# Random Hadamard transform of the columnwise operand (reading R14)
+# --------------------------------------------------------------------------
+
+def rht16(x: np.ndarray, dtype: str = "fp32", sign_mask: int = 0) -> np.ndarray:
+    """y = (1/4) H16 diag(s) x along each column, per block of 16 rows, in FP32 (the
+    oracle's reading R14; TE-3206's description names the transform, without a
+    definition).  rows must be a multiple of 16."""
+    xf = as_f32(x, dtype)
+    rows, cols = xf.shape
+    y = np.empty((rows, cols), np.float32)
+    if lib().oracle_rht16(xf, rows, cols, sign_mask & 0xFFFF, y) != 0:
+        raise ValueError("oracle_rht16: rows must be a multiple of 16")
+    return y
+
+
+def quantize_columnwise_rht(x: np.ndarray, dtype: str = "fp32", sign_mask: int = 0, *,
+                            mode: int = ROW_SCALED, bound: float = 448.0,
+                            four_over_six: bool = False):
+    """The columnwise quantization of rht16(x): (codes, scales, amax)."""
+    return quantize(rht16(x, dtype, sign_mask), "fp32", mode=mode, bound=bound,
+                    four_over_six=four_over_six, rowwise=False)["col"]

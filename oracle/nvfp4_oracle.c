@@ -57,6 +57,18 @@
  *       dequantized operands, each element code * decode(scale) * amax /
  *       (bound * 6) as a real number; computed here in FP64, not FP32, because it
  *       is the exact target that the GPU's FP32 accumulation is bounded against.
+ *   R14 random Hadamard transform (RHT) of the columnwise operand: [TE-3206]'s
+ *       description names it only among what that PR leaves out (no RHT or
+ *       four-over-six fusion on the transposed path); its definition comes from
+ *       outside the pages. Along each column, every run of 16 consecutive rows (one
+ *       columnwise 1x16 block) x is replaced by y = (1/4) H16 diag(s) x, where H16 is
+ *       the Sylvester Hadamard matrix (H1 = [1], H2n = [[Hn, Hn], [Hn, -Hn]]; entry
+ *       (i, j) is (-1)^popcount(i & j)), s_j = -1 where bit j of a caller-given
+ *       16-bit sign mask is set and +1 elsewhere, and 1/4 = 1/sqrt(16) makes the
+ *       map orthonormal. FP32 steps: the signs (exact); then the four butterfly
+ *       stages of the fast Walsh-Hadamard transform in natural order (h = 1, 2, 4,
+ *       8: the pair at rows (i, i + h), i & h == 0, becomes (u + v, u - v)); then
+ *       the product with 0.25. The columnwise output is the quantization of y.
  *
  * Parity pins: every function here is checked in tests/ against something other
  * than itself (brute force, library conversions, closed forms, invariants from
@@ -557,4 +569,36 @@ ORACLE_API void oracle_gemm(const uint8_t *a_codes, const uint8_t *a_scales, con
         }
     }
     free(va);
+}
+
+/* ------------------------------------------------------------------------- */
+/* R14 random Hadamard transform of the columnwise operand                    */
+/* ------------------------------------------------------------------------- */
+
+/* y [rows][cols] = the transform of x [rows][cols] along rows, per column, in
+ * blocks of 16 rows (R14).  rows must be a multiple of 16; returns -1 otherwise
+ * and writes nothing. */
+ORACLE_API int oracle_rht16(const float *x, int64_t rows, int64_t cols, uint32_t sign_mask,
+                            float *y)
+{
+    if (rows < 0 || cols < 0 || rows % 16 != 0) return -1;
+    for (int64_t c = 0; c < cols; ++c) {
+        for (int64_t r0 = 0; r0 < rows; r0 += 16) {
+            float v[16];
+            for (int j = 0; j < 16; ++j) {
+                float t = x[(r0 + j) * cols + c];
+                v[j] = ((sign_mask >> j) & 1u) ? -t : t;
+            }
+            for (int h = 1; h < 16; h *= 2) {
+                for (int i = 0; i < 16; ++i) {
+                    if (i & h) continue;
+                    float u = v[i], w = v[i + h];
+                    v[i] = u + w;
+                    v[i + h] = u - w;
+                }
+            }
+            for (int j = 0; j < 16; ++j) y[(r0 + j) * cols + c] = v[j] * 0.25f;
+        }
+    }
+    return 0;
 }

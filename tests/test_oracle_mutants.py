@@ -51,6 +51,15 @@ MUTANTS = {
         ("element_value(b_codes, b_scales, b_amax, b_row_scaled, b_bound, k, j, c)",
          "element_value(b_codes, b_scales, b_amax, b_row_scaled, b_bound, k, i % n, c)"),
     "GEMM divides by bound * 4": ("a / ((double)bound * 6.0)", "a / ((double)bound * 4.0)"),
+    "RHT sign mask read in reverse bit order":
+        ("v[j] = ((sign_mask >> j) & 1u) ? -t : t;", "v[j] = ((sign_mask >> (15 - j)) & 1u) ? -t : t;"),
+    "RHT normalised by 1/2": ("y[(r0 + j) * cols + c] = v[j] * 0.25f;",
+                              "y[(r0 + j) * cols + c] = v[j] * 0.5f;"),
+    "RHT butterfly difference reversed": ("v[i + h] = u - w;", "v[i + h] = w - u;"),
+    "RHT skips the last butterfly stage": ("for (int h = 1; h < 16; h *= 2) {",
+                                           "for (int h = 1; h < 8; h *= 2) {"),
+    "RHT reads the block along a row": ("float t = x[(r0 + j) * cols + c];",
+                                        "float t = x[r0 * cols + (c + j) % cols];"),
 }
 
 
@@ -65,6 +74,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_formats.py"),
                         os.path.join(ROOT, "tests", "test_oracle_recipe.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_gemm.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_gemm.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_rht.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
