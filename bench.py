@@ -345,11 +345,18 @@ SUPPLEMENTARY = {
                 "and per-expert wgrad (dY^T [2048 x tokens] times X^T [7168 x tokens], "
                 "columnwise, per-group column amax, K = each group's tokens); BF16 out; "
                 "FLOPs over the padded rows",
+    "rht": "random Hadamard transform of the wgrad operand dY 16384x28672 BF16 (per column, "
+           "16-row blocks, (1/4) H16 diag(s), sign mask 0x6D2B) into an FP32 workspace, then its "
+           "row-scaled columnwise quantize (per-column amax, bound 448)",
     "gemm": "NVFP4 GEMM consumer of the linear layer: fprop Y[16384x28672] = X[16384x8192] "
             "W[28672x8192]^T (X row-scaled, W per-tensor) and wgrad dW[28672x8192] = "
             "dY^T[28672x16384] X (both row-scaled: bilateral post-scale); random NVFP4 operand "
             "bytes, BF16 output",
 }
+
+
+# the transform's sign mask in the rht workload (the method's random signs, fixed)
+RHT_SIGN_MASK = 0x6D2B
 
 
 def supplementary_oracle_sample(w: str, sample_rows: int):
@@ -375,6 +382,17 @@ def supplementary_oracle_sample(w: str, sample_rows: int):
             nbytes = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + 4 * rows
         dt = time.perf_counter() - t0
         what = f"{sample_rows} tokens x 7168 (one group)"
+    elif w == "rht":
+        g = workloads.generator(workloads.SEEDS["linear"], "cpu")
+        x = workloads.row_lognormal(sample_rows, 28672, g, "cpu")
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        rows, cols = xb.shape
+        t0 = time.perf_counter()
+        oracle.quantize_columnwise_rht(xb, "bf16", RHT_SIGN_MASK, mode=oracle.ROW_SCALED,
+                                       bound=448.0)
+        dt = time.perf_counter() - t0
+        nbytes = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + 4 * cols
+        what = f"the first {sample_rows} rows (tokens) of a 28672-column dY of the same recipe"
     elif w == "weights16x16":
         x = workloads.edge_normal(sample_rows, 8192, torch.bfloat16, "cpu", std=0.02)
         xb = x.view(torch.int16).numpy().view(np.uint16)
@@ -490,6 +508,21 @@ def run_supplementary(args):
         bio = 2 * T * K + M * K // 2 + M * K // 16 + 4 * M + 4 * G
         bmin = bio + 2 * T * K
         kern, kbytes, launches = "whole step (check, grouped amax, expand, rowwise encode)", bio, 4
+        dtype, elems = "bf16", M * K
+    elif w == "rht":
+        x = workloads.linear(dev)[1]
+        M, K = x.shape
+        cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+        col = nv.alloc_out(K, M, K, dev)
+        ws = torch.empty(M * K, dtype=torch.float32, device=dev)
+
+        def step(ev):
+            ev[0].record(stream)
+            nv.nvfp4_quantize_columnwise_rht(x, RHT_SIGN_MASK, cfg, col, ws, stream=stream)
+        bio = 2 * M * K + M * K // 2 + M * K // 16 + 4 * K
+        # the pipeline as built: x read, the FP32 transform written and read twice
+        bmin = bio + 12 * M * K
+        kern, kbytes, launches = "whole step (transform, prep, column amax, encode)", bmin, 4
         dtype, elems = "bf16", M * K
     elif w == "dequant":
         x = workloads.outliers(dev)

@@ -235,6 +235,39 @@ NVFP4_API nvfp4_status nvfp4_grouped_quantize_columnwise(const void *x, int32_t 
                                                const float *noop, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_rht16 -- random Hadamard transform (RHT) of x along its rows, per column and
+ * per block of 16 consecutive rows (one columnwise 1x16 block).  [TE-3206]'s
+ * description names an RHT of the transposed path without defining it; the reading
+ * implemented is y = (1/4) H16 diag(s) x, H16 the Sylvester Hadamard matrix (entry
+ * (i, j) = (-1)^popcount(i & j)), s_j = -1 where bit j of sign_mask is set, else +1.
+ * It is orthonormal, so a wgrad product of two operands transformed with the same
+ * signs equals the product of the originals.  FP32 steps: the signs, the four
+ * natural-order butterfly stages of the fast Walsh-Hadamard transform (h = 1, 2, 4, 8:
+ * rows i and i + h, i & h == 0, become u + v and u - v), then the product with 0.25.
+ *   x [rows][cols] BF16 or FP32; y [rows][cols] FP32, caller-owned.  y may equal x
+ *   when x is FP32 (in place); no other overlap.  rows must be a multiple of 16
+ *   (NVFP4_ERR_UNSUPPORTED otherwise); sign_mask < 2^16 (NVFP4_ERR_INVALID otherwise).
+ */
+NVFP4_API nvfp4_status nvfp4_rht16(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                   uint32_t sign_mask, float *y, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_quantize_columnwise_rht -- the columnwise quantization (as
+ * nvfp4_quantize_columnwise, every cfg) of nvfp4_rht16(x, sign_mask): the wgrad
+ * operand with its 16-row blocks rotated before the amax and the encode.
+ *   workspace: FP32 device buffer of rows * cols elements (ws_bytes at least
+ *   4 * rows * cols) that receives the transformed operand; the call then reads it
+ *   twice (amax pass, encode pass).  noop as for every call: the transform is
+ *   skipped as well.  rows a multiple of 16 (NVFP4_ERR_UNSUPPORTED otherwise).
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_columnwise_rht(const void *x, int32_t in_dtype, int64_t rows,
+                                                     int64_t cols, uint32_t sign_mask,
+                                                     const nvfp4_config *cfg,
+                                                     const nvfp4_out *col, float *workspace,
+                                                     uint64_t ws_bytes, const float *noop,
+                                                     nvfp4_stream_t stream);
+
+/*
  * One operand of nvfp4_gemm: an NVFP4 tensor in K-major layout -- a rowwise output
  * (lines = rows of x) or a columnwise output (lines = columns of x, the operand
  * that enters the GEMM transposed).

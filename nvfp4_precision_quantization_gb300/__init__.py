@@ -28,7 +28,8 @@ __all__ = [
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws", "Operand",
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
-    "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS",
+    "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS", "nvfp4_rht16",
+    "nvfp4_quantize_columnwise_rht",
 ]
 
 NVFP4_OK = 0
@@ -53,6 +54,7 @@ EXPORTED_SYMBOLS = (
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws",
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
+    "nvfp4_rht16", "nvfp4_quantize_columnwise_rht",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -130,6 +132,9 @@ def load_library():
         "nvfp4_grouped_gemm": [vp, vp, vp, i32, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
         "nvfp4_grouped_gemm_wgrad": [vp, vp, vp, i32, i64, i64, i64, vp, i32, vp, C.c_uint64,
                                      vp],
+        "nvfp4_rht16": [vp, i32, i64, i64, C.c_uint32, vp, vp],
+        "nvfp4_quantize_columnwise_rht": [vp, i32, i64, i64, C.c_uint32, vp, vp, vp, C.c_uint64,
+                                          vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -202,6 +207,28 @@ def nvfp4_quantize_columnwise(x: torch.Tensor, cfg: Config, col: Out, noop=None,
     _check(load_library().nvfp4_quantize_columnwise(_ptr(x), _in_dtype(x), rows, cols,
                                                     C.byref(cfg), C.byref(c), _ptr(noop),
                                                     _stream(stream)))
+
+
+def nvfp4_rht16(x: torch.Tensor, sign_mask: int, y: torch.Tensor, stream=None) -> None:
+    """y (FP32, x's shape) = the random Hadamard transform of x along its rows, per
+    column and per 16-row block, with the given 16-bit sign mask."""
+    rows, cols = _matrix(x)
+    if y.dtype != torch.float32 or tuple(y.shape) != (rows, cols) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous float32 tensor of x's shape")
+    _check(load_library().nvfp4_rht16(_ptr(x), _in_dtype(x), rows, cols, sign_mask, _ptr(y),
+                                      _stream(stream)))
+
+
+def nvfp4_quantize_columnwise_rht(x: torch.Tensor, sign_mask: int, cfg: Config, col: Out,
+                                  workspace: torch.Tensor, noop=None, stream=None) -> None:
+    """Columnwise quantization of the transformed x; workspace: a device buffer of at
+    least 4 * rows * cols bytes that receives the transformed operand."""
+    rows, cols = _matrix(x)
+    c = col._c()
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load_library().nvfp4_quantize_columnwise_rht(
+        _ptr(x), _in_dtype(x), rows, cols, sign_mask, C.byref(cfg), C.byref(c), _ptr(workspace),
+        nbytes, _ptr(noop), _stream(stream)))
 
 
 def nvfp4_quantize_both(x: torch.Tensor, cfg: Config, row: Out, col: Out, noop=None,

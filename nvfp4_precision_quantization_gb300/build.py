@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 SOURCES = ["api.cu", "kernels_amax.cu", "kernels_quantize.cu", "kernels_misc.cu",
-           "kernels_gemm.cu"]
+           "kernels_gemm.cu", "kernels_rht.cu"]
 HEADERS = ["device_common.cuh", "internal.h", "tile_pipeline.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

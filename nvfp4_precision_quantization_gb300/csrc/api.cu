@@ -382,6 +382,61 @@ nvfp4_status nvfp4_quantize_both(const void* x, int32_t in_dtype, int64_t rows, 
   return quantize_impl(x, in_dtype, rows, cols, cfg, row, col, noop, stream);
 }
 
+namespace {
+
+nvfp4_status check_rht(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                       uint32_t sign_mask) {
+  nvfp4_status st = check_sizes(rows, cols);
+  if (st != NVFP4_OK) return st;
+  if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
+  if (sign_mask > 0xFFFFu) return fail(NVFP4_ERR_INVALID, "sign_mask must be < 2^16");
+  if (rows % 16 != 0)
+    return fail(NVFP4_ERR_UNSUPPORTED, "the transform needs rows a multiple of 16");
+  if (rows * cols > 0 && x == nullptr) return fail(NVFP4_ERR_INVALID, "x is NULL");
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+nvfp4_status nvfp4_rht16(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                         uint32_t sign_mask, float* y, nvfp4_stream_t stream) {
+  nvfp4_status st = check_rht(x, in_dtype, rows, cols, sign_mask);
+  if (st != NVFP4_OK) return st;
+  if (rows * cols > 0 && y == nullptr) return fail(NVFP4_ERR_INVALID, "y is NULL");
+  if (y != nullptr && static_cast<const void*>(y) == x && in_dtype != NVFP4_IN_FP32)
+    return fail(NVFP4_ERR_INVALID, "y may equal x only for FP32 input");
+  DeviceInfo dev{};
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  RhtArgs a{x, in_dtype == NVFP4_IN_BF16, rows, cols, sign_mask, y, nullptr};
+  cudaError_t e = launch_rht16(a, dev, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "transform launch");
+}
+
+nvfp4_status nvfp4_quantize_columnwise_rht(const void* x, int32_t in_dtype, int64_t rows,
+                                           int64_t cols, uint32_t sign_mask,
+                                           const nvfp4_config* cfg, const nvfp4_out* col,
+                                           float* workspace, uint64_t ws_bytes,
+                                           const float* noop, nvfp4_stream_t stream) {
+  // every argument is checked before the first launch, so a rejected call enqueues nothing
+  nvfp4_status st = check_rht(x, in_dtype, rows, cols, sign_mask);
+  if (st != NVFP4_OK) return st;
+  st = check_config(cfg);
+  if (st != NVFP4_OK) return st;
+  st = check_out(col, "col", cols, rows, cfg->mode == NVFP4_ROW_SCALED ? cols : 1);
+  if (st != NVFP4_OK) return st;
+  const uint64_t need = 4ull * (uint64_t)rows * (uint64_t)cols;
+  if (need > 0 && (workspace == nullptr || ws_bytes < need))
+    return fail(NVFP4_ERR_INVALID, "workspace must hold rows * cols FP32 values");
+  DeviceInfo dev{};
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  RhtArgs a{x, in_dtype == NVFP4_IN_BF16, rows, cols, sign_mask, workspace, noop};
+  cudaError_t e = launch_rht16(a, dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "transform launch");
+  return quantize_impl(workspace, NVFP4_IN_FP32, rows, cols, cfg, nullptr, col, noop, stream);
+}
+
 nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const float* amax,
                               int32_t mode, int64_t rows, int64_t cols, float bound, void* out,
                               int32_t out_dtype, nvfp4_stream_t stream) {

@@ -134,6 +134,18 @@ cudaError_t launch_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, u
 
 // GEMM consumer of two NVFP4 operands (kernels_gemm.cu): D [M][N] = A [M][K] x B [N][K]^T
 // on the dequantized values, K-major codes [lines][K/2] and compact scales [lines][K/16].
+// Random Hadamard transform of x along its rows, per column and per 16-row block,
+// into the FP32 y (kernels_rht.cu); rows a multiple of 16.
+struct RhtArgs {
+  const void* x;
+  bool bf16;
+  int64_t rows, cols;
+  uint32_t sign_mask;
+  float* y;
+  const float* noop;
+};
+cudaError_t launch_rht16(const RhtArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
 struct GemmArgs {
   const uint8_t* a_codes;
   const uint8_t* a_scales;

@@ -1,0 +1,132 @@
+// kernels_rht.cu -- random Hadamard transform (RHT) of the columnwise operand.
+//
+// "NVFP4: enable row-scaled transpose quantization for backward" (TransformerEngine
+// PR #3206, description) names an RHT of the transposed path, among what that PR
+// leaves out, without defining it.  The reading implemented here: per column and per
+// block of 16 consecutive rows (one columnwise 1x16 block), y = (1/4) H16 diag(s) x,
+// with H16 the Sylvester Hadamard matrix (entry (i, j) = (-1)^popcount(i & j)) and
+// s_j = -1 where bit j of the caller's sign mask is set.  FP32 steps, in this
+// order: the signs (exact), the four butterfly stages of the natural-order fast
+// Walsh-Hadamard transform (h = 1, 2, 4, 8: rows i and i + h with i & h == 0 become
+// u + v and u - v), then the product with 0.25.
+//
+// HBM-bound: 2 (BF16) or 4 (FP32) bytes in and 4 bytes out per element, 64 FP32
+// operations per 16 elements.  A thread transforms one 16-row block of V adjacent
+// columns (V = 2 where the row pitch and the base addresses allow 4- or 8-byte
+// accesses, else 1), so each of its 16 loads and 16 stores is part of a warp-wide
+// run of 32 V contiguous elements.  Items (row block, column group) are walked with a
+// grid-stride loop, adjacent threads on adjacent column groups.
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kRhtThreads = 256;
+
+struct RhtKernelArgs {
+  const void* x;
+  float* y;
+  int64_t cols;
+  int64_t groups;  // column groups per row block
+  int64_t items;   // row blocks x column groups
+  uint32_t mask;
+  const float* noop;
+};
+
+// y = (1/4) H16 diag(s) v, in place, in the step order stated above.
+__device__ __forceinline__ void rht16_block(float (&v)[16], uint32_t mask) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((mask >> j) & 1u) << 31));
+#pragma unroll
+  for (int h = 1; h < 16; h *= 2) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      const float u = v[i], w = v[i + h];
+      v[i] = __fadd_rn(u, w);
+      v[i + h] = __fsub_rn(u, w);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+template <bool BF16, int V>
+__global__ void __launch_bounds__(kRhtThreads) k_rht16(RhtKernelArgs a) {
+  if (a.noop != nullptr && *a.noop == 1.0f) return;
+  const int64_t stride = (int64_t)gridDim.x * kRhtThreads;
+  for (int64_t it = (int64_t)blockIdx.x * kRhtThreads + threadIdx.x; it < a.items;
+       it += stride) {
+    const int64_t rb = it / a.groups;
+    const int64_t c0 = (it - rb * a.groups) * V;
+    const int64_t base = rb * 16 * a.cols + c0;  // element (16 rb, c0)
+    float v[V][16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int64_t e = base + r * a.cols;
+      if constexpr (BF16) {
+        const uint16_t* xb = static_cast<const uint16_t*>(a.x);
+        if constexpr (V == 2) {
+          const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(xb + e));
+          v[0][r] = __uint_as_float(w << 16);
+          v[1][r] = __uint_as_float(w & 0xffff0000u);
+        } else {
+          v[0][r] = __uint_as_float((uint32_t)__ldg(xb + e) << 16);
+        }
+      } else {
+        const float* xf = static_cast<const float*>(a.x);
+        if constexpr (V == 2) {
+          const float2 t = __ldg(reinterpret_cast<const float2*>(xf + e));
+          v[0][r] = t.x;
+          v[1][r] = t.y;
+        } else {
+          v[0][r] = __ldg(xf + e);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) rht16_block(v[k], a.mask);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float* yp = a.y + base + r * a.cols;
+      if constexpr (V == 2) {
+        *reinterpret_cast<float2*>(yp) = make_float2(v[0][r], v[1][r]);
+      } else {
+        *yp = v[0][r];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rht16(const RhtArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
+  if (q.rows == 0 || q.cols == 0) return cudaSuccess;
+  const int elem = q.bf16 ? 2 : 4;
+  // two columns per thread: even row pitch, and bases aligned for 2-element accesses
+  const bool pair = (q.cols % 2 == 0) &&
+                    (reinterpret_cast<uintptr_t>(q.x) % (2 * elem) == 0) &&
+                    (reinterpret_cast<uintptr_t>(q.y) % 8 == 0);
+  RhtKernelArgs a{};
+  a.x = q.x;
+  a.y = q.y;
+  a.cols = q.cols;
+  a.groups = pair ? q.cols / 2 : q.cols;
+  a.items = (q.rows / 16) * a.groups;
+  a.mask = q.sign_mask;
+  a.noop = q.noop;
+  const int64_t blocks =
+      std::min<int64_t>((a.items + kRhtThreads - 1) / kRhtThreads, 8LL * dev.num_sms);
+  void (*fn)(RhtKernelArgs);
+  if (q.bf16) fn = pair ? k_rht16<true, 2> : k_rht16<true, 1>;
+  else fn = pair ? k_rht16<false, 2> : k_rht16<false, 1>;
+  fn<<<(unsigned)blocks, kRhtThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -117,3 +117,32 @@ def test_gemm_static_ws_rejects_oversize_without_gpu(lib_path):
     assert nv.nvfp4_gemm_workspace_size(65536, 65536, 65536) > nv.NVFP4_GEMM_STATIC_WS_BYTES
     st = L.nvfp4_gemm_static_ws(R(ok), R(ok), 65536, 65536, 65536, 256, nv.NVFP4_OUT_BF16, None)
     assert st == nv.NVFP4_ERR_UNSUPPORTED and "static workspace" in nv.nvfp4_last_error()
+
+
+def test_rht_host_validation_without_gpu(lib_path):
+    """The transform's argument checks run before any CUDA call."""
+    import nvfp4_precision_quantization_gb300 as nv
+    L = nv.load_library()
+    R = ctypes.byref
+    st = L.nvfp4_rht16(256, nv.NVFP4_IN_BF16, 24, 8, 0, 512, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "multiple of 16" in nv.nvfp4_last_error()
+    st = L.nvfp4_rht16(256, nv.NVFP4_IN_BF16, 32, 8, 0x10000, 512, None)
+    assert st == nv.NVFP4_ERR_INVALID and "sign_mask" in nv.nvfp4_last_error()
+    st = L.nvfp4_rht16(256, 7, 32, 8, 0, 512, None)
+    assert st == nv.NVFP4_ERR_INVALID and "dtype" in nv.nvfp4_last_error()
+    st = L.nvfp4_rht16(256, nv.NVFP4_IN_BF16, 32, 8, 0, 256, None)
+    assert st == nv.NVFP4_ERR_INVALID and "FP32" in nv.nvfp4_last_error()
+    st = L.nvfp4_rht16(256, nv.NVFP4_IN_FP32, 32, 8, 0, None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "y is NULL" in nv.nvfp4_last_error()
+    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+    col = nv._COut(1024, 2048, 4096, None)
+    st = L.nvfp4_quantize_columnwise_rht(256, nv.NVFP4_IN_BF16, 32, 8, 0, R(cfg), R(col), 512,
+                                         4 * 32 * 8 - 4, None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "workspace" in nv.nvfp4_last_error()
+    bad = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 1)
+    st = L.nvfp4_quantize_columnwise_rht(256, nv.NVFP4_IN_BF16, 32, 8, 0, R(bad), R(col), 512,
+                                         4 * 32 * 8, None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "16x16" in nv.nvfp4_last_error()
+    st = L.nvfp4_quantize_columnwise_rht(256, nv.NVFP4_IN_BF16, 40, 8, 0, R(cfg), R(col), 512,
+                                         4 * 40 * 8, None, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED

@@ -1,0 +1,127 @@
+"""Random Hadamard transform of the columnwise operand (GPU, through the C ABI)
+against the oracle's reading R14 (TE-3206's description names the transform without
+defining it): y = (1/4) H16 diag(s) x per column and 16-row block, FP32, bit for bit;
+then the columnwise quantization of y, byte for byte."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_precision_quantization_gb300 as nv
+import oracle
+import workloads
+from gpu_helpers import assert_same, cfg, host_bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _input(rows, cols, dtype, seed):
+    return workloads.seeded_normal(rows, cols, seed=seed, dtype=dtype, device=DEV,
+                                   row_scale_decades=1.0)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(16, 1), (64, 7), (128, 256), (2048, 200), (4096, 514)])
+@pytest.mark.parametrize("mask", [0x0000, 0xFFFF, 0xBEEF])
+def test_transform_matches_oracle_bit_for_bit(dtype, shape, mask):
+    rows, cols = shape
+    x = _input(rows, cols, dtype, seed=rows + cols)
+    y = torch.full((rows, cols), float("nan"), dtype=torch.float32, device=DEV)
+    nv.nvfp4_rht16(x, mask, y)
+    torch.cuda.synchronize()
+    xb, tag = host_bits(x)
+    exp = oracle.rht16(xb, tag, mask)
+    got = y.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), exp.view(np.uint32)), \
+        f"{np.count_nonzero(got.view(np.uint32) != exp.view(np.uint32))} values differ"
+
+
+def test_transform_in_place_and_unaligned_column_offset():
+    x = _input(256, 130, torch.float32, seed=5)
+    xb, _ = host_bits(x)
+    exp = oracle.rht16(xb, "fp32", 0x1234)
+    nv.nvfp4_rht16(x, 0x1234, x)  # in place (FP32 only)
+    # a view that starts one column in: odd offset, so one column per thread
+    base = _input(64, 33, torch.bfloat16, seed=6)
+    sub = torch.empty(64, 32, dtype=torch.bfloat16, device=DEV)
+    sub.copy_(base[:, 1:])
+    y = torch.empty(64, 32, dtype=torch.float32, device=DEV)
+    nv.nvfp4_rht16(sub, 0x00FF, y)
+    torch.cuda.synchronize()
+    assert np.array_equal(x.cpu().numpy().view(np.uint32), exp.view(np.uint32))
+    sb, _ = host_bits(sub)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32),
+                          oracle.rht16(sb, "bf16", 0x00FF).view(np.uint32))
+
+
+CONFIGS = [(nv.NVFP4_ROW_SCALED, 448.0, False), (nv.NVFP4_PER_TENSOR, 256.0, True),
+           (nv.NVFP4_ROW_SCALED, 256.0, True), (nv.NVFP4_PER_TENSOR, 448.0, False)]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(256, 200), (1024, 96), (4096, 130)])
+@pytest.mark.parametrize("conf", CONFIGS)
+def test_quantize_columnwise_rht_matches_oracle(dtype, shape, conf):
+    rows, cols = shape
+    x = _input(rows, cols, dtype, seed=11 + rows)
+    c = cfg(*conf)
+    mask = 0xA5C3
+    col = nv.alloc_out(cols, rows, cols if conf[0] == nv.NVFP4_ROW_SCALED else 1, DEV)
+    ws = torch.empty(rows * cols, dtype=torch.float32, device=DEV)
+    nv.nvfp4_quantize_columnwise_rht(x, mask, c, col, ws)
+    torch.cuda.synchronize()
+    xb, tag = host_bits(x)
+    exp = oracle.quantize_columnwise_rht(xb, tag, mask, mode=conf[0], bound=conf[1],
+                                         four_over_six=conf[2])
+    assert_same(col, exp, f"rht {shape} {conf}")
+
+
+def test_full_size_sampled_columns():
+    """The bench's operand (dY 16384 x 28672 BF16, row-scaled, bound 448) in the bench's
+    launch configuration; 48 columns checked against the oracle (each column's result
+    depends only on that column when the amax is per column)."""
+    rows, cols = 16384, 28672
+    x = workloads.linear(DEV)[1]  # dY of the linear-layer workload
+    assert tuple(x.shape) == (rows, cols)
+    c = cfg(nv.NVFP4_ROW_SCALED, 448.0, False)
+    col = nv.alloc_out(cols, rows, cols, DEV)
+    ws = torch.empty(rows * cols, dtype=torch.float32, device=DEV)
+    nv.nvfp4_quantize_columnwise_rht(x, 0x6D2B, c, col, ws)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(8)
+    pick = np.unique(np.concatenate([[0, 1, cols - 1], rng.integers(0, cols, 45)]))
+    xs = x[:, torch.from_numpy(pick).to(DEV)].contiguous()
+    xb, tag = host_bits(xs)
+    exp = oracle.quantize_columnwise_rht(xb, tag, 0x6D2B, mode=nv.NVFP4_ROW_SCALED, bound=448.0)
+    got = (col.codes[pick].cpu().numpy(), col.scales[pick].cpu().numpy(),
+           col.amax[pick].cpu().numpy())
+    assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1])
+    assert np.array_equal(got[2].view(np.uint32), exp[2].view(np.uint32))
+    del ws
+
+
+def test_noop_writes_nothing_and_empty_shapes():
+    x = _input(64, 32, torch.bfloat16, seed=9)
+    c = cfg(nv.NVFP4_ROW_SCALED, 448.0, False)
+    col = nv.alloc_out(32, 64, 32, DEV, fill=0xA5)
+    col.amax.fill_(-1.0)
+    ws = torch.full((64 * 32,), 3.0, dtype=torch.float32, device=DEV)
+    noop = torch.ones(1, dtype=torch.float32, device=DEV)
+    nv.nvfp4_quantize_columnwise_rht(x, 0x1, c, col, ws, noop=noop)
+    torch.cuda.synchronize()
+    assert bool((col.codes == 0xA5).all()) and bool((col.scales == 0xA5).all())
+    assert bool((col.amax == -1.0).all()) and bool((ws == 3.0).all())
+    # rows == 0: nothing to transform; the amax of the empty columns is 0
+    e = torch.empty(0, 32, dtype=torch.bfloat16, device=DEV)
+    col0 = nv.alloc_out(32, 0, 32, DEV)
+    nv.nvfp4_quantize_columnwise_rht(e, 0x1, c, col0, torch.empty(0, device=DEV))
+    torch.cuda.synchronize()
+    assert bool((col0.amax == 0).all())
+
+
+def test_rows_not_multiple_of_16_rejected():
+    x = _input(40, 8, torch.bfloat16, seed=10)
+    y = torch.empty(40, 8, dtype=torch.float32, device=DEV)
+    with pytest.raises(nv.NVFP4Error) as ei:
+        nv.nvfp4_rht16(x, 0, y)
+    assert ei.value.status == nv.NVFP4_ERR_UNSUPPORTED
