@@ -346,8 +346,8 @@ SUPPLEMENTARY = {
                 "columnwise, per-group column amax, K = each group's tokens); BF16 out; "
                 "FLOPs over the padded rows",
     "rht": "random Hadamard transform of the wgrad operand dY 16384x28672 BF16 (per column, "
-           "16-row blocks, (1/4) H16 diag(s), sign mask 0x6D2B) into an FP32 workspace, then its "
-           "row-scaled columnwise quantize (per-column amax, bound 448)",
+           "16-row blocks, (1/4) H16 diag(s), sign mask 0x6D2B) fused into its row-scaled "
+           "columnwise quantize (per-column amax of the transform, bound 448)",
     "gemm": "NVFP4 GEMM consumer of the linear layer: fprop Y[16384x28672] = X[16384x8192] "
             "W[28672x8192]^T (X row-scaled, W per-tensor) and wgrad dW[28672x8192] = "
             "dY^T[28672x16384] X (both row-scaled: bilateral post-scale); random NVFP4 operand "
@@ -514,15 +514,14 @@ def run_supplementary(args):
         M, K = x.shape
         cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
         col = nv.alloc_out(K, M, K, dev)
-        ws = torch.empty(M * K, dtype=torch.float32, device=dev)
 
         def step(ev):
             ev[0].record(stream)
-            nv.nvfp4_quantize_columnwise_rht(x, RHT_SIGN_MASK, cfg, col, ws, stream=stream)
+            nv.nvfp4_quantize_columnwise_rht(x, RHT_SIGN_MASK, cfg, col, stream=stream)
         bio = 2 * M * K + M * K // 2 + M * K // 16 + 4 * K
-        # the pipeline as built: x read, the FP32 transform written and read twice
-        bmin = bio + 12 * M * K
-        kern, kbytes, launches = "whole step (transform, prep, column amax, encode)", bmin, 4
+        # fused: the amax pass and the encode pass each read x and transform it
+        bmin = bio + 2 * M * K
+        kern, kbytes, launches = "whole step (prep, transformed column amax, encode)", bmin, 3
         dtype, elems = "bf16", M * K
     elif w == "dequant":
         x = workloads.outliers(dev)

@@ -255,10 +255,15 @@ NVFP4_API nvfp4_status nvfp4_rht16(const void *x, int32_t in_dtype, int64_t rows
  * nvfp4_quantize_columnwise_rht -- the columnwise quantization (as
  * nvfp4_quantize_columnwise, every cfg) of nvfp4_rht16(x, sign_mask): the wgrad
  * operand with its 16-row blocks rotated before the amax and the encode.
- *   workspace: FP32 device buffer of rows * cols elements (ws_bytes at least
- *   4 * rows * cols) that receives the transformed operand; the call then reads it
- *   twice (amax pass, encode pass).  noop as for every call: the transform is
- *   skipped as well.  rows a multiple of 16 (NVFP4_ERR_UNSUPPORTED otherwise).
+ *   1x16 blocks (cfg->block_2d == 0): the transform is fused; the amax pass and the
+ *   encode pass each read x and transform the blocks they read, and nothing else is
+ *   written (workspace unused, may be NULL).  col->amax_in, if given, is taken as
+ *   the amax of the transformed operand.
+ *   16x16 blocks: workspace, an FP32 device buffer of rows * cols elements
+ *   (ws_bytes at least 4 * rows * cols), receives the transformed operand, which is
+ *   then quantized from there.
+ *   noop as for every call: the transform is skipped as well.  rows a multiple of 16
+ *   (NVFP4_ERR_UNSUPPORTED otherwise).
  */
 NVFP4_API nvfp4_status nvfp4_quantize_columnwise_rht(const void *x, int32_t in_dtype, int64_t rows,
                                                      int64_t cols, uint32_t sign_mask,

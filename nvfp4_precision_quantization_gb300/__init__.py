@@ -220,12 +220,14 @@ def nvfp4_rht16(x: torch.Tensor, sign_mask: int, y: torch.Tensor, stream=None) -
 
 
 def nvfp4_quantize_columnwise_rht(x: torch.Tensor, sign_mask: int, cfg: Config, col: Out,
-                                  workspace: torch.Tensor, noop=None, stream=None) -> None:
-    """Columnwise quantization of the transformed x; workspace: a device buffer of at
-    least 4 * rows * cols bytes that receives the transformed operand."""
+                                  workspace: Optional[torch.Tensor] = None, noop=None,
+                                  stream=None) -> None:
+    """Columnwise quantization of the transformed x.  1x16 blocks: fused, no
+    workspace.  16x16 blocks: workspace, a device buffer of at least 4 * rows * cols
+    bytes, receives the transformed operand."""
     rows, cols = _matrix(x)
     c = col._c()
-    nbytes = workspace.numel() * workspace.element_size()
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().nvfp4_quantize_columnwise_rht(
         _ptr(x), _in_dtype(x), rows, cols, sign_mask, C.byref(cfg), C.byref(c), _ptr(workspace),
         nbytes, _ptr(noop), _stream(stream)))

@@ -139,7 +139,8 @@ EncodeTiledFn encode_tiled() {
 nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
                            const nvfp4_config* cfg, const nvfp4_out* row, const nvfp4_out* col,
                            const float* noop, cudaStream_t stream,
-                           const int64_t* group_ends = nullptr, int num_groups = 0) {
+                           const int64_t* group_ends = nullptr, int num_groups = 0,
+                           bool rht = false, uint32_t rht_mask = 0) {
   nvfp4_status st;
   if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
   if ((st = check_sizes(rows, cols)) != NVFP4_OK) return st;
@@ -177,6 +178,8 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
   q.noop = noop;
   q.group_ends = group_ends;
   q.num_groups = num_groups;
+  q.rht = rht;
+  q.rht_mask = rht_mask;
   if (row) {
     q.row_codes = row->codes;
     q.row_scales = row->scales;
@@ -245,7 +248,13 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
       return cuda_fail(e, "prep launch");
     }
   }
-  if (am.row_amax || am.col_amax || am.tensor_amax) {
+  if (rht && (am.col_amax || am.tensor_amax)) {
+    // the amax of the transformed columns, computed from x without writing them
+    RhtAmaxArgs ra{x, in == InType::BF16, rows, cols, rht_mask, am.col_amax, am.tensor_amax,
+                   noop};
+    if ((e = launch_rht16_amax(ra, dev, stream)) != cudaSuccess)
+      return cuda_fail(e, "transform amax launch");
+  } else if (am.row_amax || am.col_amax || am.tensor_amax) {
     if ((e = launch_amax(am, dev, stream)) != cudaSuccess) return cuda_fail(e, "amax launch");
   }
   if (q.block_2d && row && col && q.row_amax != q.col_amax) {
@@ -425,6 +434,12 @@ nvfp4_status nvfp4_quantize_columnwise_rht(const void* x, int32_t in_dtype, int6
   if (st != NVFP4_OK) return st;
   st = check_out(col, "col", cols, rows, cfg->mode == NVFP4_ROW_SCALED ? cols : 1);
   if (st != NVFP4_OK) return st;
+  if (!cfg->block_2d) {
+    // fused: the amax pass and the encode pass each transform the blocks they read
+    return quantize_impl(x, in_dtype, rows, cols, cfg, nullptr, col, noop, stream, nullptr, 0,
+                         true, sign_mask);
+  }
+  // 16x16 blocks: the transformed operand is written to the workspace and quantized
   const uint64_t need = 4ull * (uint64_t)rows * (uint64_t)cols;
   if (need > 0 && (workspace == nullptr || ws_bytes < need))
     return fail(NVFP4_ERR_INVALID, "workspace must hold rows * cols FP32 values");

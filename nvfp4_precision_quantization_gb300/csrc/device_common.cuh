@@ -228,6 +228,29 @@ __device__ __forceinline__ float sse8(float err, const float* x, uint32_t codes,
   return err;
 }
 
+// Random Hadamard transform of one 16-value block, in place: v = (1/4) H16 diag(s) v
+// with H16 the Sylvester Hadamard matrix and s_j = -1 where bit j of mask is set.
+// FP32 steps in this order: the signs (exact), the four natural-order butterfly
+// stages (h = 1, 2, 4, 8: entries i and i + h, i & h == 0, become u + v and u - v),
+// then the product with 0.25.
+__device__ __forceinline__ void rht16_block(float (&v)[16], uint32_t mask) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((mask >> j) & 1u) << 31));
+#pragma unroll
+  for (int h = 1; h < 16; h *= 2) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      const float u = v[i], w = v[i + h];
+      v[i] = __fadd_rn(u, w);
+      v[i + h] = __fsub_rn(u, w);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
 // Quantize 16 FP32 values of one block whose max |x| is b: writes the two code
 // words (value k in nibble k) and returns the scale byte.  FOS: four-over-six
 // (needs the line amax a and F_inv for the error of each candidate).

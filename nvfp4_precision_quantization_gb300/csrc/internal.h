@@ -114,6 +114,10 @@ struct QuantArgs {
   // own amax -- col_amax [num_groups][K] (per column) or [num_groups] (per tensor)
   bool col_grouped;
   bool col_grouped_per_tensor;
+  // optional, columnwise only (1x16 blocks): each 16-row block of a column is
+  // replaced by its random Hadamard transform with this sign mask before encoding
+  bool rht;
+  uint32_t rht_mask;
 };
 cudaError_t launch_quantize(const QuantArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
@@ -145,6 +149,18 @@ struct RhtArgs {
   const float* noop;
 };
 cudaError_t launch_rht16(const RhtArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+// Exact amax of the transformed x (never written): col_amax [cols] and / or
+// tensor_amax [1], accumulated by atomic max into zeroed buffers.
+struct RhtAmaxArgs {
+  const void* x;
+  bool bf16;
+  int64_t rows, cols;
+  uint32_t sign_mask;
+  float* col_amax;
+  float* tensor_amax;
+  const float* noop;
+};
+cudaError_t launch_rht16_amax(const RhtAmaxArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 struct GemmArgs {
   const uint8_t* a_codes;

@@ -66,6 +66,7 @@ struct EncodeArgs {
   // grouped columns: col_amax is [G][K] (or [G] with col_grouped_pt), one row per group
   // of ends (multiples of kTileRows); the producer stages each tile's column scales
   int col_grouped, col_grouped_pt;
+  uint32_t rht_mask;  // sign mask of the columnwise transform (RHT kernels only)
   int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
   int col_scale_sectors;  // columnwise scales of four tile rows go out as one 32-byte sector
 };
@@ -339,7 +340,8 @@ __device__ __forceinline__ void rowwise_store_scales(const EncodeArgs& a, int r,
 // ---------------------------------------------------------------- columnwise
 
 // Codes and scales of column pair (cl, cl + 1) over rows [rb0, rb0 + RG).
-template <typename T, int RG, bool FOS, bool B2D, bool LOOP = false, typename M>
+template <typename T, int RG, bool FOS, bool B2D, bool LOOP = false, bool RHT = false,
+          typename M>
 __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m,
                                                 const EncodeArgs& a, int cl, int rb0,
                                                 const int32_t (&coff)[8], float S_t, float A_t,
@@ -432,6 +434,13 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
         b1 = absmax16_f32(x1);
       }
     }
+    if constexpr (RHT) {
+      // the block of each column replaced by its transform; its max from the result
+      rht16_block(x0, a.rht_mask);
+      rht16_block(x1, a.rht_mask);
+      b0 = absmax16_f32(x0);
+      b1 = absmax16_f32(x1);
+    }
     uint32_t s2 = 0;
     float e2 = 0.0f;
     if constexpr (B2D) {
@@ -439,9 +448,11 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
       s2 = m.s2d(sub);
       e2 = m.e2d(sub);
     }
-    sc0 |= encode_block<FOS, B2D, sizeof(T) == 2>(x0, b0, S0, A0, a.F_inv, s2, e2, w0[2 * jb], w0[2 * jb + 1])
+    // SHORT (the BF16 block-max division shortcut) holds only for BF16 block maxima
+    constexpr bool SHORT = sizeof(T) == 2 && !RHT;
+    sc0 |= encode_block<FOS, B2D, SHORT>(x0, b0, S0, A0, a.F_inv, s2, e2, w0[2 * jb], w0[2 * jb + 1])
            << (8 * jb);
-    sc1 |= encode_block<FOS, B2D, sizeof(T) == 2>(x1, b1, S1, A1, a.F_inv, s2, e2, w1[2 * jb], w1[2 * jb + 1])
+    sc1 |= encode_block<FOS, B2D, SHORT>(x1, b1, S1, A1, a.F_inv, s2, e2, w1[2 * jb], w1[2 * jb + 1])
            << (8 * jb);
   }
 }
@@ -636,7 +647,8 @@ struct EncodeSmem {
 // TOUT: codes leave through per-warp shared-memory staging and TMA tensor stores
 // (full lines instead of one 16-byte partial sector per thread); the ring then
 // has 2 stages so that 2 CTAs still fit on an SM.
-template <typename T, bool ROW, bool COL, bool FOS, bool B2D, bool TMA, int OUTM>
+template <typename T, bool ROW, bool COL, bool FOS, bool B2D, bool TMA, int OUTM,
+          bool RHT = false>
 __global__ void __launch_bounds__(kPipeThreads, 2)
     k_encode(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap map_rc,
              const __grid_constant__ CUtensorMap map_cc, EncodeArgs a) {
@@ -1046,7 +1058,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     } else if (COL) {
       uint32_t w0[RG / 8], w1[RG / 8];
       uint32_t sc0, sc1;
-      colwise_compute<T, RG, FOS, B2D, ROW && COL>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1,
+      colwise_compute<T, RG, FOS, B2D, ROW && COL, RHT>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1,
                                                    sc0, sc1);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -1158,6 +1170,16 @@ EncodeFn pick_mode(bool fos, bool b2d, bool tma, int outm) {
   return fos ? pick_io<T, ROW, COL, true, false>(tma, outm) : pick_io<T, ROW, COL, false, false>(tma, outm);
 }
 
+// Columnwise only, 1x16 blocks, each block transformed first.
+template <typename T>
+EncodeFn pick_rht(bool fos, bool tma) {
+  if (fos)
+    return tma ? k_encode<T, false, true, true, false, true, kOutDirect, true>
+               : k_encode<T, false, true, true, false, false, kOutDirect, true>;
+  return tma ? k_encode<T, false, true, false, false, true, kOutDirect, true>
+             : k_encode<T, false, true, false, false, false, kOutDirect, true>;
+}
+
 template <typename T>
 EncodeFn pick_dir(bool row, bool col, bool fos, bool b2d, bool tma, int outm) {
   if (row && col) return pick_mode<T, true, true>(fos, b2d, tma, outm);
@@ -1212,7 +1234,10 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.col_grouped = q.col_grouped ? 1 : 0;
   a.col_grouped_pt = q.col_grouped_per_tensor ? 1 : 0;
   a.in_rows = q.pad_ends != nullptr ? q.in_rows : q.M;
+  a.rht_mask = q.rht_mask;
   if (a.grid.num_tiles == 0) return cudaSuccess;
+  if (q.rht && (row || q.block_2d || q.col_grouped || q.pad_ends != nullptr))
+    return cudaErrorInvalidValue;  // the transform is built for the plain columnwise path
 
   CUtensorMap map, map_rc, map_cc;
   memset(&map_rc, 0, sizeof(map_rc));
@@ -1249,8 +1274,10 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.row_scale_groups = (tout && both && bf16 && a.row_spitch % 32 == 0 &&
                         aligned(q.row_scales, 32)) ? 1 : 0;
 
-  EncodeFn fn = bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, outm)
-                     : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, outm);
+  EncodeFn fn = q.rht ? (bf16 ? pick_rht<uint16_t>(q.four_over_six, tma)
+                              : pick_rht<float>(q.four_over_six, tma))
+               : bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, outm)
+                      : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, outm);
   const int smem = outm == kOutTma ? EncodeSmem<kOutTma>::kBytes
                    : outm == kOutSector ? EncodeSmem<kOutSector>::kBytes
                                         : EncodeSmem<kOutDirect>::kBytes;

@@ -37,25 +37,6 @@ struct RhtKernelArgs {
   const float* noop;
 };
 
-// y = (1/4) H16 diag(s) v, in place, in the step order stated above.
-__device__ __forceinline__ void rht16_block(float (&v)[16], uint32_t mask) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((mask >> j) & 1u) << 31));
-#pragma unroll
-  for (int h = 1; h < 16; h *= 2) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i & h) continue;
-      const float u = v[i], w = v[i + h];
-      v[i] = __fadd_rn(u, w);
-      v[i + h] = __fsub_rn(u, w);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
-}
-
 template <bool BF16, int V>
 __global__ void __launch_bounds__(kRhtThreads) k_rht16(RhtKernelArgs a) {
   if (a.noop != nullptr && *a.noop == 1.0f) return;
@@ -103,15 +84,125 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16(RhtKernelArgs a) {
   }
 }
 
+// Exact amax of the transformed operand without writing it: per column (col_amax,
+// [cols]) or over the tensor (tensor_amax, [1]), into buffers the prep step zeroed.
+// A thread walks kAmaxBlocks consecutive 16-row blocks of its V columns, keeps the
+// running max |y| of each, and ends with one atomic max per column (per-tensor: a
+// warp maximum, one atomic per warp).  Non-negative floats order like their bit
+// patterns, so the atomic works on the bits; the result is the exact max whatever
+// the order.
+constexpr int kAmaxBlocks = 16;
+
+struct RhtAmaxKernelArgs {
+  const void* x;
+  int64_t rows, cols;
+  int64_t groups;  // column groups
+  int64_t chunks;  // runs of kAmaxBlocks row blocks
+  int64_t items;   // chunks x groups
+  uint32_t mask;
+  float* col_amax;
+  float* tensor_amax;
+  const float* noop;
+};
+
+template <bool BF16, int V>
+__global__ void __launch_bounds__(kRhtThreads) k_rht16_amax(RhtAmaxKernelArgs a) {
+  if (a.noop != nullptr && *a.noop == 1.0f) return;
+  const int64_t stride = (int64_t)gridDim.x * kRhtThreads;
+  const int64_t row_blocks = a.rows / 16;
+  float tmax = 0.0f;  // per-tensor: this thread's max over all its items
+  for (int64_t it = (int64_t)blockIdx.x * kRhtThreads + threadIdx.x; it < a.items;
+       it += stride) {
+    const int64_t ch = it / a.groups;
+    const int64_t c0 = (it - ch * a.groups) * V;
+    const int64_t rb1 = min(row_blocks, (ch + 1) * kAmaxBlocks);
+    float cmax[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) cmax[k] = 0.0f;
+    for (int64_t rb = ch * kAmaxBlocks; rb < rb1; ++rb) {
+      const int64_t base = rb * 16 * a.cols + c0;
+      float v[V][16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int64_t e = base + r * a.cols;
+        if constexpr (BF16) {
+          const uint16_t* xb = static_cast<const uint16_t*>(a.x);
+          if constexpr (V == 2) {
+            const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(xb + e));
+            v[0][r] = __uint_as_float(w << 16);
+            v[1][r] = __uint_as_float(w & 0xffff0000u);
+          } else {
+            v[0][r] = __uint_as_float((uint32_t)__ldg(xb + e) << 16);
+          }
+        } else {
+          const float* xf = static_cast<const float*>(a.x);
+          if constexpr (V == 2) {
+            const float2 t = __ldg(reinterpret_cast<const float2*>(xf + e));
+            v[0][r] = t.x;
+            v[1][r] = t.y;
+          } else {
+            v[0][r] = __ldg(xf + e);
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        rht16_block(v[k], a.mask);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) cmax[k] = fmaxf(cmax[k], fabsf(v[k][r]));
+      }
+    }
+    if (a.col_amax != nullptr) {
+#pragma unroll
+      for (int k = 0; k < V; ++k)
+        atomicMax(reinterpret_cast<unsigned int*>(a.col_amax + c0 + k), __float_as_uint(cmax[k]));
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) tmax = fmaxf(tmax, cmax[k]);
+  }
+  if (a.tensor_amax != nullptr) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    if ((threadIdx.x & 31) == 0)
+      atomicMax(reinterpret_cast<unsigned int*>(a.tensor_amax), __float_as_uint(tmax));
+  }
+}
+
+bool pair_ok(const void* x, bool bf16, int64_t cols, const void* y) {
+  const int elem = bf16 ? 2 : 4;
+  return cols % 2 == 0 && reinterpret_cast<uintptr_t>(x) % (2 * elem) == 0 &&
+         (y == nullptr || reinterpret_cast<uintptr_t>(y) % 8 == 0);
+}
+
 }  // namespace
+
+cudaError_t launch_rht16_amax(const RhtAmaxArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
+  if (q.rows == 0 || q.cols == 0) return cudaSuccess;
+  const bool pair = pair_ok(q.x, q.bf16, q.cols, nullptr);
+  RhtAmaxKernelArgs a{};
+  a.x = q.x;
+  a.rows = q.rows;
+  a.cols = q.cols;
+  a.groups = pair ? q.cols / 2 : q.cols;
+  a.chunks = (q.rows / 16 + kAmaxBlocks - 1) / kAmaxBlocks;
+  a.items = a.chunks * a.groups;
+  a.mask = q.sign_mask;
+  a.col_amax = q.col_amax;
+  a.tensor_amax = q.tensor_amax;
+  a.noop = q.noop;
+  const int64_t blocks =
+      std::min<int64_t>((a.items + kRhtThreads - 1) / kRhtThreads, 8LL * dev.num_sms);
+  void (*fn)(RhtAmaxKernelArgs);
+  if (q.bf16) fn = pair ? k_rht16_amax<true, 2> : k_rht16_amax<true, 1>;
+  else fn = pair ? k_rht16_amax<false, 2> : k_rht16_amax<false, 1>;
+  fn<<<(unsigned)blocks, kRhtThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rht16(const RhtArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
   if (q.rows == 0 || q.cols == 0) return cudaSuccess;
-  const int elem = q.bf16 ? 2 : 4;
   // two columns per thread: even row pitch, and bases aligned for 2-element accesses
-  const bool pair = (q.cols % 2 == 0) &&
-                    (reinterpret_cast<uintptr_t>(q.x) % (2 * elem) == 0) &&
-                    (reinterpret_cast<uintptr_t>(q.y) % 8 == 0);
+  const bool pair = pair_ok(q.x, q.bf16, q.cols, q.y);
   RhtKernelArgs a{};
   a.x = q.x;
   a.y = q.y;

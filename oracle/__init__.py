@@ -343,7 +343,7 @@ def rht16(x: np.ndarray, dtype: str = "fp32", sign_mask: int = 0) -> np.ndarray:
 
 def quantize_columnwise_rht(x: np.ndarray, dtype: str = "fp32", sign_mask: int = 0, *,
                             mode: int = ROW_SCALED, bound: float = 448.0,
-                            four_over_six: bool = False):
+                            four_over_six: bool = False, block_2d: bool = False):
     """The columnwise quantization of rht16(x): (codes, scales, amax)."""
     return quantize(rht16(x, dtype, sign_mask), "fp32", mode=mode, bound=bound,
-                    four_over_six=four_over_six, rowwise=False)["col"]
+                    four_over_six=four_over_six, block_2d=block_2d, rowwise=False)["col"]

@@ -136,7 +136,8 @@ def test_rht_host_validation_without_gpu(lib_path):
     assert st == nv.NVFP4_ERR_INVALID and "y is NULL" in nv.nvfp4_last_error()
     cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
     col = nv._COut(1024, 2048, 4096, None)
-    st = L.nvfp4_quantize_columnwise_rht(256, nv.NVFP4_IN_BF16, 32, 8, 0, R(cfg), R(col), 512,
+    tiles = nv.Config(nv.NVFP4_PER_TENSOR, 448.0, 0, 1)  # 16x16 blocks need the workspace
+    st = L.nvfp4_quantize_columnwise_rht(256, nv.NVFP4_IN_BF16, 32, 8, 0, R(tiles), R(col), 512,
                                          4 * 32 * 8 - 4, None, None)
     assert st == nv.NVFP4_ERR_INVALID and "workspace" in nv.nvfp4_last_error()
     bad = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 1)

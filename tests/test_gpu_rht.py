@@ -54,12 +54,15 @@ def test_transform_in_place_and_unaligned_column_offset():
                           oracle.rht16(sb, "bf16", 0x00FF).view(np.uint32))
 
 
-CONFIGS = [(nv.NVFP4_ROW_SCALED, 448.0, False), (nv.NVFP4_PER_TENSOR, 256.0, True),
-           (nv.NVFP4_ROW_SCALED, 256.0, True), (nv.NVFP4_PER_TENSOR, 448.0, False)]
+# (mode, bound, four-over-six, 16x16 blocks); 1x16 blocks take the fused path (the
+# amax and encode passes transform the blocks they read), 16x16 the workspace path
+CONFIGS = [(nv.NVFP4_ROW_SCALED, 448.0, False, False), (nv.NVFP4_PER_TENSOR, 256.0, True, False),
+           (nv.NVFP4_ROW_SCALED, 256.0, True, False), (nv.NVFP4_PER_TENSOR, 448.0, False, False),
+           (nv.NVFP4_PER_TENSOR, 448.0, False, True), (nv.NVFP4_PER_TENSOR, 256.0, True, True)]
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("shape", [(256, 200), (1024, 96), (4096, 130)])
+@pytest.mark.parametrize("shape", [(256, 200), (1024, 96), (4096, 130), (512, 75)])
 @pytest.mark.parametrize("conf", CONFIGS)
 def test_quantize_columnwise_rht_matches_oracle(dtype, shape, conf):
     rows, cols = shape
@@ -67,13 +70,29 @@ def test_quantize_columnwise_rht_matches_oracle(dtype, shape, conf):
     c = cfg(*conf)
     mask = 0xA5C3
     col = nv.alloc_out(cols, rows, cols if conf[0] == nv.NVFP4_ROW_SCALED else 1, DEV)
-    ws = torch.empty(rows * cols, dtype=torch.float32, device=DEV)
+    ws = torch.empty(rows * cols, dtype=torch.float32, device=DEV) if conf[3] else None
     nv.nvfp4_quantize_columnwise_rht(x, mask, c, col, ws)
     torch.cuda.synchronize()
     xb, tag = host_bits(x)
     exp = oracle.quantize_columnwise_rht(xb, tag, mask, mode=conf[0], bound=conf[1],
-                                         four_over_six=conf[2])
+                                         four_over_six=conf[2], block_2d=conf[3])
     assert_same(col, exp, f"rht {shape} {conf}")
+
+
+def test_fused_equals_transform_then_quantize():
+    """The fused call and the two-step composition of the public calls agree byte
+    for byte (the transform into a buffer, then the plain columnwise quantize)."""
+    x = _input(2048, 384, torch.bfloat16, seed=12)
+    c = cfg(nv.NVFP4_ROW_SCALED, 448.0, False)
+    fused = nv.alloc_out(384, 2048, 384, DEV)
+    nv.nvfp4_quantize_columnwise_rht(x, 0x0F0F, c, fused)
+    y = torch.empty(2048, 384, dtype=torch.float32, device=DEV)
+    nv.nvfp4_rht16(x, 0x0F0F, y)
+    two = nv.alloc_out(384, 2048, 384, DEV)
+    nv.nvfp4_quantize_columnwise(y, c, two)
+    torch.cuda.synchronize()
+    for a, b in ((fused.codes, two.codes), (fused.scales, two.scales), (fused.amax, two.amax)):
+        assert torch.equal(a, b)
 
 
 def test_full_size_sampled_columns():
@@ -85,8 +104,7 @@ def test_full_size_sampled_columns():
     assert tuple(x.shape) == (rows, cols)
     c = cfg(nv.NVFP4_ROW_SCALED, 448.0, False)
     col = nv.alloc_out(cols, rows, cols, DEV)
-    ws = torch.empty(rows * cols, dtype=torch.float32, device=DEV)
-    nv.nvfp4_quantize_columnwise_rht(x, 0x6D2B, c, col, ws)
+    nv.nvfp4_quantize_columnwise_rht(x, 0x6D2B, c, col)
     torch.cuda.synchronize()
     rng = np.random.default_rng(8)
     pick = np.unique(np.concatenate([[0, 1, cols - 1], rng.integers(0, cols, 45)]))
@@ -97,7 +115,6 @@ def test_full_size_sampled_columns():
            col.amax[pick].cpu().numpy())
     assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1])
     assert np.array_equal(got[2].view(np.uint32), exp[2].view(np.uint32))
-    del ws
 
 
 def test_noop_writes_nothing_and_empty_shapes():
@@ -107,14 +124,20 @@ def test_noop_writes_nothing_and_empty_shapes():
     col.amax.fill_(-1.0)
     ws = torch.full((64 * 32,), 3.0, dtype=torch.float32, device=DEV)
     noop = torch.ones(1, dtype=torch.float32, device=DEV)
-    nv.nvfp4_quantize_columnwise_rht(x, 0x1, c, col, ws, noop=noop)
+    nv.nvfp4_quantize_columnwise_rht(x, 0x1, c, col, ws, noop=noop)  # fused path
+    t = cfg(nv.NVFP4_PER_TENSOR, 448.0, False, True)  # 16x16: the workspace path
+    col_t = nv.alloc_out(32, 64, 1, DEV, fill=0xA5)
+    col_t.amax.fill_(-1.0)
+    nv.nvfp4_quantize_columnwise_rht(x, 0x1, t, col_t, ws, noop=noop)
     torch.cuda.synchronize()
-    assert bool((col.codes == 0xA5).all()) and bool((col.scales == 0xA5).all())
-    assert bool((col.amax == -1.0).all()) and bool((ws == 3.0).all())
+    for o in (col, col_t):
+        assert bool((o.codes == 0xA5).all()) and bool((o.scales == 0xA5).all())
+        assert bool((o.amax == -1.0).all())
+    assert bool((ws == 3.0).all())
     # rows == 0: nothing to transform; the amax of the empty columns is 0
     e = torch.empty(0, 32, dtype=torch.bfloat16, device=DEV)
     col0 = nv.alloc_out(32, 0, 32, DEV)
-    nv.nvfp4_quantize_columnwise_rht(e, 0x1, c, col0, torch.empty(0, device=DEV))
+    nv.nvfp4_quantize_columnwise_rht(e, 0x1, c, col0)
     torch.cuda.synchronize()
     assert bool((col0.amax == 0).all())
 
