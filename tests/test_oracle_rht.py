@@ -1,8 +1,9 @@
 """Pins for the oracle's random Hadamard transform of the columnwise operand (CPU).
 
 TE-3206's description names the transform, as something that PR leaves out of the
-transposed path, but does not define it; the oracle's reading R14 is y = (1/4) H16 diag(s) x per column and per
-block of 16 rows, H16 the Sylvester Hadamard matrix, in FP32 butterfly steps.  These
+transposed path, but does not define it; the oracle's reading R14 is
+y = (1/4) H16 diag(s) x per column and per block of 16 rows, H16 the Sylvester
+Hadamard matrix, in FP32 butterfly steps.  These
 tests tie oracle.rht16 to facts outside its code: scipy's Hadamard matrix on inputs
 whose products and sums are exact in FP32, the FP64 product within the butterfly's
 rounding bound, orthonormality (the transform applied twice is the identity; the
