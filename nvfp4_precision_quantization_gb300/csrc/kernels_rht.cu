@@ -10,12 +10,20 @@
 // Walsh-Hadamard transform (h = 1, 2, 4, 8: rows i and i + h with i & h == 0 become
 // u + v and u - v), then the product with 0.25.
 //
-// HBM-bound: 2 (BF16) or 4 (FP32) bytes in and 4 bytes out per element, 64 FP32
-// operations per 16 elements.  A thread transforms one 16-row block of V adjacent
-// columns (V = 2 where the row pitch and the base addresses allow 4- or 8-byte
-// accesses, else 1), so each of its 16 loads and 16 stores is part of a warp-wide
-// run of 32 V contiguous elements.  Items (row block, column group) are walked with a
-// grid-stride loop, adjacent threads on adjacent column groups.
+// Two kernels, both HBM-bound, with 64 FP32 operations per 16 elements:
+//   k_rht16       writes the transform to an FP32 buffer: 2 (BF16) or 4 (FP32) bytes
+//                 in and 4 bytes out per element.  It serves nvfp4_rht16 and the
+//                 16x16-block path of the transformed quantize.
+//   k_rht16_amax  reads x once and writes only the exact amax of the transform, per
+//                 column or per tensor.  It is the amax pass of the fused transformed
+//                 quantize, whose encode pass transforms its blocks in registers
+//                 (kernels_quantize.cu).
+// A thread works on V adjacent columns: V = 2 where the row pitch and the base
+// addresses allow 4- or 8-byte accesses, else 1.  So each of its row loads and
+// stores is part of a warp-wide run of 32 V contiguous elements.  Items (row block or
+// run of row blocks, column group) are walked with a grid-stride loop, adjacent
+// threads on adjacent column groups.  Both kernels return at once when the noop flag
+// is set.
 #include <algorithm>
 
 #include "device_common.cuh"
