@@ -148,3 +148,50 @@ def test_rows_not_multiple_of_16_rejected():
     with pytest.raises(nv.NVFP4Error) as ei:
         nv.nvfp4_rht16(x, 0, y)
     assert ei.value.status == nv.NVFP4_ERR_UNSUPPORTED
+
+
+def test_given_amax_is_used_as_the_transform_amax():
+    x = _input(512, 96, torch.bfloat16, seed=13)
+    c = cfg(nv.NVFP4_ROW_SCALED, 448.0, False)
+    ref = nv.alloc_out(96, 512, 96, DEV)
+    nv.nvfp4_quantize_columnwise_rht(x, 0x2468, c, ref)
+    given = nv.alloc_out(96, 512, 96, DEV)
+    given.amax_in = ref.amax.clone()
+    nv.nvfp4_quantize_columnwise_rht(x, 0x2468, c, given)
+    torch.cuda.synchronize()
+    assert torch.equal(given.codes, ref.codes) and torch.equal(given.scales, ref.scales)
+    assert torch.equal(given.amax, ref.amax)
+
+
+def test_wgrad_gemm_on_transformed_operands():
+    """The transform's use: dY and X quantized columnwise, both with the same signs,
+    then dW = dY^T X on the tensor cores.  The result is within the GEMM's derived
+    bound of the oracle's product of the same (oracle-made) operands.  Because the
+    transform is orthonormal, it is also close to the unquantized dY^T X."""
+    from test_gpu_gemm import _bound, _dev_op, _host_op
+    rng = np.random.default_rng(14)
+    tokens, d_out, d_in, mask = 512, 256, 192, 0x5A3C
+    dy = (rng.standard_normal((tokens, d_out)) * np.exp(rng.uniform(-1, 1, (tokens, 1))))
+    x = rng.standard_normal((tokens, d_in)) * 0.5
+    dy_t = torch.from_numpy(dy.astype(np.float32)).to(DEV).to(torch.bfloat16)
+    x_t = torch.from_numpy(x.astype(np.float32)).to(DEV).to(torch.bfloat16)
+    c = cfg(nv.NVFP4_ROW_SCALED, 448.0, False)
+    ops, hosts = [], []
+    for t, lines in ((dy_t, d_out), (x_t, d_in)):
+        o = nv.alloc_out(lines, tokens, lines, DEV)
+        nv.nvfp4_quantize_columnwise_rht(t, mask, c, o)
+        ops.append(o.as_operand(nv.NVFP4_ROW_SCALED, 448.0))
+        tb, tag = host_bits(t)
+        hosts.append(_host_op(*oracle.quantize_columnwise_rht(tb, tag, mask), nv.NVFP4_ROW_SCALED,
+                              448.0))
+    d = torch.empty(d_out, d_in, dtype=torch.float32, device=DEV)
+    nv.nvfp4_gemm(ops[0], ops[1], d)
+    torch.cuda.synchronize()
+    # the GPU's quantized operands are the oracle's, byte for byte
+    for o, h in zip(ops, hosts):
+        assert np.array_equal(o.codes.cpu().numpy(), h["codes"])
+    exact, dabs = oracle.gemm(hosts[0], hosts[1], with_abs=True)
+    got = d.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - exact) <= _bound(tokens, dabs, exact, False))
+    ref = dy_t.float().cpu().numpy().astype(np.float64).T @ x_t.float().cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(got - ref) < 0.2 * np.linalg.norm(ref)
