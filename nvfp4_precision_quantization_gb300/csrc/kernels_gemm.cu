@@ -25,10 +25,12 @@
 //             stage's scales to TMEM (tcgen05.cp) and issues the MMAs (M = 128,
 //             N = 256, K = 64, four per stage), releasing each stage with
 //             tcgen05.commit and the finished accumulator with one more;
-//   warps 2-9 epilogue, two per TMEM lane quarter (128 columns each): copy the
-//             accumulator to registers (tcgen05.ld), hand TMEM back to the MMA
-//             warp at once (the next tile's MMAs overlap the rest), then apply
-//             alpha_i * beta_j, convert and store D.
+//   warps 2-9 epilogue, two per TMEM lane quarter (128 columns each): before the
+//             accumulator is ready, load alpha_i and stage the 128 beta_j in shared
+//             memory; then copy the accumulator to registers (tcgen05.ld), hand
+//             TMEM back to the MMA warp at once (the next tile's MMAs overlap the
+//             rest), apply alpha_i * beta_j, convert and store D in whole 32-byte
+//             sectors.
 // Scales reach the kernel in the layout their TMEM copies want (see SfLayout): a
 // pre-pass (k_sf_layout) rewrites the compact [lines][k/16] scales of both operands
 // into the caller's workspace.
