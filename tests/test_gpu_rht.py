@@ -62,7 +62,9 @@ CONFIGS = [(nv.NVFP4_ROW_SCALED, 448.0, False, False), (nv.NVFP4_PER_TENSOR, 256
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("shape", [(256, 200), (1024, 96), (4096, 130), (512, 75)])
+# (272, 40): a last tile of 16 rows; (16, 8): one block; (512, 75): odd columns
+@pytest.mark.parametrize("shape", [(256, 200), (1024, 96), (4096, 130), (512, 75), (272, 40),
+                                   (16, 8)])
 @pytest.mark.parametrize("conf", CONFIGS)
 def test_quantize_columnwise_rht_matches_oracle(dtype, shape, conf):
     rows, cols = shape
