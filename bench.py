@@ -41,6 +41,14 @@ def bytes_io(rows, cols):
     return 2 * rows * cols + codes + scales + 4 * (rows + cols)
 
 
+def quant_bytes(rows, cols, elem=2, row_scaled=True):
+    """B_io of one two-direction quantize call: x (elem bytes per value) in once, codes
+    and scales of both directions out, and the amax written (a float per line
+    row-scaled, one per direction per-tensor)."""
+    amax = 4 * (rows + cols) if row_scaled else 8
+    return bytes_io(rows, cols) - 4 * (rows + cols) + amax + (elem - 2) * rows * cols
+
+
 def bytes_min(rows, cols):
     """B_io plus the second read of x that a global amax forces (x exceeds on-chip storage)."""
     return bytes_io(rows, cols) + 2 * rows * cols
@@ -53,9 +61,8 @@ def encode_bytes(rows, cols):
 
 # DRAM bytes (read + write) per launch of the encode kernel on this workload, mean of
 # the X and dY launches, from one ncu capture of a full step (dram__bytes_read.sum +
-# dram__bytes_write.sum, L2 left as the step leaves it); the capture and its command
-# are in profiles/traffic_linear_step_x16384x8192_dy16384x28672.md.  To be taken
-# again whenever the encode kernel changes.
+# dram__bytes_write.sum, L2 left as the step leaves it).  To be taken again whenever
+# the encode kernel changes.
 ENCODE_TRAFFIC_BYTES = (312.95e6 + 1352.78e6) / 2
 
 
@@ -87,12 +94,16 @@ class ClockSampler:
         except (OSError, ValueError):
             self.proc = None
             return
+        self.first = threading.Event()
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        # nvidia-smi takes a moment to start: the timed region begins once it samples
+        self.first.wait(timeout=10.0)
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+            self.first.set()
 
     def stop(self):
         if self.proc is None:
@@ -148,37 +159,86 @@ def job_throughput(t_local: float, world: int, units_per_rank_step: float, steps
 
 # ---------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(sample_rows: int, seed: int = 2):
-    """Time the oracle on the first `sample_rows` rows of X and dY (drawn from the
-    same distribution on the CPU), both directions, row-scaled."""
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def timed_strips(jobs, threads: int, min_seconds: float):
+    """Run the callables in `jobs` (one per row strip) on `threads` host threads, all
+    of them once per round, rounds repeated until at least min_seconds have passed.
+    The oracle's C calls release the GIL, so the strips run on separate cores.
+    Returns (seconds, rounds)."""
+    import concurrent.futures as cf
+    rounds, t0 = 0, time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            list(ex.map(lambda f: f(), jobs))
+            rounds += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds:
+                return dt, rounds
+
+
+def prepare_oracle_sample(strip_rows: int, threads: int = 1, seed: int = 2):
+    """`threads` strips of `strip_rows` rows of X and dY (drawn from the same
+    distribution on the CPU) and one job per strip: the single-threaded oracle on that
+    strip, both directions, row-scaled (each strip's column amax is over its own rows,
+    as a data-parallel rank's would be).  Returns (jobs, B_io bytes per round, what)."""
     import numpy as np
     import torch
 
     import oracle
     import workloads
     g = workloads.generator(seed, "cpu")
-    xs = [workloads.row_lognormal(sample_rows, k, g, "cpu") for k in (K_X, K_DY)]
+    rows = strip_rows * threads
+    xs = [workloads.row_lognormal(rows, k, g, "cpu") for k in (K_X, K_DY)]
     bits = [x.view(torch.int16).numpy().view(np.uint16) for x in xs]
-    t0 = time.perf_counter()
-    for b in bits:
-        oracle.quantize(b, "bf16", mode=oracle.ROW_SCALED, bound=448.0)
-    dt = time.perf_counter() - t0
-    nbytes = sum(bytes_io(sample_rows, k) for k in (K_X, K_DY))
-    return nbytes / dt / 1e9, dt, f"first {sample_rows} rows of X and dY, both directions"
+
+    def job(i):
+        parts = [b[i * strip_rows:(i + 1) * strip_rows] for b in bits]
+        return lambda: [oracle.quantize(p, "bf16", mode=oracle.ROW_SCALED, bound=448.0)
+                        for p in parts]
+
+    nbytes = threads * sum(bytes_io(strip_rows, k) for k in (K_X, K_DY))
+    what = (f"{threads} strip(s) of {strip_rows} rows of X and dY, both directions, one "
+            f"thread per strip")
+    return [job(i) for i in range(threads)], nbytes, what
+
+
+def oracle_sample(strip_rows: int, threads: int = 1, min_seconds: float = 0.0, seed: int = 2):
+    """The cpu_baseline object (GB/s of B_io over the rows processed) of the oracle on
+    prepare_oracle_sample's strips, repeated until min_seconds have passed."""
+    jobs, nbytes, what = prepare_oracle_sample(strip_rows, threads, seed)
+    dt, rounds = timed_strips(jobs, threads, min_seconds)
+    return {"value": rounds * nbytes / dt / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "sample": f"{what}, {rounds} round(s)", "seconds": dt}
+
+
+def headline_cpu_baseline(args):
+    """The oracle on all host cores (one row strip per core), and on one core."""
+    cores = host_cores()
+    allc = oracle_sample(args.oracle_rows or 256, threads=cores, min_seconds=10.0)
+    allc["single_core"] = oracle_sample(args.oracle_rows or 256, threads=1, min_seconds=5.0)
+    return allc
 
 
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    sample_rows = args.oracle_rows or 128
-    vals = []
+    cores = host_cores()
+    # one step: every core quantizes its own strip of the workload's rows once
+    jobs, nbytes, what = prepare_oracle_sample(args.oracle_rows or 64, threads=cores)
     for _ in range(args.warmup):
-        oracle_sample(sample_rows)
-    t_all = []
+        timed_strips(jobs, cores, 0.0)
+    vals, t_all = [], []
     for _ in range(args.steps):
-        v, dt, what = oracle_sample(sample_rows)
-        vals.append(v)
+        dt, _ = timed_strips(jobs, cores, 0.0)
+        vals.append(nbytes / dt / 1e9)
         t_all.append(dt)
     value = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
@@ -186,7 +246,7 @@ def run_reference(args):
             "ms_per_step": 1e3 * statistics.median(t_all), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample": what},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": what},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -250,6 +310,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    t_region = time.perf_counter()
     for k in range(K):
         flush.zero_()
         starts[k].record(stream)
@@ -258,7 +319,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    t_region = time.perf_counter() - t_region
     clocks = sampler.stop()
+    clocks["timed_region_s"] = t_region
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     shapes = [t.shape for t in ops]
@@ -283,9 +346,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, what = oracle_sample(args.oracle_rows or 2560)
-        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": what,
-               "seconds": dt}
+        cpu = headline_cpu_baseline(args)
 
     if rank == 0:
         line = {
@@ -348,6 +409,14 @@ SUPPLEMENTARY = {
     "rht": "random Hadamard transform of the wgrad operand dY 16384x28672 BF16 (per column, "
            "16-row blocks, (1/4) H16 diag(s), sign mask 0x6D2B) fused into its row-scaled "
            "columnwise quantize (per-column amax of the transform, bound 448)",
+    "outliers": "X 4096x4096 BF16 N(0,1), 0.1 % of the entries x50: per-tensor then "
+                "row-scaled NVFP4 quantize, both directions, 1x16, bound 448 (each call: "
+                "prep, amax pass, encode; X fits in L2, so its second read comes from L2)",
+    "edge": "non-aligned 4000x5000 N(0,1), in BF16 and in FP32: row-scaled NVFP4 quantize, "
+            "both directions, 1x16, bound 448 (direct stores: the pitches allow no sector "
+            "or TMA stores)",
+    "tiny": "X 256x256 BF16, N(0,1) x per-row factor log-uniform in [1e-2, 1e2]: row-scaled "
+            "NVFP4 quantize, both directions, bound 448 (latency-bound)",
     "gemm": "NVFP4 GEMM consumer of the linear layer: fprop Y[16384x28672] = X[16384x8192] "
             "W[28672x8192]^T (X row-scaled, W per-tensor) and wgrad dW[28672x8192] = "
             "dY^T[28672x16384] X (both row-scaled: bilateral post-scale); random NVFP4 operand "
@@ -359,71 +428,119 @@ SUPPLEMENTARY = {
 RHT_SIGN_MASK = 0x6D2B
 
 
-def supplementary_oracle_sample(w: str, sample_rows: int, min_seconds: float = 10.0):
-    """The oracle (single thread) on the first rows of the workload's input, in the
-    same unit (algorithmic GB/s of the rows processed).  The sample is repeated until
-    at least min_seconds of CPU work have been timed; the rate is over all repetitions."""
+def supplementary_oracle_sample(w: str, strip_rows: int, min_seconds: float = 10.0,
+                                threads: int = 1):
+    """The oracle on `threads` strips of `strip_rows` rows of the workload's input, one
+    host thread per strip (each runs the single-threaded oracle on its own strip), in
+    the workload's unit (algorithmic GB/s of the rows processed).  All strips once make
+    a round; rounds repeat until at least min_seconds have been timed."""
     import numpy as np
     import torch
 
     import oracle
     import workloads
+
+    def bits(t):
+        t = t.contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16), "bf16"
+        return t.numpy(), "fp32"
+
+    n = strip_rows * threads
+    jobs, nbytes = [], 0
     if w in ("moe", "moe-ragged", "moe-col"):
-        x = workloads.seeded_normal(sample_rows, 7168, seed=workloads.SEEDS["moe"] + 1000)
-        xb = x.view(torch.int16).numpy().view(np.uint16)
-        ends = np.array([sample_rows], np.int64)
-        rows, cols = xb.shape
-        if w == "moe-col":
-            def run():
-                oracle.quantize(xb, "bf16", mode=oracle.ROW_SCALED, bound=448.0, rowwise=False)
-            nbytes = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + 4 * cols
-        else:
-            def run():
-                oracle.grouped_quantize_rowwise(xb, "bf16", ends, mode=oracle.PER_TENSOR,
-                                                bound=256.0, four_over_six=True)
-            nbytes = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + 4 * rows
-        what = f"{sample_rows} tokens x 7168 (one group)"
+        xb, _ = bits(workloads.seeded_normal(n, 7168, seed=workloads.SEEDS["moe"] + 1000))
+        ends = np.array([strip_rows], np.int64)
+        cols = 7168
+        for i in range(threads):
+            part = xb[i * strip_rows:(i + 1) * strip_rows]
+            if w == "moe-col":
+                jobs.append(lambda p=part: oracle.quantize(p, "bf16", mode=oracle.ROW_SCALED,
+                                                           bound=448.0, rowwise=False))
+            else:
+                jobs.append(lambda p=part: oracle.grouped_quantize_rowwise(
+                    p, "bf16", ends, mode=oracle.PER_TENSOR, bound=256.0, four_over_six=True))
+        per = 2 * strip_rows * cols + strip_rows * cols // 2 + strip_rows * cols // 16
+        per += 4 * (cols if w == "moe-col" else strip_rows)
+        nbytes = threads * per
+        what = f"{threads} strip(s) of {strip_rows} tokens x 7168 (one group each)"
     elif w == "rht":
         g = workloads.generator(workloads.SEEDS["linear"], "cpu")
-        x = workloads.row_lognormal(sample_rows, 28672, g, "cpu")
-        xb = x.view(torch.int16).numpy().view(np.uint16)
-        rows, cols = xb.shape
-
-        def run():
-            oracle.quantize_columnwise_rht(xb, "bf16", RHT_SIGN_MASK, mode=oracle.ROW_SCALED,
-                                           bound=448.0)
-        nbytes = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + 4 * cols
-        what = f"the first {sample_rows} rows (tokens) of a 28672-column dY of the same recipe"
+        xb, _ = bits(workloads.row_lognormal(n, 28672, g, "cpu"))
+        cols = 28672
+        for i in range(threads):
+            part = xb[i * strip_rows:(i + 1) * strip_rows]
+            jobs.append(lambda p=part: oracle.quantize_columnwise_rht(
+                p, "bf16", RHT_SIGN_MASK, mode=oracle.ROW_SCALED, bound=448.0))
+        nbytes = threads * (2 * strip_rows * cols + strip_rows * cols // 2
+                            + strip_rows * cols // 16 + 4 * cols)
+        what = f"{threads} strip(s) of {strip_rows} rows (tokens) of a 28672-column dY"
     elif w == "weights16x16":
-        x = workloads.edge_normal(sample_rows, 8192, torch.bfloat16, "cpu", std=0.02)
-        xb = x.view(torch.int16).numpy().view(np.uint16)
-        rows, cols = xb.shape
-
-        def run():
-            oracle.quantize(xb, "bf16", mode=oracle.PER_TENSOR, bound=448.0, block_2d=True)
-        nbytes = 2 * rows * cols + 2 * (rows * cols // 2 + rows * cols // 16) + 8
-        what = f"first {sample_rows} rows of the 8192x8192 weights, both directions"
+        xb, _ = bits(workloads.edge_normal(n, 8192, torch.bfloat16, "cpu", std=0.02))
+        cols = 8192
+        for i in range(threads):
+            part = xb[i * strip_rows:(i + 1) * strip_rows]
+            jobs.append(lambda p=part: oracle.quantize(p, "bf16", mode=oracle.PER_TENSOR,
+                                                       bound=448.0, block_2d=True))
+        nbytes = threads * (2 * strip_rows * cols
+                            + 2 * (strip_rows * cols // 2 + strip_rows * cols // 16) + 8)
+        what = f"{threads} strip(s) of {strip_rows} rows of the 8192x8192 weights, both directions"
+    elif w in ("outliers", "edge", "tiny"):
+        if w == "outliers":
+            srcs = [bits(workloads.outliers("cpu")[:n])]
+            modes = (oracle.PER_TENSOR, oracle.ROW_SCALED)
+        elif w == "edge":
+            srcs = [bits(workloads.edge_normal(n, 5000, dt, "cpu"))
+                    for dt in (torch.bfloat16, torch.float32)]
+            modes = (oracle.ROW_SCALED,)
+        else:
+            srcs = [bits(workloads.tiny("cpu")[:n])]
+            modes = (oracle.ROW_SCALED,)
+        for i in range(threads):
+            parts = [(xb[i * strip_rows:(i + 1) * strip_rows], tag) for xb, tag in srcs]
+            jobs.append(lambda ps=parts: [oracle.quantize(p, tag, mode=m, bound=448.0)
+                                          for p, tag in ps for m in modes])
+        for xb, tag in srcs:
+            for m in modes:
+                nbytes += threads * quant_bytes(strip_rows, xb.shape[1], 2 if tag == "bf16" else 4,
+                                                m == oracle.ROW_SCALED)
+        what = (f"{threads} strip(s) of {strip_rows} rows of the workload's input, "
+                "both directions")
     else:  # dequant
-        x = workloads.outliers("cpu")[:sample_rows]
-        xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
-        rows, cols = xb.shape
-        o = oracle.quantize(xb, "bf16", mode=oracle.ROW_SCALED, bound=448.0, columnwise=False)
-        codes, scales, amax = o["row"]
+        xb, _ = bits(workloads.outliers("cpu")[:n])
+        cols = 4096
+        for i in range(threads):
+            part = xb[i * strip_rows:(i + 1) * strip_rows]
+            o = oracle.quantize(part, "bf16", mode=oracle.ROW_SCALED, bound=448.0,
+                                columnwise=False)["row"]
+            jobs.append(lambda o=o: oracle.dequantize(o[0], o[1], o[2], row_scaled=True,
+                                                      rows=strip_rows, cols=cols, bound=448.0,
+                                                      out_dtype="fp32"))
+        nbytes = threads * (strip_rows * cols // 2 + strip_rows * cols // 16 + 4 * strip_rows
+                            + 4 * strip_rows * cols)
+        what = (f"{threads} strip(s) of {strip_rows} rows of the 4096x4096 rowwise "
+                "quantization, to FP32")
+    dt, rounds = timed_strips(jobs, threads, min_seconds)
+    return {"value": rounds * nbytes / dt / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "sample": f"{what}, {rounds} round(s)", "seconds": dt}
 
-        def run():
-            oracle.dequantize(codes, scales, amax, row_scaled=True, rows=rows, cols=cols,
-                              bound=448.0, out_dtype="fp32")
-        nbytes = rows * cols // 2 + rows * cols // 16 + 4 * rows + 4 * rows * cols
-        what = f"first {sample_rows} rows of the 4096x4096 rowwise quantization, to FP32"
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        run()
-        reps += 1
-        dt = time.perf_counter() - t0
-        if dt >= min_seconds:
-            break
-    return {"value": reps * nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{what}, {reps} times", "seconds": dt}
+
+# rows per host thread in the oracle samples of the other rows of the path (the
+# 4096-row inputs are cut into as many strips as there are cores)
+SUPPLEMENTARY_STRIP_ROWS = {"tiny": 16, "outliers": 256, "dequant": 256, "edge": 128}
+
+
+def supplementary_cpu_baseline(w: str, args):
+    """All host cores (one strip each); on the small configs a single core as well."""
+    cores = host_cores()
+    rows = args.oracle_rows or SUPPLEMENTARY_STRIP_ROWS.get(w, 256)
+    if w in ("outliers", "dequant", "tiny"):
+        total = {"tiny": 256}.get(w, 4096)
+        rows = max(1, min(rows, total // cores))
+    r = supplementary_oracle_sample(w, rows, min_seconds=10.0, threads=cores)
+    if w in ("tiny", "outliers", "edge"):
+        r["single_core"] = supplementary_oracle_sample(w, rows, min_seconds=5.0, threads=1)
+    return r
 
 
 def run_supplementary(args):
@@ -531,6 +648,41 @@ def run_supplementary(args):
         bmin = bio + 2 * M * K
         kern, kbytes, launches = "whole step (prep, transformed column amax, encode)", bmin, 3
         dtype, elems = "bf16", M * K
+    elif w in ("outliers", "edge", "tiny"):
+        if w == "outliers":
+            xs = [workloads.outliers(dev)]
+            modes = [nv.NVFP4_PER_TENSOR, nv.NVFP4_ROW_SCALED]
+        elif w == "edge":
+            xs = [workloads.edge_normal(4000, 5000, dt_, dev)
+                  for dt_ in (torch.bfloat16, torch.float32)]
+            modes = [nv.NVFP4_ROW_SCALED]
+        else:
+            xs = [workloads.tiny(dev)]
+            modes = [nv.NVFP4_ROW_SCALED]
+        calls = []
+        for xx in xs:
+            M, K = xx.shape
+            for md in modes:
+                rs_ = md == nv.NVFP4_ROW_SCALED
+                calls.append((xx, nv.Config(md, 448.0, 0, 0),
+                              nv.alloc_out(M, K, M if rs_ else 1, dev),
+                              nv.alloc_out(K, M, K if rs_ else 1, dev),
+                              quant_bytes(M, K, xx.element_size(), rs_)))
+
+        def step(ev):
+            # whole calls (prep, amax pass, encode each); ev[0] precedes the last one
+            for j, (xx, cc, row_, col_, _) in enumerate(calls):
+                if j == len(calls) - 1:
+                    ev[0].record(stream)
+                nv.nvfp4_quantize_both(xx, cc, row_, col_, stream=stream)
+        bio = sum(c_[4] for c_ in calls)
+        # the second read of x (the encode pass after the amax pass) stays in L2 here
+        bmin = bio
+        last = "FP32 " if w == "edge" else "row-scaled " if w == "outliers" else ""
+        kern = f"whole {last}quantize call (prep, amax, encode)"
+        kbytes, launches = calls[-1][4], 3 * len(calls)
+        dtype = "bf16" if w != "edge" else "bf16, f32"
+        elems = sum(c_[0].numel() for c_ in calls)
     elif w == "dequant":
         x = workloads.outliers(dev)
         M, K = x.shape
@@ -556,7 +708,7 @@ def run_supplementary(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = supplementary_oracle_sample(w, args.oracle_rows or 256)
+        cpu = supplementary_cpu_baseline(w, args)
 
     flush = l2_flush_buffer(dev)
     for _ in range(args.warmup):
@@ -572,6 +724,7 @@ def run_supplementary(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    t_region = time.perf_counter()
     for k in range(K_):
         flush.zero_()
         starts[k].record(stream)
@@ -580,7 +733,9 @@ def run_supplementary(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    t_region = time.perf_counter() - t_region
     clocks = sampler.stop()
+    clocks["timed_region_s"] = t_region
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends_)]
     t_total, rate = job_throughput(sum(step_ms) / 1e3, world, bio, K_, dev)
     kern_ms = statistics.mean(m[0].elapsed_time(e) for m, e in zip(mids, ends_))
@@ -660,9 +815,8 @@ def measure_e2e(nv, ops, outs, cfg, stream, dev, steps):
             "overlap": "H2D, quantize and D2H on separate streams"}
 
 
-# DRAM bytes (read + write) of the k_gemm_nvf4 launch of the wgrad call, from the
-# full-size capture in profiles/launches_gemm_fprop16384x28672x8192_wgrad28672x8192x16384.md;
-# to be taken again whenever the GEMM kernel changes.
+# DRAM bytes (read + write) of the k_gemm_nvf4 launch of the wgrad call, from one ncu
+# capture of the full-size step; to be taken again whenever the GEMM kernel changes.
 GEMM_TRAFFIC_BYTES = 1962.3e6 + 516.5e6
 
 
@@ -811,6 +965,7 @@ def run_gemm(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    t_region = time.perf_counter()
     for k_ in range(K_):
         flush.zero_()
         starts[k_].record(stream)
@@ -819,7 +974,9 @@ def run_gemm(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    t_region = time.perf_counter() - t_region
     clocks = sampler.stop()
+    clocks["timed_region_s"] = t_region
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends_)]
     t_total, rate = job_throughput(sum(step_ms) / 1e3, world, flops, K_, dev)
     kern_ms = statistics.mean(m[0].elapsed_time(e) for m, e in zip(mids, ends_))

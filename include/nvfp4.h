@@ -245,7 +245,8 @@ NVFP4_API nvfp4_status nvfp4_grouped_quantize_columnwise(const void *x, int32_t 
  * natural-order butterfly stages of the fast Walsh-Hadamard transform (h = 1, 2, 4, 8:
  * rows i and i + h, i & h == 0, become u + v and u - v), then the product with 0.25.
  *   x [rows][cols] BF16 or FP32; y [rows][cols] FP32, caller-owned.  y may equal x
- *   when x is FP32 (in place); no other overlap.  rows must be a multiple of 16
+ *   when x is FP32 (in place); any other overlap of the two byte ranges is rejected
+ *   (NVFP4_ERR_INVALID, nothing enqueued).  rows must be a multiple of 16
  *   (NVFP4_ERR_UNSUPPORTED otherwise); sign_mask < 2^16 (NVFP4_ERR_INVALID otherwise).
  */
 NVFP4_API nvfp4_status nvfp4_rht16(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
@@ -261,7 +262,8 @@ NVFP4_API nvfp4_status nvfp4_rht16(const void *x, int32_t in_dtype, int64_t rows
  *   the amax of the transformed operand.
  *   16x16 blocks: workspace, an FP32 device buffer of rows * cols elements
  *   (ws_bytes at least 4 * rows * cols), receives the transformed operand, which is
- *   then quantized from there.
+ *   then quantized from there; a workspace that overlaps x or an output buffer is
+ *   rejected (NVFP4_ERR_INVALID, nothing enqueued).
  *   noop as for every call: the transform is skipped as well.  rows a multiple of 16
  *   (NVFP4_ERR_UNSUPPORTED otherwise).
  */
@@ -386,8 +388,25 @@ NVFP4_API const char *nvfp4_last_error(void);
  * nvfp4_device_status -- read (and if reset != 0, clear) the device status word
  * of the current device.  Synchronizes the device; not for use inside graph
  * capture.  *status receives NVFP4_DEVICE_* bits (0 = nothing happened).
+ * Returns NVFP4_ERR_TIMEOUT when the word holds NVFP4_DEVICE_TIMEOUT (a kernel
+ * gave up a bounded wait, so some outputs of the calls since the last reset
+ * are incomplete); *status is filled (and reset, if asked) in that case too.
  */
 NVFP4_API nvfp4_status nvfp4_device_status(int32_t *status, int32_t reset);
+
+/*
+ * nvfp4_selftest_wait_timeout -- diagnostic of the failure path every pipeline
+ * kernel shares (their mbarrier waits are bounded, 2 s): one warp waits on a
+ * shared-memory mbarrier that nothing ever arrives on, bounded by limit_ns
+ * nanoseconds (0 .. 1e9; NVFP4_ERR_INVALID otherwise).  The wait gives up, the
+ * kernel sets NVFP4_DEVICE_TIMEOUT in the status word and returns without
+ * writing *out (device uint32; it would be set to 1 only had the wait
+ * completed).  No copy or tensor-memory allocation is in flight, so the context
+ * stays usable.  A test calls it, then nvfp4_device_status, which returns
+ * NVFP4_ERR_TIMEOUT.
+ */
+NVFP4_API nvfp4_status nvfp4_selftest_wait_timeout(int64_t limit_ns, uint32_t *out,
+                                                   nvfp4_stream_t stream);
 
 /*
  * nvfp4_selftest_convert -- diagnostic: run the device conversions used by the

@@ -26,6 +26,7 @@ __all__ = [
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
+    "nvfp4_selftest_wait_timeout",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws", "Operand",
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
     "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS", "nvfp4_rht16",
@@ -52,6 +53,7 @@ EXPORTED_SYMBOLS = (
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
+    "nvfp4_selftest_wait_timeout",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws",
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
     "nvfp4_rht16", "nvfp4_quantize_columnwise_rht",
@@ -125,6 +127,7 @@ def load_library():
         "nvfp4_grouped_quantize_columnwise": [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp],
         "nvfp4_device_status": [C.POINTER(C.c_int32), i32],
         "nvfp4_selftest_convert": [vp, i64, vp, vp, vp],
+        "nvfp4_selftest_wait_timeout": [i64, vp, vp],
         "nvfp4_gemm_workspace_size": [i64, i64, i64, C.POINTER(C.c_uint64)],
         "nvfp4_gemm": [vp, vp, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
         "nvfp4_gemm_static_ws": [vp, vp, i64, i64, i64, vp, i32, vp],
@@ -293,10 +296,23 @@ def nvfp4_grouped_quantize_columnwise(x: torch.Tensor, group_ends: torch.Tensor,
         C.byref(cfg), C.byref(c), _ptr(noop), _stream(stream)))
 
 
-def nvfp4_device_status(reset: bool = False) -> int:
+def nvfp4_device_status(reset: bool = False, raise_on_timeout: bool = False) -> int:
+    """The device status word's NVFP4_DEVICE_* bits.  The C call returns
+    NVFP4_ERR_TIMEOUT when the timeout bit is set; that raises here only with
+    raise_on_timeout, else the bits are returned as for any other state."""
     v = C.c_int32(0)
-    _check(load_library().nvfp4_device_status(C.byref(v), int(reset)))
+    rc = load_library().nvfp4_device_status(C.byref(v), int(reset))
+    if rc != NVFP4_ERR_TIMEOUT or raise_on_timeout:
+        _check(rc)
     return v.value
+
+
+def nvfp4_selftest_wait_timeout(limit_ns: int, out: torch.Tensor, stream=None) -> None:
+    """Run the bounded-wait self-test: a wait that nothing completes, given up after
+    limit_ns nanoseconds (out: one device uint32, left untouched when it gives up)."""
+    if out.dtype not in (torch.int32, torch.uint32) or out.numel() < 1:
+        raise TypeError("out must hold at least one 32-bit integer")
+    _check(load_library().nvfp4_selftest_wait_timeout(int(limit_ns), _ptr(out), _stream(stream)))
 
 
 def nvfp4_selftest_convert(x: torch.Tensor, e2m1_out=None, e4m3_out=None, stream=None) -> None:

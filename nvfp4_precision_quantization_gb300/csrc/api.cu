@@ -43,6 +43,14 @@ nvfp4_status cuda_fail(cudaError_t e, const char* what) {
   return fail(NVFP4_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte (empty ranges and
+// NULL pointers share none).
+bool bytes_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
 struct DevCacheEntry {
   bool ready = false;
   int num_sms = 0;
@@ -412,8 +420,13 @@ nvfp4_status nvfp4_rht16(const void* x, int32_t in_dtype, int64_t rows, int64_t 
   nvfp4_status st = check_rht(x, in_dtype, rows, cols, sign_mask);
   if (st != NVFP4_OK) return st;
   if (rows * cols > 0 && y == nullptr) return fail(NVFP4_ERR_INVALID, "y is NULL");
-  if (y != nullptr && static_cast<const void*>(y) == x && in_dtype != NVFP4_IN_FP32)
-    return fail(NVFP4_ERR_INVALID, "y may equal x only for FP32 input");
+  const uint64_t n = (uint64_t)rows * (uint64_t)cols;
+  const uint64_t x_bytes = n * (in_dtype == NVFP4_IN_FP32 ? 4u : 2u);
+  // a thread reads its 16-row block before writing it, but a neighbouring block of a
+  // partly overlapping y may already have been overwritten: only y == x (FP32) is safe
+  const bool same = static_cast<const void*>(y) == x && in_dtype == NVFP4_IN_FP32;
+  if (!same && bytes_overlap(x, x_bytes, y, 4 * n))
+    return fail(NVFP4_ERR_INVALID, "y overlaps x (only y == x, for FP32 input, is allowed)");
   DeviceInfo dev{};
   st = current_device(&dev);
   if (st != NVFP4_OK) return st;
@@ -443,6 +456,14 @@ nvfp4_status nvfp4_quantize_columnwise_rht(const void* x, int32_t in_dtype, int6
   const uint64_t need = 4ull * (uint64_t)rows * (uint64_t)cols;
   if (need > 0 && (workspace == nullptr || ws_bytes < need))
     return fail(NVFP4_ERR_INVALID, "workspace must hold rows * cols FP32 values");
+  const uint64_t n = (uint64_t)rows * (uint64_t)cols;
+  const uint64_t na = cfg->mode == NVFP4_ROW_SCALED ? (uint64_t)cols : 1u;
+  if (bytes_overlap(workspace, need, x, n * (in_dtype == NVFP4_IN_FP32 ? 4u : 2u)) ||
+      bytes_overlap(workspace, need, col->codes, (uint64_t)cols * (((uint64_t)rows + 1) / 2)) ||
+      bytes_overlap(workspace, need, col->scales, (uint64_t)cols * (((uint64_t)rows + 15) / 16)) ||
+      bytes_overlap(workspace, need, col->amax, 4 * na) ||
+      bytes_overlap(workspace, need, col->amax_in, col->amax_in ? 4 * na : 0))
+    return fail(NVFP4_ERR_INVALID, "workspace overlaps x or an output");
   DeviceInfo dev{};
   st = current_device(&dev);
   if (st != NVFP4_OK) return st;
@@ -889,6 +910,20 @@ nvfp4_status nvfp4_device_status(int32_t* status, int32_t reset) {
     if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int))) != cudaSuccess)
       return cuda_fail(e, "reset status word");
   }
+  if (v & NVFP4_DEVICE_TIMEOUT)
+    return fail(NVFP4_ERR_TIMEOUT, "a kernel gave up a bounded wait; its outputs are incomplete");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_selftest_wait_timeout(int64_t limit_ns, uint32_t* out, nvfp4_stream_t stream) {
+  if (limit_ns < 0 || limit_ns > 1000000000LL)
+    return fail(NVFP4_ERR_INVALID, "limit_ns must lie in [0, 1e9]");
+  if (out == nullptr) return fail(NVFP4_ERR_INVALID, "out is NULL");
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  cudaError_t e = launch_selftest_wait_timeout((uint64_t)limit_ns, out, dev, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return NVFP4_OK;
 }
 

@@ -323,14 +323,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase: gives up after ~2 s (or 2^28 polls) and
-// returns false; the caller then records a timeout and leaves.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Bounded wait on an mbarrier phase: gives up after limit_ns of %globaltimer
+// (2 s unless a self-test passes a shorter limit) or 2^28 polls, whichever comes
+// first, and returns false; the caller then records a timeout and leaves.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 28); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && global_timer_ns() - t0 > 2000000000ull) break;
+    if ((it & 255u) == 255u && global_timer_ns() - t0 > limit_ns) break;
   }
   return false;
 }

@@ -115,7 +115,35 @@ __global__ void k_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, ui
   }
 }
 
+// A bounded wait that runs out: thread 0 initialises a shared-memory mbarrier that
+// expects one arrival, and no thread ever arrives on it.  Every thread of the warp
+// waits on its first phase through the same bounded wait the pipelines use, with
+// the caller's limit.  When the wait gives up, the kernel sets the timeout bit of
+// the status word and returns without writing *out.  Had the wait completed, *out
+// would be set to 1.  Nothing is in flight (no copy, no TMEM), so returning leaves
+// the context clean.
+__global__ void k_selftest_wait_timeout(uint64_t limit_ns, uint32_t* out, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+  if (__all_sync(0xffffffffu, ok)) {
+    if (threadIdx.x == 0) *out = 1u;
+  } else if (threadIdx.x == 0) {
+    raise_status(status, kStatusTimeout);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, uint32_t* out, const DeviceInfo& dev,
+                                         cudaStream_t stream) {
+  k_selftest_wait_timeout<<<1, 32, 0, stream>>>(limit_ns, out, dev.status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dequantize(const DequantArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
   DequantKernelArgs a{};

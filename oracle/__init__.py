@@ -206,6 +206,70 @@ def quantize(x: np.ndarray, dtype: str = "fp32", *, mode: int = ROW_SCALED, boun
     return out
 
 
+def quantize_parallel(x: np.ndarray, dtype: str = "fp32", *, mode: int = ROW_SCALED,
+                      bound: float = 448.0, four_over_six: bool = False, block_2d: bool = False,
+                      rowwise: bool = True, columnwise: bool = True, threads: int | None = None,
+                      strip: int = 64):
+    """quantize() spread over host threads: the same C routine applied to strips of
+    rows (rowwise output) and strips of columns (columnwise output), each strip given
+    the amax the whole tensor has for its lines.
+
+    No arithmetic is added.  Once every line's amax is known, each line (each 16x16
+    tile with block_2d) is quantized on its own.  So a strip quantized with its
+    lines' amax gives exactly the bytes that the whole-tensor call gives for those
+    lines.  tests/test_oracle_parallel.py checks this equality.  The
+    C calls release the GIL (ctypes), so the strips run on as many cores as there
+    are threads.  Returns what quantize() returns."""
+    import concurrent.futures as cf
+
+    xf = as_f32(x, dtype)
+    rows, cols = xf.shape
+    threads = threads or os.cpu_count() or 1
+    strip = max(16, (strip // 16) * 16)  # whole 16-line blocks (16x16 tiles)
+    ra, ca, t = amax(xf, "fp32")
+    rs = mode == ROW_SCALED
+    out = {}
+    jobs = []
+    if rowwise:
+        out["row"] = (np.zeros((rows, (cols + 1) // 2), np.uint8),
+                      np.zeros((rows, (cols + 15) // 16), np.uint8),
+                      ra.copy() if rs else np.array([t], np.float32))
+        rc, rsc, _ = out["row"]
+        for r0 in range(0, rows, strip):
+            r1 = min(rows, r0 + strip)
+            jobs.append(("row", r0, r1, rc[r0:r1], rsc[r0:r1],
+                         ra[r0:r1] if rs else np.array([t], np.float32)))
+    if columnwise:
+        out["col"] = (np.zeros((cols, (rows + 1) // 2), np.uint8),
+                      np.zeros((cols, (rows + 15) // 16), np.uint8),
+                      ca.copy() if rs else np.array([t], np.float32))
+        cc, csc, _ = out["col"]
+        for c0 in range(0, cols, strip):
+            c1 = min(cols, c0 + strip)
+            jobs.append(("col", c0, c1, cc[c0:c1], csc[c0:c1],
+                         ca[c0:c1] if rs else np.array([t], np.float32)))
+
+    def run(job):
+        d, lo, hi, codes, scales, a = job
+        L = lib()
+        if d == "row":
+            part = np.ascontiguousarray(xf[lo:hi])
+            rc_ = L.oracle_quantize(part, hi - lo, cols, mode, bound, int(four_over_six),
+                                    int(block_2d), _ptr(_f32(a)), None, _ptr(codes),
+                                    _ptr(scales), None, None, None, None, None)
+        else:
+            part = np.ascontiguousarray(xf[:, lo:hi])
+            rc_ = L.oracle_quantize(part, rows, hi - lo, mode, bound, int(four_over_six),
+                                    int(block_2d), None, _ptr(_f32(a)), None, None, None,
+                                    _ptr(codes), _ptr(scales), None, None)
+        if rc_ != 0:
+            raise ValueError("oracle_quantize rejected the arguments")
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, jobs))
+    return out
+
+
 def dequantize(codes, scales, amax_vec, *, row_scaled: bool, rows: int, cols: int,
                bound: float = 448.0, out_dtype: str = "fp32") -> np.ndarray:
     codes = np.ascontiguousarray(codes, np.uint8).reshape(-1)

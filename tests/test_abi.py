@@ -147,3 +147,47 @@ def test_rht_host_validation_without_gpu(lib_path):
     st = L.nvfp4_quantize_columnwise_rht(256, nv.NVFP4_IN_BF16, 40, 8, 0, R(cfg), R(col), 512,
                                          4 * 40 * 8, None, None)
     assert st == nv.NVFP4_ERR_UNSUPPORTED
+
+
+def test_overlap_and_selftest_validation_without_gpu(lib_path):
+    """Overlapping buffers of the transform and the self-test's limits are rejected on
+    the host, before any CUDA call."""
+    import nvfp4_precision_quantization_gb300 as nv
+    L = nv.load_library()
+    R = ctypes.byref
+    base = 1 << 20
+    # FP32 x of 32 x 8 values is 1 KB: a y 4 bytes further overlaps it, y == x does not count
+    st = L.nvfp4_rht16(base, nv.NVFP4_IN_FP32, 32, 8, 0, base + 4, None)
+    assert st == nv.NVFP4_ERR_INVALID and "overlaps" in nv.nvfp4_last_error()
+    # BF16 x is 512 bytes: y inside it, or ending inside it, is rejected
+    st = L.nvfp4_rht16(base, nv.NVFP4_IN_BF16, 32, 8, 0, base + 256, None)
+    assert st == nv.NVFP4_ERR_INVALID and "overlaps" in nv.nvfp4_last_error()
+    st = L.nvfp4_rht16(base, nv.NVFP4_IN_BF16, 32, 8, 0, base - 1020, None)
+    assert st == nv.NVFP4_ERR_INVALID and "overlaps" in nv.nvfp4_last_error()
+    # adjacent buffers pass the checks (the call then needs a device)
+    for y in (base + 512, base - 1024):
+        st = L.nvfp4_rht16(base, nv.NVFP4_IN_BF16, 32, 8, 0, y, None)
+        assert st != nv.NVFP4_ERR_INVALID, nv.nvfp4_last_error()
+    st = L.nvfp4_rht16(base, nv.NVFP4_IN_FP32, 32, 8, 0, base, None)
+    assert st != nv.NVFP4_ERR_INVALID, nv.nvfp4_last_error()
+    # 16x16 transform workspace against x and each output
+    tiles = nv.Config(nv.NVFP4_PER_TENSOR, 448.0, 0, 1)
+    ws = 1 << 24
+    need = 4 * 32 * 8
+    for col in (nv._COut(ws + 8, 2 << 20, 3 << 20, None),       # codes inside the workspace
+                nv._COut(2 << 20, ws + need - 1, 3 << 20, None),  # scales start on its last byte
+                nv._COut(2 << 20, 3 << 20, ws, None)):           # amax at its start
+        st = L.nvfp4_quantize_columnwise_rht(base, nv.NVFP4_IN_BF16, 32, 8, 0, R(tiles), R(col),
+                                             ws, need, None, None)
+        assert st == nv.NVFP4_ERR_INVALID and "overlaps" in nv.nvfp4_last_error()
+    col = nv._COut(2 << 20, 3 << 20, 4 << 20, None)
+    st = L.nvfp4_quantize_columnwise_rht(ws + 16, nv.NVFP4_IN_BF16, 32, 8, 0, R(tiles), R(col),
+                                         ws, need, None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "overlaps" in nv.nvfp4_last_error()
+    # the bounded-wait self-test: limit within [0, 1 s], an output pointer
+    st = L.nvfp4_selftest_wait_timeout(2_000_000_000, base, None)
+    assert st == nv.NVFP4_ERR_INVALID and "limit_ns" in nv.nvfp4_last_error()
+    st = L.nvfp4_selftest_wait_timeout(-1, base, None)
+    assert st == nv.NVFP4_ERR_INVALID
+    st = L.nvfp4_selftest_wait_timeout(1000, None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "out" in nv.nvfp4_last_error()

@@ -24,12 +24,35 @@ def test_bytes_io_counts_every_output():
         + 4 * (17 + 33)
 
 
-@pytest.mark.parametrize("w", ["rht", "dequant", "moe-col", "weights16x16"])
-def test_supplementary_oracle_samples_repeat_to_the_minimum_time(w):
-    r = bench.supplementary_oracle_sample(w, 16, min_seconds=0.2)
-    assert KEYS <= set(r) and r["kind"] == "oracle" and r["cores"] == 1
+def test_quant_bytes_by_dtype_and_mode():
+    assert bench.quant_bytes(32, 48) == bench.bytes_io(32, 48)
+    # FP32 input reads 4 bytes per value; per-tensor writes one amax per direction
+    assert bench.quant_bytes(32, 48, 4, True) == bench.bytes_io(32, 48) + 2 * 32 * 48
+    assert bench.quant_bytes(32, 48, 2, False) == bench.bytes_io(32, 48) - 4 * 80 + 8
+
+
+@pytest.mark.parametrize("w", ["rht", "dequant", "moe-col", "weights16x16", "moe", "outliers",
+                               "edge", "tiny"])
+@pytest.mark.parametrize("threads", [1, 2])
+def test_supplementary_oracle_samples_repeat_to_the_minimum_time(w, threads):
+    r = bench.supplementary_oracle_sample(w, 16, min_seconds=0.2, threads=threads)
+    assert KEYS <= set(r) and r["kind"] == "oracle" and r["cores"] == threads
     assert r["seconds"] >= 0.2 and r["value"] > 0 and r["unit"] == "GB/s"
-    assert r["sample"].endswith("times")
+    assert r["sample"].endswith("round(s)") and r["sample"].startswith(f"{threads} strip")
+
+
+def test_headline_oracle_sample_strips():
+    jobs, nbytes, what = bench.prepare_oracle_sample(8, threads=3)
+    assert len(jobs) == 3
+    assert nbytes == 3 * (bench.bytes_io(8, bench.K_X) + bench.bytes_io(8, bench.K_DY))
+    dt, rounds = bench.timed_strips(jobs, 3, 0.1)
+    assert dt >= 0.1 and rounds >= 1
+    r = bench.oracle_sample(8, threads=2, min_seconds=0.1)
+    assert KEYS <= set(r) and r["cores"] == 2
+
+
+def test_host_cores_is_positive():
+    assert bench.host_cores() >= 1
 
 
 def test_gemm_oracle_sample_counts_its_flops():

@@ -75,37 +75,70 @@ def test_outliers_full_with_dequantize(mode):
 
 @pytest.fixture(scope="module")
 def linear_operands():
-    return workloads.linear(DEV)
+    x, dy = workloads.linear(DEV)
+    out = {}
+    for name, t in (("x", x), ("dy", dy)):
+        xb, tag = host_bits(t)
+        out[name] = (t, oracle.amax(xb, tag))  # the oracle's full row / column / tensor amax
+    return out
+
+
+def _check_sampled_lines(x, g, ri, ci, mode, amaxes, bound=448.0, fos=False):
+    """Sampled rows of the rowwise output and sampled columns of the columnwise output
+    against the oracle, one line at a time from the same bytes."""
+    ra, ca, t = amaxes
+    rs = mode == nv.NVFP4_ROW_SCALED
+    _check_sampled_rows(x, g["row"] if rs else _per_line(g["row"], ri),
+                        ri, lambda r, v: ra[r] if rs else np.float32(t), bound, fos)
+    xt_cols = x[:, ci.to(DEV)].t().contiguous()
+    gc = g["col"]
+    codes = gc.codes[ci].cpu().numpy()
+    scales = gc.scales[ci].cpu().numpy()
+    for i, c in enumerate(ci.tolist()):
+        v = _line_f32(xt_cols[i])
+        a = ca[c] if rs else np.float32(t)
+        cc, ss = oracle.quantize_line(v, a, bound, fos)
+        assert np.array_equal(codes[i], cc), ("col codes", c)
+        assert np.array_equal(scales[i], ss), ("col scales", c)
+    if rs:
+        assert np.array_equal(gc.amax.cpu().numpy(), ca)
+    else:
+        assert g["row"].amax.item() == t and gc.amax.item() == t
+
+
+def _per_line(out, ri):
+    """A per-tensor output seen through the row checker: its one amax repeated."""
+    return nv.Out(out.codes, out.scales, out.amax.expand(out.codes.shape[0]))
 
 
 @pytest.mark.parametrize("which", ["x", "dy"])
 def test_linear_operands_sampled(linear_operands, which):
-    x = linear_operands[0] if which == "x" else linear_operands[1]
+    x, amaxes = linear_operands[which]
     rows, cols = x.shape
     c = cfg(nv.NVFP4_ROW_SCALED, 448.0)
     g = gpu_quantize(x, c)
     ri = _sample(rows, 40, 1)
     ci = _sample(cols, 40, 2)
-    _check_sampled_rows(x, g["row"], ri, lambda r, v: np.float32(np.abs(v).max()))
-    xt_cols = x[:, ci.to(DEV)].t().contiguous()
-    gc = g["col"]
-    codes = gc.codes[ci].cpu().numpy()
-    scales = gc.scales[ci].cpu().numpy()
-    amax = gc.amax[ci].cpu().numpy()
-    for i in range(len(ci)):
-        v = _line_f32(xt_cols[i])
-        a = np.float32(np.abs(v).max())
-        cc, ss = oracle.quantize_line(v, a)
-        assert amax[i] == a and np.array_equal(codes[i], cc) and np.array_equal(scales[i], ss)
-    if which == "x":
-        # full amax vectors against the oracle's reduction of the whole matrix
-        xb, tag = host_bits(x)
-        ra, ca, _ = oracle.amax(xb, tag)
-        assert np.array_equal(g["row"].amax.cpu().numpy(), ra)
-        assert np.array_equal(g["col"].amax.cpu().numpy(), ca)
+    _check_sampled_lines(x, g, ri, ci, nv.NVFP4_ROW_SCALED, amaxes)
+    # the full amax vectors against the oracle's reduction of the whole matrix
+    assert np.array_equal(g["row"].amax.cpu().numpy(), amaxes[0])
+    assert np.array_equal(g["col"].amax.cpu().numpy(), amaxes[1])
     # property at any size: every row's block holding the row amax has scale 0x7E
     top = (g["row"].scales == 0x7E).any(dim=1)
     assert bool(top[g["row"].amax > 0].all())
+
+
+@pytest.mark.parametrize("which", ["x", "dy"])
+@pytest.mark.parametrize("mode", [nv.NVFP4_ROW_SCALED, nv.NVFP4_PER_TENSOR])
+@pytest.mark.parametrize("bound", [256.0, 448.0])
+def test_linear_operands_fos_sampled(linear_operands, which, mode, bound):
+    """Four-over-six on the linear-layer operands, both directions: the configuration
+    of the four-over-six benchmark row, each CTA walking 13 (X) or 47 (dY) tiles."""
+    x, amaxes = linear_operands[which]
+    rows, cols = x.shape
+    g = gpu_quantize(x, cfg(mode, bound, fos=True))
+    _check_sampled_lines(x, g, _sample(rows, 32, 5), _sample(cols, 32, 6), mode, amaxes,
+                         bound=bound, fos=True)
 
 
 @pytest.fixture(scope="module")
@@ -156,6 +189,7 @@ def test_moe_ragged_padded_equals_aligned(moe_operands):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_edge_4000x5000_full(dtype):
+    """Without four-over-six; tests/test_gpu_fos_multitile.py has it with."""
     x = workloads.edge_normal(4000, 5000, dtype, DEV)
     for mode in (nv.NVFP4_ROW_SCALED, nv.NVFP4_PER_TENSOR):
         c = cfg(mode, 448.0)
@@ -164,12 +198,15 @@ def test_edge_4000x5000_full(dtype):
         assert_same(g["col"], o["col"], f"col {mode}")
 
 
-def test_edge_8192_blocks_16x16_vs_1x16_sampled():
+@pytest.mark.parametrize("fos", [False, True])
+def test_edge_8192_blocks_16x16_vs_1x16_sampled(fos):
+    """8192 x 8192 per-tensor, 1x16 and 16x16 blocks, with and without four-over-six
+    (4096 tiles: each CTA walks about 13), on strips of 16 rows in both layouts."""
     x = workloads.edge_normal(8192, 8192, torch.bfloat16, DEV, std=0.02)
     xb, tag = host_bits(x)
     _, _, t = oracle.amax(xb, tag)
     for b2d in (False, True):
-        c = cfg(nv.NVFP4_PER_TENSOR, 448.0, False, b2d)
+        c = cfg(nv.NVFP4_PER_TENSOR, 448.0, fos, b2d)
         g = gpu_quantize(x, c)
         assert g["row"].amax.item() == t and g["col"].amax.item() == t
         for r0 in (0, 4096, 8176):
