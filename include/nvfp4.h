@@ -395,6 +395,17 @@ NVFP4_API const char *nvfp4_last_error(void);
 NVFP4_API nvfp4_status nvfp4_device_status(int32_t *status, int32_t reset);
 
 /*
+ * nvfp4_selftest_scale_division -- diagnostic: the encode factor fl(S / sd) as the
+ * encode kernels compute it (a reciprocal and two FMA steps in place of the IEEE
+ * division; the IEEE division for S outside [2^-90, 2^90]), for each of n FP32
+ * values S and each E4M3 byte s8 = 0 .. 126 (sd its value; 0 when sd == 0):
+ * e_out[i * 127 + s8], device buffers.  Lets a test compare every block scale's
+ * quotient with the correctly rounded one.
+ */
+NVFP4_API nvfp4_status nvfp4_selftest_scale_division(const float *S, int64_t n, float *e_out,
+                                                     nvfp4_stream_t stream);
+
+/*
  * nvfp4_selftest_wait_timeout -- diagnostic of the failure path every pipeline
  * kernel shares (their mbarrier waits are bounded, 2 s): one warp waits on a
  * shared-memory mbarrier that nothing ever arrives on, bounded by limit_ns

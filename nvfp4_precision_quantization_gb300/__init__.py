@@ -26,7 +26,7 @@ __all__ = [
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
-    "nvfp4_selftest_wait_timeout",
+    "nvfp4_selftest_wait_timeout", "nvfp4_selftest_scale_division",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws", "Operand",
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
     "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS", "nvfp4_rht16",
@@ -53,7 +53,7 @@ EXPORTED_SYMBOLS = (
     "nvfp4_dequantize", "nvfp4_grouped_amax", "nvfp4_grouped_quantize_rowwise",
     "nvfp4_grouped_quantize_rowwise_padded", "nvfp4_grouped_quantize_columnwise",
     "nvfp4_last_error", "nvfp4_device_status", "nvfp4_selftest_convert",
-    "nvfp4_selftest_wait_timeout",
+    "nvfp4_selftest_wait_timeout", "nvfp4_selftest_scale_division",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws",
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
     "nvfp4_rht16", "nvfp4_quantize_columnwise_rht",
@@ -128,6 +128,7 @@ def load_library():
         "nvfp4_device_status": [C.POINTER(C.c_int32), i32],
         "nvfp4_selftest_convert": [vp, i64, vp, vp, vp],
         "nvfp4_selftest_wait_timeout": [i64, vp, vp],
+        "nvfp4_selftest_scale_division": [vp, i64, vp, vp],
         "nvfp4_gemm_workspace_size": [i64, i64, i64, C.POINTER(C.c_uint64)],
         "nvfp4_gemm": [vp, vp, i64, i64, i64, vp, i32, vp, C.c_uint64, vp],
         "nvfp4_gemm_static_ws": [vp, vp, i64, i64, i64, vp, i32, vp],
@@ -305,6 +306,16 @@ def nvfp4_device_status(reset: bool = False, raise_on_timeout: bool = False) -> 
     if rc != NVFP4_ERR_TIMEOUT or raise_on_timeout:
         _check(rc)
     return v.value
+
+
+def nvfp4_selftest_scale_division(S: torch.Tensor, e_out: torch.Tensor, stream=None) -> None:
+    """e_out[i, s8] = the encode kernels' fl(S[i] / decode(s8)) for s8 = 0 .. 126."""
+    if S.dtype != torch.float32 or not S.is_contiguous():
+        raise TypeError("S must be contiguous float32")
+    if e_out.dtype != torch.float32 or e_out.numel() != S.numel() * 127:
+        raise TypeError("e_out must be float32 with S.numel() * 127 elements")
+    _check(load_library().nvfp4_selftest_scale_division(_ptr(S), S.numel(), _ptr(e_out),
+                                                        _stream(stream)))
 
 
 def nvfp4_selftest_wait_timeout(limit_ns: int, out: torch.Tensor, stream=None) -> None:

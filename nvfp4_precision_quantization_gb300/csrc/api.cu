@@ -915,6 +915,17 @@ nvfp4_status nvfp4_device_status(int32_t* status, int32_t reset) {
   return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_selftest_scale_division(const float* S, int64_t n, float* e_out,
+                                          nvfp4_stream_t stream) {
+  if (n < 0) return fail(NVFP4_ERR_INVALID, "n must be >= 0");
+  if (n > (int64_t(1) << 40)) return fail(NVFP4_ERR_INVALID, "n too large");
+  if (n > 0 && (S == nullptr || e_out == nullptr))
+    return fail(NVFP4_ERR_INVALID, "S and e_out must be non-NULL");
+  cudaError_t e = launch_selftest_scale_division(S, n, e_out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_selftest_wait_timeout(int64_t limit_ns, uint32_t* out, nvfp4_stream_t stream) {
   if (limit_ns < 0 || limit_ns > 1000000000LL)
     return fail(NVFP4_ERR_INVALID, "limit_ns must lie in [0, 1e9]");

@@ -7,9 +7,11 @@
 // for MoE training", torchao PR #9) and the dequantize formula ("Add backward
 // overrides and 1x16 weights to NVFP4 four-over-six", torchao PR #8).
 //
-// Every floating-point step of the recipe is one explicitly rounded FP32
-// operation (__fmul_rn / __fdiv_rn / __fadd_rn / __fsub_rn) so that nothing is
-// contracted into an FMA; the conversions use the sm_100-family cvt
+// Every floating-point step of the recipe is one correctly rounded FP32 operation,
+// as in the oracle: explicitly rounded scalar operations (__fmul_rn / __fadd_rn /
+// __fsub_rn), packed pairs whose products cannot be contracted (mul2_fma), and two
+// divisions replaced by FMA sequences proven to return the correctly rounded
+// quotient (div6_short, div_by_scale).  The conversions use the sm_100-family cvt
 // instructions (RNE, satfinite).
 #pragma once
 
@@ -174,6 +176,23 @@ __device__ __forceinline__ float div6_short(float b) {
   return __fmaf_rn(rem, r, q0);
 }
 
+// fl(S / sd) for a positive E4M3 value sd (the decoded block scale): Markstein's
+// division.  r = rcp.approx(sd) is the correctly rounded reciprocal of each of the
+// 126 positive E4M3 values on sm_100-family GPUs (a device test checks all of
+// them); q0 = fl(S r), the residual S - q0 sd is exact (one FMA), and
+// q1 = fl(q0 + residual r) is the correctly rounded quotient for every FP32
+// significand of S and every E4M3 significand of sd (checked exhaustively in exact
+// integer arithmetic on the CPU).  The argument needs every intermediate in the
+// normal range, so S outside [2^-90, 2^90] takes the IEEE division instead.
+__device__ __forceinline__ float div_by_scale(float S, float sd) {
+  if (!(S >= 0x1p-90f && S <= 0x1p90f)) return __fdiv_rn(S, sd);
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(sd));
+  const float q0 = __fmul_rn(S, r);
+  const float rem = __fmaf_rn(-q0, sd, S);
+  return __fmaf_rn(rem, r, q0);
+}
+
 // SHORT: b is a BF16 value (the block max of BF16 inputs), so fl(b / 6) may use
 // div6_short; otherwise it is an IEEE division.
 template <int T, bool SHORT = false>
@@ -185,7 +204,7 @@ __device__ __forceinline__ BlockEnc block_encode(float b, float S) {
   BlockEnc r;
   r.s8 = e4m3_byte(s32);
   r.sd = e4m3_value(r.s8);
-  r.e = (r.sd == 0.0f) ? 0.0f : __fdiv_rn(S, r.sd);
+  r.e = (r.sd == 0.0f) ? 0.0f : div_by_scale(S, r.sd);
   return r;
 }
 
@@ -214,16 +233,97 @@ __device__ __forceinline__ uint32_t codes8(const float* x, float e) {
   return e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 
-// Running squared error over 8 values and their 8 codes (packed), in order.
-__device__ __forceinline__ float sse8(float err, const float* x, uint32_t codes, float D) {
+// (d0, d1) = (fl(a0 b0), fl(a1 b1)): one fma.rn.f32x2 whose addend is -0.0, which
+// leaves every product as the plain rounded product (a nonzero product plus -0 is
+// itself, +0 + -0 is +0, -0 + -0 is -0).  negz must hold -0.0 at run time (a kernel
+// argument): the compiler then cannot see the addend, so it cannot turn the
+// instruction into a multiply and contract that multiply into the add or subtract
+// that consumes it (it does so with packed multiplies, despite their .rn).
+__device__ __forceinline__ void mul2_fma(float a0, float a1, float b0, float b1, float negz,
+                                         float& d0, float& d1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %6};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(negz));
+}
+
+// (d0, d1) = (fl(a0 - b0), fl(a1 - b1)), one packed subtraction.
+__device__ __forceinline__ void sub2_rn(float a0, float a1, float b0, float b1, float& d0,
+                                        float& d1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// |value| of the four E2M1 codes in nibbles 0..3 of m (their sign bits clear), as
+// FP32, by table lookup: the FP32 pattern of magnitude code k is hi[k] << 24 |
+// lo[k] << 16 with hi = 00 3F 3F 3F 40 40 40 40 and lo = 00 00 80 C0 00 40 80 C0
+// (0, 0.5, 1, 1.5, 2, 3, 4, 6).  Two byte permutes look up the hi and lo bytes of
+// the four codes; one more per value places them, its two low bytes copying the
+// (clear) sign bit of a hi byte.
+__device__ __forceinline__ void e2m1_magnitudes4(uint32_t m, float (&v)[4]) {
+  const uint32_t hi = byte_perm(0x3F3F3F00u, 0x40404040u, m);
+  const uint32_t lo = byte_perm(0xC0800000u, 0xC0804000u, m);
+  v[0] = __uint_as_float(byte_perm(lo, hi, 0x40CCu));
+  v[1] = __uint_as_float(byte_perm(lo, hi, 0x51DDu));
+  v[2] = __uint_as_float(byte_perm(lo, hi, 0x62EEu));
+  v[3] = __uint_as_float(byte_perm(lo, hi, 0x73FFu));
+}
+
+// Four-over-six error of one candidate: err continued over 16 values in order,
+// err = fl(err + fl(d_i * d_i)) with d_i = fl(x_i - fl(v_i * D)), v_i the value of
+// code i (c0: values 0..7, c1: 8..15) and D the candidate's dequantize factor.
+// Two ways of decoding, so that the two candidates load different pipes:
+//   sse16_magnitudes: from |x| (ax) and the codes' magnitudes (table lookup).  The
+//     sign of a nonzero code is the sign of its x, so |x_i| - |v_i D| is d_i up to
+//     its sign, and d_i * d_i is the same.
+//   sse16_signed: from x and the signed values (hardware E2M1 -> FP16 conversion).
+// The dequantized values, the differences and the squares are formed two at a time
+// (packed); the additions stay one at a time, in order.
+__device__ __forceinline__ float sse16_magnitudes(float err, const float* ax, uint32_t c0,
+                                                  uint32_t c1, float D, float negz) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float v0, v1;
-    e2m1x2_values(codes >> (8 * k), v0, v1);
-    float d0 = __fsub_rn(x[2 * k], __fmul_rn(v0, D));
-    err = __fadd_rn(err, __fmul_rn(d0, d0));
-    float d1 = __fsub_rn(x[2 * k + 1], __fmul_rn(v1, D));
-    err = __fadd_rn(err, __fmul_rn(d1, d1));
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w = q < 2 ? c0 : c1;
+    float v[4], g[4], d[4], p[4];
+    e2m1_magnitudes4(((q & 1) ? (w >> 16) : w) & 0x7777u, v);
+    mul2_fma(v[0], v[1], D, D, negz, g[0], g[1]);
+    mul2_fma(v[2], v[3], D, D, negz, g[2], g[3]);
+    sub2_rn(ax[4 * q], ax[4 * q + 1], g[0], g[1], d[0], d[1]);
+    sub2_rn(ax[4 * q + 2], ax[4 * q + 3], g[2], g[3], d[2], d[3]);
+    mul2_fma(d[0], d[1], d[0], d[1], negz, p[0], p[1]);
+    mul2_fma(d[2], d[3], d[2], d[3], negz, p[2], p[3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) err = __fadd_rn(err, p[k]);
+  }
+  return err;
+}
+
+__device__ __forceinline__ float sse16_signed(float err, const float* x, uint32_t c0, uint32_t c1,
+                                              float D, float negz) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w = (q < 2 ? c0 : c1) >> (16 * (q & 1));
+    float v[4], g[4], d[4], p[4];
+    e2m1x2_values(w, v[0], v[1]);
+    e2m1x2_values(w >> 8, v[2], v[3]);
+    mul2_fma(v[0], v[1], D, D, negz, g[0], g[1]);
+    mul2_fma(v[2], v[3], D, D, negz, g[2], g[3]);
+    sub2_rn(x[4 * q], x[4 * q + 1], g[0], g[1], d[0], d[1]);
+    sub2_rn(x[4 * q + 2], x[4 * q + 3], g[2], g[3], d[2], d[3]);
+    mul2_fma(d[0], d[1], d[0], d[1], negz, p[0], p[1]);
+    mul2_fma(d[2], d[3], d[2], d[3], negz, p[2], p[3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) err = __fadd_rn(err, p[k]);
   }
   return err;
 }
@@ -253,10 +353,12 @@ __device__ __forceinline__ void rht16_block(float (&v)[16], uint32_t mask) {
 
 // Quantize 16 FP32 values of one block whose max |x| is b: writes the two code
 // words (value k in nibble k) and returns the scale byte.  FOS: four-over-six
-// (needs the line amax a and F_inv for the error of each candidate).
+// (needs the line amax a and F_inv for the error of each candidate, and negz =
+// -0.0 at run time, see mul2_fma).
 template <bool FOS, bool SHORT = false>
 __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S, float a,
-                                               float F_inv, uint32_t& c0, uint32_t& c1) {
+                                               float F_inv, float negz, uint32_t& c0,
+                                               uint32_t& c1) {
   BlockEnc e6 = block_encode<6, SHORT>(b, S);
   c0 = codes8(x, e6.e);
   c1 = codes8(x + 8, e6.e);
@@ -268,8 +370,11 @@ __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S,
     const uint32_t d1 = codes8(x + 8, e4.e);
     const float D6 = dequant_factor(e6.sd, a, F_inv);
     const float D4 = dequant_factor(e4.sd, a, F_inv);
-    const float err6 = sse8(sse8(0.0f, x, c0, D6), x + 8, c1, D6);
-    const float err4 = sse8(sse8(0.0f, x, d0, D4), x + 8, d1, D4);
+    float ax[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ax[i] = fabsf(x[i]);
+    const float err6 = sse16_magnitudes(0.0f, ax, c0, c1, D6, negz);
+    const float err4 = sse16_signed(0.0f, x, d0, d1, D4, negz);
     if (err4 < err6) {
       c0 = d0;
       c1 = d1;

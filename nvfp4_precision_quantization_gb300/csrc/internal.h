@@ -135,6 +135,8 @@ cudaError_t launch_dequantize(const DequantArgs& a, const DeviceInfo& dev, cudaS
 
 cudaError_t launch_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3,
                                     cudaStream_t stream);
+cudaError_t launch_selftest_scale_division(const float* S, int64_t n, float* e,
+                                           cudaStream_t stream);
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, uint32_t* out, const DeviceInfo& dev,
                                          cudaStream_t stream);
 

@@ -1,4 +1,5 @@
-// kernels_misc.cu -- NVFP4 dequantize and the conversion self-test.
+// kernels_misc.cu -- NVFP4 dequantize and the self-tests (conversions, the division
+// by a block scale, a bounded wait that runs out).
 //
 // Dequantize follows "Add backward overrides and 1x16 weights to NVFP4
 // four-over-six" (torchao PR #8, description): value = code * ((scale * amax) *
@@ -115,6 +116,17 @@ __global__ void k_selftest_convert(const float* in, int64_t n, uint8_t* e2m1, ui
   }
 }
 
+// The encode factor e = fl(S / decode(s8)) as the encode kernels compute it (0 when
+// the scale decodes to 0), for each S[i] and each E4M3 byte s8 = 0 .. 126:
+// e[i * 127 + s8].
+__global__ void k_selftest_scale_division(const float* S, int64_t n, float* e) {
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n * 127;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const float sd = e4m3_value((uint32_t)(g % 127));
+    e[g] = sd == 0.0f ? 0.0f : div_by_scale(S[g / 127], sd);
+  }
+}
+
 // A bounded wait that runs out: thread 0 initialises a shared-memory mbarrier that
 // expects one arrival, and no thread ever arrives on it.  Every thread of the warp
 // waits on its first phase through the same bounded wait the pipelines use, with
@@ -138,6 +150,14 @@ __global__ void k_selftest_wait_timeout(uint64_t limit_ns, uint32_t* out, int* s
 }
 
 }  // namespace
+
+cudaError_t launch_selftest_scale_division(const float* S, int64_t n, float* e,
+                                           cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n * 127 + 255) / 256, 4096);
+  k_selftest_scale_division<<<(unsigned)blocks, 256, 0, stream>>>(S, n, e);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, uint32_t* out, const DeviceInfo& dev,
                                          cudaStream_t stream) {

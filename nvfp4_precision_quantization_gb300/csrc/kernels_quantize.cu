@@ -69,6 +69,7 @@ struct EncodeArgs {
   uint32_t rht_mask;  // sign mask of the columnwise transform (RHT kernels only)
   int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
   int col_scale_sectors;  // columnwise scales of four tile rows go out as one 32-byte sector
+  float neg_zero;         // -0.0, the addend of the four-over-six products (see mul2_fma)
 };
 
 // Per-stage values staged by the producer: the tile's per-row and per-column
@@ -153,13 +154,13 @@ __device__ __forceinline__ void store_tail_words(uint8_t* p, const uint32_t (&w)
 
 template <bool FOS, bool B2D, bool SHORT>
 __device__ __forceinline__ uint32_t encode_block(const float* x, float b, float S, float a,
-                                                 float F_inv, uint32_t s2d, float e2d,
+                                                 float F_inv, float negz, uint32_t s2d, float e2d,
                                                  uint32_t& c0, uint32_t& c1) {
   if constexpr (B2D) {
     codes16(x, e2d, c0, c1);
     return s2d;
   } else {
-    return quantize16<FOS, SHORT>(x, b, S, a, F_inv, c0, c1);
+    return quantize16<FOS, SHORT>(x, b, S, a, F_inv, negz, c0, c1);
   }
 }
 
@@ -218,7 +219,8 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m
         b = absmax16_f32(x);
       }
       uint32_t c0, c1;
-      const uint32_t s8 = quantize16<true, sizeof(T) == 2>(x, b, S, A, a.F_inv, c0, c1);
+      const uint32_t s8 =
+          quantize16<true, sizeof(T) == 2>(x, b, S, A, a.F_inv, a.neg_zero, c0, c1);
 #pragma unroll
       for (int k = 0; k < 2 * NT - 2; ++k) flat[k] = flat[k + 2];
       flat[2 * NT - 2] = c0;
@@ -270,7 +272,8 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m
         s2 = m.s2d(sub);
         e2 = m.e2d(sub);
       }
-      sc[bi] |= encode_block<FOS, B2D, sizeof(T) == 2>(x, b, S, A, a.F_inv, s2, e2, w[bi][2 * j], w[bi][2 * j + 1])
+      sc[bi] |= encode_block<FOS, B2D, sizeof(T) == 2>(x, b, S, A, a.F_inv, a.neg_zero, s2, e2,
+                                                       w[bi][2 * j], w[bi][2 * j + 1])
                 << (8 * j);
     }
   }
@@ -379,9 +382,10 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
         x1[i] = bf16_hi(v[i]);
       }
       uint32_t a0, a1, d0, d1;
-      const uint32_t s0 = quantize16<true, true>(x0, __uint_as_float(mm << 16), S0, A0, a.F_inv, a0, a1);
+      const uint32_t s0 = quantize16<true, true>(x0, __uint_as_float(mm << 16), S0, A0, a.F_inv,
+                                                 a.neg_zero, a0, a1);
       const uint32_t s1 = quantize16<true, true>(x1, __uint_as_float(mm & 0xffff0000u), S1, A1,
-                                                 a.F_inv, d0, d1);
+                                                 a.F_inv, a.neg_zero, d0, d1);
 #pragma unroll
       for (int k = 0; k < RG / 8 - 2; ++k) {
         w0[k] = w0[k + 2];
@@ -450,9 +454,11 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
     }
     // SHORT (the BF16 block-max division shortcut) holds only for BF16 block maxima
     constexpr bool SHORT = sizeof(T) == 2 && !RHT;
-    sc0 |= encode_block<FOS, B2D, SHORT>(x0, b0, S0, A0, a.F_inv, s2, e2, w0[2 * jb], w0[2 * jb + 1])
+    sc0 |= encode_block<FOS, B2D, SHORT>(x0, b0, S0, A0, a.F_inv, a.neg_zero, s2, e2, w0[2 * jb],
+                                         w0[2 * jb + 1])
            << (8 * jb);
-    sc1 |= encode_block<FOS, B2D, SHORT>(x1, b1, S1, A1, a.F_inv, s2, e2, w1[2 * jb], w1[2 * jb + 1])
+    sc1 |= encode_block<FOS, B2D, SHORT>(x1, b1, S1, A1, a.F_inv, a.neg_zero, s2, e2, w1[2 * jb],
+                                         w1[2 * jb + 1])
            << (8 * jb);
   }
 }
@@ -516,7 +522,7 @@ __device__ __forceinline__ void colwise_store(const EncodeArgs& a, int cl, int r
 // its target, by the error summed in row-major order inside the sub-tile).
 template <typename T, bool FOS, typename M>
 __device__ __forceinline__ void subtile_scales(const uint8_t* stage, M& m, float S,
-                                               float amax, float F_inv, int t) {
+                                               float amax, float F_inv, float negz, int t) {
   using G = TileGeo<T>;
   constexpr int SUBC = G::TILEC / 16, NSUB = (kTileRows / 16) * SUBC;
   if (t >= NSUB) return;
@@ -560,8 +566,11 @@ __device__ __forceinline__ void subtile_scales(const uint8_t* stage, M& m, float
       uint32_t c0, c1, d0, d1;
       codes16(x, e6.e, c0, c1);
       codes16(x, e4.e, d0, d1);
-      err6 = sse8(sse8(err6, x, c0, D6), x + 8, c1, D6);
-      err4 = sse8(sse8(err4, x, d0, D4), x + 8, d1, D4);
+      float ax[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) ax[k] = fabsf(x[k]);
+      err6 = sse16_magnitudes(err6, ax, c0, c1, D6, negz);
+      err4 = sse16_signed(err4, x, d0, d1, D4, negz);
     }
     if (err4 < err6) e6 = e4;
   }
@@ -913,7 +922,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       if constexpr (!FOS && sizeof(T) == 2)
         subtile_scales_max(stage, m, ROW ? S_r : S_c, tid);
       else
-        subtile_scales<T, FOS>(stage, m, ROW ? S_r : S_c, ROW ? A_r : A_c, a.F_inv, tid);
+        subtile_scales<T, FOS>(stage, m, ROW ? S_r : S_c, ROW ? A_r : A_c, a.F_inv, a.neg_zero,
+                               tid);
       consumer_sync();
     }
     if (PAIRED && is_row) {
@@ -1223,6 +1233,7 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.row_scaled = q.row_scaled ? 1 : 0;
   a.F = q.bound * 6.0f;
   a.F_inv = 1.0f / a.F;  // correctly rounded IEEE division on the host
+  a.neg_zero = -0.0f;
   a.copy_dst = q.copy_dst;
   a.copy_src = q.copy_src;
   a.noop = q.noop;

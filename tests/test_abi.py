@@ -191,3 +191,12 @@ def test_overlap_and_selftest_validation_without_gpu(lib_path):
     assert st == nv.NVFP4_ERR_INVALID
     st = L.nvfp4_selftest_wait_timeout(1000, None, None)
     assert st == nv.NVFP4_ERR_INVALID and "out" in nv.nvfp4_last_error()
+
+
+def test_scale_division_selftest_validation_without_gpu(lib_path):
+    import nvfp4_precision_quantization_gb300 as nv
+    L = nv.load_library()
+    assert L.nvfp4_selftest_scale_division(1 << 20, -1, 1 << 21, None) == nv.NVFP4_ERR_INVALID
+    assert L.nvfp4_selftest_scale_division(None, 4, 1 << 21, None) == nv.NVFP4_ERR_INVALID
+    assert L.nvfp4_selftest_scale_division(1 << 20, 4, None, None) == nv.NVFP4_ERR_INVALID
+    assert L.nvfp4_selftest_scale_division(None, 0, None, None) == nv.NVFP4_OK
