@@ -57,6 +57,9 @@ struct EncodeArgs {
   int G;
   int full_m, full_n;  // tiles with tm < full_m and tn < full_n lie entirely inside x
   int vec_ok;          // output pitches / bases allow the 16-byte stores
+  // widest store (16, 8, 4, 2 or 1 bytes) that the pitch and base of each output
+  // allow: row codes, row scales, column codes, column scales
+  int rc_g, rs_g, cc_g, cs_g;
   // ragged x into a padded output (grouped tokens): group g's output rows
   // [pad_ends[g-1], pad_ends[g]) take x rows from rag_ends[g-1] on, as many as the
   // group has; the rest of the group's rows are padding (zero codes and scales).
@@ -279,11 +282,44 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m
   }
 }
 
-// Direct stores of one row's codes and scales (no TMA for the outputs).
+// NW code words (4 NW bytes) to p: 16-byte stores when g >= 16, 4-byte stores when
+// g >= 4, else bytes (g: the widest store that the output's pitch and base allow, the
+// same for every thread of a launch).
+template <int NW>
+__device__ __forceinline__ void store_words_g(uint8_t* p, const uint32_t* w, int g) {
+  if (NW % 4 == 0 && g >= 16) {
+#pragma unroll
+    for (int q = 0; q < NW / 4; ++q)
+      stg_v4_cs(p + 16 * q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+  } else if (g >= 4) {
+#pragma unroll
+    for (int q = 0; q < NW; ++q) stg_u32_cs(p + 4 * q, w[q]);
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < 4 * NW; ++i) p[i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+  }
+}
+
+// N (1, 2 or 4) scale bytes to p, one store when g >= N, else bytes; kept in L2 (scale
+// sectors fill up over several tiles).
+template <int N>
+__device__ __forceinline__ void store_scales_g(uint8_t* p, uint32_t s, int g, uint64_t keep) {
+  if (g >= N) {
+    if constexpr (N == 4) stg_u32_keep(p, s, keep);
+    else if constexpr (N == 2) stg_u16_keep(p, s, keep);
+    else p[0] = (uint8_t)s;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) p[i] = (uint8_t)(s >> (8 * i));
+  }
+}
+
+// Direct stores of one row's codes and scales (no TMA for the outputs): whole
+// stores of the widest size the output allows on tiles inside x, bytes on edge tiles.
 template <typename T, int NBOX>
 __device__ __forceinline__ void rowwise_store(const EncodeArgs& a, int r, int b0, int tm, int tn,
                                               const uint32_t (&w)[NBOX][TileGeo<T>::BOXC / 8],
-                                              const uint32_t (&sc)[NBOX], bool fast) {
+                                              const uint32_t (&sc)[NBOX], bool interior) {
   using G = TileGeo<T>;
   constexpr int NB = G::BOXC / 16;
   const int64_t gr = (int64_t)tm * kTileRows + r;
@@ -294,13 +330,9 @@ __device__ __forceinline__ void rowwise_store(const EncodeArgs& a, int r, int b0
     if (gc0 >= a.K) return;
     uint8_t* cp = a.row_codes + gr * a.row_cpitch + gc0 / 2;
     uint8_t* sp = a.row_scales + gr * a.row_spitch + gc0 / 16;
-    if (fast) {
-#pragma unroll
-      for (int q = 0; q < NB / 2; ++q)
-        stg_v4_cs(cp + 16 * q, make_uint4(w[bi][4 * q], w[bi][4 * q + 1], w[bi][4 * q + 2],
-                                          w[bi][4 * q + 3]));
-      if constexpr (NB == 4) stg_u32_keep(sp, sc[bi], policy_evict_last());
-      else stg_u16_keep(sp, sc[bi], policy_evict_last());
+    if (interior) {
+      store_words_g<2 * NB>(cp, w[bi], a.rc_g);
+      store_scales_g<NB>(sp, sc[bi], a.rs_g, policy_evict_last());
     } else {
       const int64_t rem = a.K - gc0;
       const int ncols = rem < G::BOXC ? (int)rem : G::BOXC;
@@ -468,7 +500,7 @@ template <typename T, int RG, bool CODES>
 __device__ __forceinline__ void colwise_store(const EncodeArgs& a, int cl, int rb0, int tm, int tn,
                                               const uint32_t (&w0)[RG / 8],
                                               const uint32_t (&w1)[RG / 8], uint32_t sc0,
-                                              uint32_t sc1, bool fast) {
+                                              uint32_t sc1, bool interior) {
   using G = TileGeo<T>;
   constexpr int NB = RG / 16;
   const int64_t gc = (int64_t)tn * G::TILEC + cl;
@@ -477,32 +509,14 @@ __device__ __forceinline__ void colwise_store(const EncodeArgs& a, int cl, int r
   const bool has1 = gc + 1 < a.K;
   uint8_t* c0p = a.col_codes + gc * a.col_cpitch + gr0 / 2;
   uint8_t* s0p = a.col_scales + gc * a.col_spitch + gr0 / 16;
-  if (fast) {
+  if (interior) {
     if constexpr (CODES) {
-      if constexpr (NB == 1) {
-        stg_v2_cs(c0p, w0[0], w0[1]);
-        stg_v2_cs(c0p + a.col_cpitch, w1[0], w1[1]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < NB / 2; ++q) {
-          stg_v4_cs(c0p + 16 * q,
-                    make_uint4(w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]));
-          stg_v4_cs(c0p + a.col_cpitch + 16 * q,
-                    make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]));
-        }
-      }
+      store_words_g<2 * NB>(c0p, w0, a.cc_g);
+      store_words_g<2 * NB>(c0p + a.col_cpitch, w1, a.cc_g);
     }
     const uint64_t keep = policy_evict_last();
-    if constexpr (NB == 4) {
-      stg_u32_keep(s0p, sc0, keep);
-      stg_u32_keep(s0p + a.col_spitch, sc1, keep);
-    } else if constexpr (NB == 2) {
-      stg_u16_keep(s0p, sc0, keep);
-      stg_u16_keep(s0p + a.col_spitch, sc1, keep);
-    } else {
-      s0p[0] = (uint8_t)sc0;
-      s0p[a.col_spitch] = (uint8_t)sc1;
-    }
+    store_scales_g<NB>(s0p, sc0, a.cs_g, keep);
+    store_scales_g<NB>(s0p + a.col_spitch, sc1, a.cs_g, keep);
   } else {
     const int64_t rem = a.M - gr0;
     const int nrows = rem < RG ? (int)rem : RG;
@@ -916,7 +930,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     if (abort_flag) break;
     const uint8_t* stage = smem + s * kTileBytes;
     auto& m = meta[s];
-    const bool fast = a.vec_ok && tm < a.full_m && tn < a.full_n;
+    const bool interior = tm < a.full_m && tn < a.full_n;
+    const bool fast = a.vec_ok && interior;
     uint8_t* staging = staging0 + (k % kStagingBuffers) * kStagingPerWarp;
     if constexpr (B2D) {
       if constexpr (!FOS && sizeof(T) == 2)
@@ -1063,7 +1078,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
           rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, false);
         }
       } else {
-        rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, fast);
+        rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, interior);
       }
     } else if (COL) {
       uint32_t w0[RG / 8], w1[RG / 8];
@@ -1149,7 +1164,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
           colwise_store<T, RG, true>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, false);
         }
       } else {
-        colwise_store<T, RG, !TOUT>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, fast);
+        colwise_store<T, RG, !TOUT>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, interior);
       }
     } else {
       __syncwarp();
@@ -1281,6 +1296,15 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
           a.col_spitch % cs == 0 && aligned(q.col_scales, cs);
   }
   a.vec_ok = vec ? 1 : 0;
+  auto gran = [](const void* base, int64_t pitch) {
+    int g = 16;
+    while (g > 1 && (reinterpret_cast<uintptr_t>(base) % g != 0 || pitch % g != 0)) g >>= 1;
+    return g;
+  };
+  a.rc_g = row ? gran(q.row_codes, a.row_cpitch) : 1;
+  a.rs_g = row ? gran(q.row_scales, a.row_spitch) : 1;
+  a.cc_g = col ? gran(q.col_codes, a.col_cpitch) : 1;
+  a.cs_g = col ? gran(q.col_scales, a.col_spitch) : 1;
   a.col_scale_sectors = (both && bf16 && a.col_spitch % 32 == 0 && aligned(q.col_scales, 32)) ? 1 : 0;
   a.row_scale_groups = (tout && both && bf16 && a.row_spitch % 32 == 0 &&
                         aligned(q.row_scales, 32)) ? 1 : 0;

@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 
-SHAPES = [(256, 256), (300, 200), (130, 1000), (1, 16), (17, 33), (129, 257), (512, 384)]
+SHAPES = [(256, 256), (300, 200), (130, 1000), (1, 16), (17, 33), (129, 257), (512, 384),
+          (272, 400)]
 
 
 def _x(shape, dtype, seed, decades=2.0):
