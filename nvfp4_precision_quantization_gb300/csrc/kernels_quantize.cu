@@ -389,12 +389,18 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
   const float A0 = a.row_scaled ? m.colA(cl) : A_t;
   const float A1 = a.row_scaled ? m.colA(cl + 1) : A_t;
   sc0 = sc1 = 0;
-  if constexpr (FOS && !B2D && LOOP && sizeof(T) == 2) {
-    // Four-over-six with both directions: the blocks in a loop (one copy of the
-    // block routine per column instead of one per block); results rotate / shift
-    // into place.
+  if constexpr (FOS && !B2D && LOOP && sizeof(T) == 2 && NB == 4) {
+    // Four-over-six with both directions: one column block per iteration (t = 2 jb +
+    // column), one copy of the block routine, and only one column's 16 values
+    // unpacked at a time (the packed pairs are loaded again for the second column),
+    // which keeps the loop inside the register budget of two CTAs per SM.  Each
+    // iteration's two code words and scale byte shift into place, so nothing is
+    // indexed at run time.
+    uint32_t flat[4 * NB];
+    uint64_t sc_all = 0;
 #pragma unroll 1
-    for (int jb = 0; jb < NB; ++jb) {
+    for (int t = 0; t < 2 * NB; ++t) {
+      const int jb = t >> 1, c = t & 1;
       const uint8_t* base = stage + (rb0 + 16 * jb) * 128;
       uint32_t v[16];
 #pragma unroll
@@ -403,33 +409,34 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
       uint32_t t8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) t8[i] = absmax_bf16x2(v[2 * i], v[2 * i + 1]);
-      uint32_t mm =
+      const uint32_t mm =
           absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(t8[0], t8[1]), absmax_bf16x2(t8[2], t8[3])),
                         absmax_bf16x2(absmax_bf16x2(t8[4], t8[5]), absmax_bf16x2(t8[6], t8[7])));
-      mm &= 0x7fff7fffu;
-      float x0[16], x1[16];
+      // this column's half of each pair, moved to the top 16 bits (the FP32 value)
+      const uint32_t sel = c ? 0x3244u : 0x1044u;
+      float x[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        x0[i] = bf16_lo(v[i]);
-        x1[i] = bf16_hi(v[i]);
-      }
-      uint32_t a0, a1, d0, d1;
-      const uint32_t s0 = quantize16<true, true>(x0, __uint_as_float(mm << 16), S0, A0, a.F_inv,
-                                                 a.neg_zero, a0, a1);
-      const uint32_t s1 = quantize16<true, true>(x1, __uint_as_float(mm & 0xffff0000u), S1, A1,
-                                                 a.F_inv, a.neg_zero, d0, d1);
+      for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(byte_perm(v[i], 0u, sel));
+      const float b = __uint_as_float(byte_perm(mm & 0x7fff7fffu, 0u, sel));
+      uint32_t q0, q1;
+      const uint32_t s8 = quantize16<true, true>(x, b, c ? S1 : S0, c ? A1 : A0, a.F_inv,
+                                                 a.neg_zero, q0, q1);
 #pragma unroll
-      for (int k = 0; k < RG / 8 - 2; ++k) {
-        w0[k] = w0[k + 2];
-        w1[k] = w1[k + 2];
-      }
-      w0[RG / 8 - 2] = a0;
-      w0[RG / 8 - 1] = a1;
-      w1[RG / 8 - 2] = d0;
-      w1[RG / 8 - 1] = d1;
-      sc0 = (sc0 >> 8) | (s0 << (8 * (NB - 1)));
-      sc1 = (sc1 >> 8) | (s1 << (8 * (NB - 1)));
+      for (int k = 0; k < 4 * NB - 2; ++k) flat[k] = flat[k + 2];
+      flat[4 * NB - 2] = q0;
+      flat[4 * NB - 1] = q1;
+      sc_all = (sc_all >> 8) | ((uint64_t)s8 << (8 * (2 * NB - 1)));
     }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      w0[2 * j] = flat[4 * j];
+      w0[2 * j + 1] = flat[4 * j + 1];
+      w1[2 * j] = flat[4 * j + 2];
+      w1[2 * j + 1] = flat[4 * j + 3];
+    }
+    const uint32_t lo = (uint32_t)sc_all, hi = (uint32_t)(sc_all >> 32);
+    sc0 = byte_perm(lo, hi, 0x6420u);
+    sc1 = byte_perm(lo, hi, 0x7531u);
     return;
   }
 #pragma unroll
@@ -1008,7 +1015,25 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     } else if (is_row) {
       uint32_t w[NBOX][G::BOXC / 8];
       uint32_t sc[NBOX];
-      rowwise_compute<T, NBOX, FOS, B2D, ROW && COL>(stage, m, a, r, b0, S_r, A_r, w, sc);
+      // Four-over-six with both directions and sector stores: one box at a time, its
+      // 32 code bytes stored as soon as they are computed (8 code words live instead
+      // of 16, which keeps the loop inside the register budget)
+      constexpr bool BOXWISE = FOS && !B2D && BOTH && SECT && sizeof(T) == 2;
+      if constexpr (BOXWISE) {
+        uint8_t* cp = a.row_codes + ((int64_t)tm * kTileRows + r) * a.row_cpitch +
+                      (int64_t)tn * (G::TILEC / 2);
+#pragma unroll 1
+        for (int bi = 0; bi < NBOX; ++bi) {
+          uint32_t wb[1][G::BOXC / 8], sb[1];
+          rowwise_compute<T, 1, FOS, B2D, true>(stage, m, a, r, b0 + bi, S_r, A_r, wb, sb);
+          if (bi == 0) sc[0] = sb[0];
+          else sc[NBOX - 1] = sb[0];
+          if (fast) stg_v8_cs(cp + (b0 + bi) * 32, wb[0]);
+          else rowwise_store<T, 1>(a, r, b0 + bi, tm, tn, wb, sb, false);
+        }
+      } else {
+        rowwise_compute<T, NBOX, FOS, B2D, ROW && COL>(stage, m, a, r, b0, S_r, A_r, w, sc);
+      }
       if (ROW && !COL && a.pad_ends != nullptr && r >= m.nrows) {
         // a padding row: zero codes and scales (what a zero row encodes to)
 #pragma unroll
@@ -1069,12 +1094,14 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         store_row_scales();
       } else if constexpr (SECT) {
         if (fast) {
-          uint8_t* cp = a.row_codes + ((int64_t)tm * kTileRows + r) * a.row_cpitch +
-                        (int64_t)tn * (G::TILEC / 2);
+          if constexpr (!BOXWISE) {
+            uint8_t* cp = a.row_codes + ((int64_t)tm * kTileRows + r) * a.row_cpitch +
+                          (int64_t)tn * (G::TILEC / 2);
 #pragma unroll
-          for (int bi = 0; bi < NBOX; ++bi) stg_v8_cs(cp + bi * 32 + b0 * 32, w[bi]);
+            for (int bi = 0; bi < NBOX; ++bi) stg_v8_cs(cp + bi * 32 + b0 * 32, w[bi]);
+          }
           store_row_scales();
-        } else {
+        } else if constexpr (!BOXWISE) {
           rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, false);
         }
       } else {
