@@ -316,3 +316,33 @@ def test_grouped_invalid_ends_write_nothing_and_set_status():
     assert torch.all(out.codes == 0xA5) and torch.all(out.scales == 0xA5)
     assert nv.nvfp4_device_status() == 0
 
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("fos,bound", [(True, 256.0), (False, 448.0)])
+@pytest.mark.parametrize("counts,cols", [
+    ([100, 156, 0, 300, 212], 640),   # ends 100, 256, 256, 556, 768: groups merged into chunks
+    ([77, 300, 135], 300),            # no end on a tile boundary but the last: one chunk
+    ([256] * 40, 1024),               # 40 chunks, 1280 items: several per CTA
+    ([128, 0, 0, 128], 128),          # empty groups between chunks
+])
+def test_grouped_quantize_per_group_amax_any_ends(dtype, fos, bound, counts, cols):
+    """Per-group amax, rowwise, with rows a multiple of 128 and group ends anywhere: the
+    amax and the encode of each chunk of groups run in one kernel (chunks end at the
+    group ends that fall on 128-row boundaries)."""
+    x, ends = _groups(counts, cols, 1, seed=14)
+    x = x.to(dtype)
+    rows = x.shape[0]
+    assert rows % 128 == 0
+    ga = torch.full((len(ends),), -1.0, device=DEV)
+    out = nv.alloc_out(rows, cols, rows, DEV, 0xA5)
+    out.amax.fill_(-1.0)
+    nv.nvfp4_grouped_quantize_rowwise(x, torch.from_numpy(ends).to(DEV),
+                                      cfg(nv.NVFP4_PER_TENSOR, bound, fos), out, ga)
+    torch.cuda.synchronize()
+    xb, tag = host_bits(x)
+    codes, scales, ra, gam = oracle.grouped_quantize_rowwise(xb, tag, ends, mode=nv.NVFP4_PER_TENSOR,
+                                                              bound=bound, four_over_six=fos)
+    assert_same(out, (codes, scales, ra), "grouped")
+    assert np.array_equal(ga.cpu().numpy(), gam)
+    assert nv.nvfp4_device_status() == 0
