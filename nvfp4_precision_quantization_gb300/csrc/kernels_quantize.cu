@@ -904,9 +904,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   // banks; their code words are put back in row order afterwards.  Otherwise
   // consecutive threads take consecutive column pairs.
   constexpr bool PAIRED = SECT && BOTH && sizeof(T) == 2 && !FOS && !B2D;
-  const int hh = PAIRED ? (lane & 1) : 0;
-  const int cl = PAIRED ? 2 * (((ct >> 5) << 4) + (lane >> 1)) : 2 * (ct % NP);
-  const int rb0 = PAIRED ? hh * RG : (ct / NP) * RG;
+  // CPAIR (sector stores, columnwise only, BF16, 1x16): a thread holds 32 rows of a
+  // column pair, and neighbouring lanes hold the two 32-row halves of the same 64-row
+  // run, so that after one exchange each lane stores one column's 32 code bytes (a
+  // whole sector) and 4 scale bytes.  The rows are read in natural order (the 2-way
+  // bank conflict between the two halves costs nothing next to the encode).
+  constexpr bool CPAIR = SECT && COL && !ROW && sizeof(T) == 2 && !B2D;
+  const int hh = (PAIRED || CPAIR) ? (lane & 1) : 0;
+  const int cl = PAIRED  ? 2 * (((ct >> 5) << 4) + (lane >> 1))
+                 : CPAIR ? 2 * ((((ct >> 5) & 3) << 4) + (lane >> 1))
+                         : 2 * (ct % NP);
+  const int rb0 = PAIRED ? hh * RG : CPAIR ? 64 * (ct >> 7) + 32 * hh : (ct / NP) * RG;
   const int r = BOTH ? tid : (tid & 127), b0 = BOTH ? 0 : (tid >> 7);
   // byte offset of row i of a 16-row block: i * 128 + coff[i & 7] (signed: with
   // the i ^ 4 row order an entry can be negative, the sum never is)
@@ -915,7 +923,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     const int box = cl / G::BOXC, byte = (cl % G::BOXC) * (int)sizeof(T);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int kk = k ^ (4 * hh);  // the row actually read, mod 8
+      const int kk = k ^ (PAIRED ? 4 * hh : 0);  // the row actually read, mod 8
       coff[k] = box * kBoxBytes + ((((byte >> 4) ^ kk)) << 4) + (byte & 15) + (kk - k) * 128;
     }
   }
@@ -1138,7 +1146,27 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
           bulk_commit();
         }
       }
-      if constexpr (SECT) {
+      if constexpr (SECT && CPAIR) {
+        if (fast) {
+          // lane hh = 0 takes column cl (its own rows 0-31 of the run, the partner's
+          // 32-63), lane hh = 1 column cl + 1 (the partner's rows 0-31, its own 32-63)
+          uint32_t cw[RG / 4];
+#pragma unroll
+          for (int q = 0; q < RG / 8; ++q) {
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, hh ? w0[q] : w1[q], 1);
+            cw[q] = hh ? got : w0[q];
+            cw[RG / 8 + q] = hh ? w1[q] : got;
+          }
+          const uint32_t gs = __shfl_xor_sync(0xffffffffu, hh ? sc0 : sc1, 1);
+          const uint32_t scw = hh ? (gs | (sc1 << 16)) : (sc0 | (gs << 16));
+          const int64_t gcol = (int64_t)tn * G::TILEC + cl + hh;
+          const int64_t grun = (int64_t)tm * kTileRows + rb0 - 32 * hh;
+          stg_v8_cs(a.col_codes + gcol * a.col_cpitch + grun / 2, cw);
+          stg_u32_keep(a.col_scales + gcol * a.col_spitch + grun / 16, scw, policy_evict_last());
+        } else {
+          colwise_store<T, RG, true>(a, cl, rb0, tm, tn, w0, w1, sc0, sc1, false);
+        }
+      } else if constexpr (SECT) {
         if (fast) {
           uint8_t* c0p = a.col_codes + ((int64_t)tn * G::TILEC + cl) * a.col_cpitch +
                          ((int64_t)tm * kTileRows + rb0) / 2;
@@ -1211,6 +1239,9 @@ EncodeFn pick_io(bool tma, int outm) {
     if (tma && outm == kOutTma) return k_encode<T, ROW, COL, FOS, B2D, true, kOutTma>;
     if (tma && outm == kOutSector) return k_encode<T, ROW, COL, FOS, B2D, true, kOutSector>;
   }
+  if constexpr (sizeof(T) == 2 && !ROW && COL && !B2D) {
+    if (tma && outm == kOutSector) return k_encode<T, ROW, COL, FOS, B2D, true, kOutSector>;
+  }
   return tma ? k_encode<T, ROW, COL, FOS, B2D, true, kOutDirect>
              : k_encode<T, ROW, COL, FOS, B2D, false, kOutDirect>;
 }
@@ -1224,7 +1255,12 @@ EncodeFn pick_mode(bool fos, bool b2d, bool tma, int outm) {
 
 // Columnwise only, 1x16 blocks, each block transformed first.
 template <typename T>
-EncodeFn pick_rht(bool fos, bool tma) {
+EncodeFn pick_rht(bool fos, bool tma, int outm) {
+  if constexpr (sizeof(T) == 2) {
+    if (tma && outm == kOutSector)
+      return fos ? k_encode<T, false, true, true, false, true, kOutSector, true>
+                 : k_encode<T, false, true, false, false, true, kOutSector, true>;
+  }
   if (fos)
     return tma ? k_encode<T, false, true, true, false, true, kOutDirect, true>
                : k_encode<T, false, true, true, false, false, kOutDirect, true>;
@@ -1309,6 +1345,10 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
              make_byte_map(&map_cc, q.col_codes, q.K, a.col_cpitch, 32, 64))
       outm = kOutTma;
   }
+  // columnwise only (BF16, 1x16): whole-sector code stores from lane pairs
+  if (bf16 && tma && col && !row && !q.block_2d && a.col_cpitch % 32 == 0 &&
+      aligned(q.col_codes, 32) && a.col_spitch % 4 == 0 && aligned(q.col_scales, 4))
+    outm = kOutSector;
   const bool tout = outm != kOutDirect;
   // aligned vector stores on interior tiles
   const int rows_per_col_thread = bf16 ? (both ? 64 : 32) : (both ? 32 : 16);
@@ -1336,8 +1376,8 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.row_scale_groups = (tout && both && bf16 && a.row_spitch % 32 == 0 &&
                         aligned(q.row_scales, 32)) ? 1 : 0;
 
-  EncodeFn fn = q.rht ? (bf16 ? pick_rht<uint16_t>(q.four_over_six, tma)
-                              : pick_rht<float>(q.four_over_six, tma))
+  EncodeFn fn = q.rht ? (bf16 ? pick_rht<uint16_t>(q.four_over_six, tma, outm)
+                              : pick_rht<float>(q.four_over_six, tma, outm))
                : bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, outm)
                       : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, outm);
   const int smem = outm == kOutTma ? EncodeSmem<kOutTma>::kBytes

@@ -346,3 +346,17 @@ def test_grouped_quantize_per_group_amax_any_ends(dtype, fos, bound, counts, col
     assert_same(out, (codes, scales, ra), "grouped")
     assert np.array_equal(ga.cpu().numpy(), gam)
     assert nv.nvfp4_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(256, 256), (640, 300), (4096, 2048)])
+@pytest.mark.parametrize("mode", [nv.NVFP4_ROW_SCALED, nv.NVFP4_PER_TENSOR])
+@pytest.mark.parametrize("fos,bound", [(False, 448.0), (True, 256.0)])
+def test_quantize_columnwise_only_sector_stores(shape, mode, fos, bound):
+    """Columnwise only, BF16, rows a multiple of 64: lane pairs exchange their 32-row
+    halves and store each column's codes as whole 32-byte sectors (4096 x 2048: 512
+    tiles, so CTAs walk several)."""
+    x = _x(shape, torch.bfloat16, seed=15)
+    c = cfg(mode, bound, fos)
+    g = gpu_quantize(x, c, rowwise=False)
+    o = oracle_quantize(x, c, rowwise=False)
+    assert_same(g["col"], o["col"], "col")
