@@ -398,6 +398,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ __align__(8) uint64_t empty[kStages];
   __shared__ volatile int abort_flag;
+  // column maxima of a super-strip, combined over the four row groups of warps
+  // before one global atomic per column (two buffers, used by alternate flushes)
+  constexpr int kSpan = TileGrid::kGroup * Geo::TILEC;
+  __shared__ uint32_t col_buf[COL ? 2 : 1][COL ? kSpan : 1];
+  __shared__ __align__(8) uint64_t col_bar[2];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   if (noop_set(a.noop)) return;
@@ -414,9 +419,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    mbar_init(&col_bar[0], kConsumerWarps);
+    mbar_init(&col_bar[1], kConsumerWarps);
     abort_flag = 0;
     fence_mbar_init();
   }
+  if (COL)
+    for (int i = tid; i < 2 * kSpan; i += kPipeThreads) col_buf[i / kSpan][i % kSpan] = 0;
   __syncthreads();
   pdl_launch_dependents();
   if (count <= 0) return;
@@ -466,11 +475,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   int cur_ss = -1;
 
   int cur_g = 0, grp_tm = -1, grp = 0;  // grouped columns: group of the partials / of tile row grp_tm
-  auto flush_cols = [&](int ss) {
-    float* const cbase = a.col_amax + (a.col_grouped ? (int64_t)cur_g * a.K : 0);
+  int n_col_flush = 0;
+  // Publish the column maxima of super-strip ss: reduce over the 4 row lanes of
+  // the warp, combine the 4 row-group warps in shared memory, then one global
+  // atomic per column.  Returns false when the wait for the other warps ran out.
+  auto flush_cols = [&](int ss) -> bool {
+    const int b = n_col_flush & 1;
+    const uint32_t parity = (uint32_t)((n_col_flush >> 1) & 1);
+    ++n_col_flush;
+    uint32_t* const buf = col_buf[b];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-      const int tn = ss * NG + g;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if constexpr (BF16) {
@@ -481,24 +496,34 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
           cm[g][j] = fmaxf(cm[g][j], __shfl_xor_sync(0xffffffffu, cm[g][j], 16));
         }
       }
-      if (ro == 0 && tn < a.grid.tiles_n) {
-        const int64_t col0 = (int64_t)tn * Geo::TILEC + box * Geo::BOXC + c * (16 / (int)sizeof(T));
+      if (ro == 0) {
+        const int c0 = g * Geo::TILEC + box * Geo::BOXC + c * (16 / (int)sizeof(T));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if constexpr (BF16) {
             const uint32_t mv = cm[g][j] & 0x7fff7fffu;
-            if (col0 + 2 * j < a.K)
-              atomic_max_nonneg(&cbase[col0 + 2 * j], __uint_as_float(mv << 16));
-            if (col0 + 2 * j + 1 < a.K)
-              atomic_max_nonneg(&cbase[col0 + 2 * j + 1], __uint_as_float(mv & 0xffff0000u));
+            if (mv & 0xffffu) atomicMax(&buf[c0 + 2 * j], mv << 16);
+            if (mv >> 16) atomicMax(&buf[c0 + 2 * j + 1], mv & 0xffff0000u);
           } else {
-            if (col0 + j < a.K) atomic_max_nonneg(&cbase[col0 + j], cm[g][j]);
+            if (cm[g][j] > 0.0f) atomicMax(&buf[c0 + j], __float_as_uint(cm[g][j]));
           }
         }
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) cm[g][j] = 0;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&col_bar[b]);
+    if (!mbar_wait_bounded(&col_bar[b], parity)) return false;
+    float* const cbase = a.col_amax + (a.col_grouped ? (int64_t)cur_g * a.K : 0);
+    const int64_t span0 = (int64_t)ss * kSpan;
+    for (int i = tid; i < kSpan; i += kConsumerWarps * 32) {
+      const uint32_t v = buf[i];
+      if (v == 0) continue;
+      buf[i] = 0;  // free for the flush after next (ordered by the next flush's barrier)
+      if (span0 + i < a.K) atomicMax(reinterpret_cast<unsigned int*>(cbase + span0 + i), v);
+    }
+    return true;
   };
 
   Acc rpa[8];
@@ -561,7 +586,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       }
       const int g_now = a.col_grouped ? grp : 0;
       if (ss != cur_ss || g_now != cur_g) {
-        if (cur_ss >= 0) flush_cols(cur_ss);
+        if (cur_ss >= 0 && !flush_cols(cur_ss)) {
+          abort_flag = 1;
+          if (lane == 0) raise_status(a.status, kStatusTimeout);
+          break;
+        }
         cur_ss = ss;
         cur_g = g_now;
       }
@@ -632,7 +661,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       }
     }
   }
-  if (COL && cur_ss >= 0 && !abort_flag) flush_cols(cur_ss);
+  if (COL && cur_ss >= 0 && !abort_flag && !flush_cols(cur_ss)) {
+    abort_flag = 1;
+    if (lane == 0) raise_status(a.status, kStatusTimeout);
+  }
   if (ROW && cur_tm >= 0 && !abort_flag) flush_rows(cur_tm);
   if (TEN) {
     float m;
