@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 SHAPES = [(256, 256), (300, 200), (130, 1000), (1, 16), (17, 33), (129, 257), (512, 384),
-          (272, 400)]
+          (272, 400), (264, 512), (136, 224)]
 
 
 def _x(shape, dtype, seed, decades=2.0):
