@@ -589,7 +589,8 @@ def run_supplementary(args):
 
         def step(ev):
             # the kernels nvfp4_grouped_quantize_rowwise (per-group amax) launches:
-            # group check, grouped amax, expansion to rows, then the rowwise encode
+            # group check, the tiled row amax, each group's max written back to its
+            # rows, then the rowwise encode
             nv.nvfp4_grouped_amax(x, ends, gam, row_amax_expanded=row.amax, stream=stream)
             ev[0].record(stream)
             row.amax_in = row.amax

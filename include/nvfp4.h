@@ -164,8 +164,9 @@ NVFP4_API nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *sca
  *   group_ends: device int64 [num_groups], cumulative row ends, non-decreasing,
  *   last == rows (an empty group is allowed and gets amax 0).
  *   group_amax [num_groups] (required); row_amax_expanded [rows] (optional)
- *   receives each row's group amax.  Invalid ends set NVFP4_DEVICE_BAD_GROUPS and
- *   nothing is written.  num_groups <= 4096.
+ *   receives each row's group amax (it also holds the row maxima between the
+ *   call's kernels).  Invalid ends set NVFP4_DEVICE_BAD_GROUPS and nothing is
+ *   written.  num_groups <= 4096.
  */
 NVFP4_API nvfp4_status nvfp4_grouped_amax(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
                                 const int64_t *group_ends, int32_t num_groups, float *group_amax,

@@ -663,11 +663,41 @@ nvfp4_status nvfp4_grouped_amax(const void* x, int32_t in_dtype, int64_t rows, i
   g.prep.zero_ptr[0] = group_amax;
   g.prep.zero_n[0] = num_groups;
   g.prep.noop = noop;
+  const InType in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+  if (row_amax_expanded) {
+    // With a per-row output to work in: the row maxima from the tiled amax pass,
+    // then each group's maximum over its rows, written back to its rows.
+    g.prep.zero_ptr[1] = row_amax_expanded;
+    g.prep.zero_n[1] = rows;
+    cudaError_t e = launch_group_check(g, dev, stream, false);
+    if (e != cudaSuccess) return cuda_fail(e, "group check launch");
+    AmaxArgs am{};
+    am.x = x;
+    am.in = in;
+    am.M = rows;
+    am.K = cols;
+    am.row_amax = row_amax_expanded;
+    am.noop = noop;
+    am.group_ends = group_ends;
+    am.num_groups = num_groups;
+    if ((e = launch_amax(am, dev, stream)) != cudaSuccess) return cuda_fail(e, "amax launch");
+    GroupReduceArgs r{};
+    r.group_ends = group_ends;
+    r.num_groups = num_groups;
+    r.M = rows;
+    r.row_max = row_amax_expanded;
+    r.group_amax = group_amax;
+    r.noop = noop;
+    r.expand = 1;
+    if ((e = launch_group_reduce(r, dev, stream)) != cudaSuccess)
+      return cuda_fail(e, "group reduce launch");
+    return NVFP4_OK;
+  }
   cudaError_t e = launch_group_check(g, dev, stream, false);
   if (e != cudaSuccess) return cuda_fail(e, "group check launch");
   GroupedAmaxArgs a{};
   a.x = x;
-  a.in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+  a.in = in;
   a.M = rows;
   a.K = cols;
   a.group_ends = group_ends;

@@ -82,6 +82,20 @@ struct GroupCheckArgs {
 cudaError_t launch_group_check(const GroupCheckArgs& a, const DeviceInfo& dev,
                                cudaStream_t stream, bool expand_pass);
 
+// Group maxima from per-row maxima (row_max [M], computed before), optionally
+// written back to every row of the group.  Writes nothing unless the ends are valid.
+struct GroupReduceArgs {
+  const int64_t* group_ends;
+  int num_groups;
+  int64_t M;
+  float* row_max;
+  float* group_amax;
+  const float* noop;
+  int expand;
+};
+cudaError_t launch_group_reduce(const GroupReduceArgs& a, const DeviceInfo& dev,
+                                cudaStream_t stream);
+
 // Tile quantize of x [M][K] into the rowwise and/or columnwise outputs.
 struct QuantArgs {
   const void* x;

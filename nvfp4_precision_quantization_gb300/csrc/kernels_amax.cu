@@ -794,6 +794,36 @@ __global__ void __launch_bounds__(kThreads) k_grouped_amax(GroupedKernelArgs a) 
   }
 }
 
+// Group maxima from per-row maxima: group_amax[g] = max of row_max over the rows of
+// group g, and with `expand` every row of group g then takes that value (row_max is
+// the per-row amax output of the grouped quantize).  A CTA owns whole groups
+// (g = blockIdx.x, += gridDim.x): it reads a group's rows before it writes them, and
+// no other CTA touches them.  Nothing is written unless the ends are valid.
+__global__ void __launch_bounds__(kThreads) k_group_reduce(GroupReduceArgs a) {
+  __shared__ int64_t s_ends[kMaxGroups];
+  __shared__ float red[kThreads / 32];
+  __shared__ float s_m;
+  if (noop_set(a.noop)) return;
+  if (!load_group_ends(a.group_ends, a.num_groups, a.M, s_ends)) return;
+  const int tid = threadIdx.x;
+  for (int g = blockIdx.x; g < a.num_groups; g += gridDim.x) {
+    const int64_t r0 = g ? s_ends[g - 1] : 0, r1 = s_ends[g];
+    float m = 0.0f;
+    for (int64_t r = r0 + tid; r < r1; r += kThreads) m = fmaxf(m, a.row_max[r]);
+    m = block_max(m, red);
+    if (tid == 0) {
+      a.group_amax[g] = m;
+      s_m = m;
+    }
+    __syncthreads();
+    if (a.expand) {
+      const float v = s_m;
+      for (int64_t r = r0 + tid; r < r1; r += kThreads) a.row_max[r] = v;
+    }
+    __syncthreads();  // s_m and red are reused by the next group
+  }
+}
+
 __global__ void k_group_check(GroupCheckArgs a, int* status, bool expand_pass) {
   __shared__ int64_t s_ends[kMaxGroups];
   if (noop_set(a.noop)) return;
@@ -940,6 +970,14 @@ cudaError_t launch_grouped_amax(const GroupedAmaxArgs& a, const DeviceInfo& dev,
   if (a.in == InType::BF16) fn = vec ? k_grouped_amax<true, true> : k_grouped_amax<true, false>;
   else fn = vec ? k_grouped_amax<false, true> : k_grouped_amax<false, false>;
   fn<<<(unsigned)items, kThreads, 0, stream>>>(k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_reduce(const GroupReduceArgs& a, const DeviceInfo& dev,
+                                cudaStream_t stream) {
+  const int blocks = std::min(a.num_groups, 2 * dev.num_sms);
+  if (blocks < 1) return cudaSuccess;
+  k_group_reduce<<<(unsigned)blocks, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
