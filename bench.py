@@ -635,7 +635,8 @@ def run_supplementary(args):
                                                      stream=stream)
         bio = 2 * T * K + M * K // 2 + M * K // 16 + 4 * M + 4 * G
         bmin = bio  # as for the padded tokens: each group fits in L2
-        kern, kbytes, launches = "whole step (check, grouped amax, expand, rowwise encode)", bio, 4
+        kern, kbytes, launches = ("whole step (check, row amax, group reduce, expand, rowwise "
+                                   "encode)"), bio, 5
         dtype, elems = "bf16", M * K
     elif w == "rht":
         x = workloads.linear(dev)[1]

@@ -786,23 +786,38 @@ nvfp4_status nvfp4_grouped_quantize_rowwise_padded(
   g.in_rows = tokens;
   g.prep.zero_ptr[0] = group_amax;
   g.prep.zero_n[0] = num_groups;
+  // row->amax [padded_rows >= tokens] holds the ragged rows' maxima until step 3
+  g.prep.zero_ptr[1] = row->amax;
+  g.prep.zero_n[1] = tokens;
   g.prep.noop = noop;
   cudaError_t e = launch_group_check(g, dev, stream, false);
   if (e != cudaSuccess) return cuda_fail(e, "group check launch");
-  // 2. group maxima over the ragged rows
-  GroupedAmaxArgs a{};
-  a.x = x;
-  a.in = in;
-  a.M = tokens;
-  a.K = cols;
-  a.group_ends = ragged_ends;
-  a.num_groups = num_groups;
-  a.group_amax = group_amax;
-  a.noop = noop;
-  a.pad_ends = padded_ends;
-  a.pad_rows = padded_rows;
-  if ((e = launch_grouped_amax(a, dev, stream)) != cudaSuccess)
-    return cuda_fail(e, "grouped amax launch");
+  // 2. group maxima over the ragged rows: the tiled row amax pass, then each
+  //    group's max over its rows
+  AmaxArgs am{};
+  am.x = x;
+  am.in = in;
+  am.M = tokens;
+  am.K = cols;
+  am.row_amax = row->amax;
+  am.noop = noop;
+  am.group_ends = ragged_ends;
+  am.num_groups = num_groups;
+  am.pad_ends = padded_ends;
+  am.pad_rows = padded_rows;
+  if ((e = launch_amax(am, dev, stream)) != cudaSuccess) return cuda_fail(e, "amax launch");
+  GroupReduceArgs rd{};
+  rd.group_ends = ragged_ends;
+  rd.num_groups = num_groups;
+  rd.M = tokens;
+  rd.row_max = row->amax;
+  rd.group_amax = group_amax;
+  rd.noop = noop;
+  rd.expand = 0;
+  rd.pad_ends = padded_ends;
+  rd.pad_rows = padded_rows;
+  if ((e = launch_group_reduce(rd, dev, stream)) != cudaSuccess)
+    return cuda_fail(e, "group reduce launch");
   // 3. every padded row (padding included) takes its group's amax
   g.prep = PrepArgs{};
   g.group_amax = group_amax;

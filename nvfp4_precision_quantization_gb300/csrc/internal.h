@@ -41,6 +41,8 @@ struct AmaxArgs {
   const float* noop;
   const int64_t* group_ends;  // optional: do nothing unless these group ends are valid
   int num_groups;
+  const int64_t* pad_ends;  // optional, with group_ends: and this padded layout of them
+  int64_t pad_rows;
   // grouped columns (TMA path): col_amax is [num_groups][K], each group's column maxima;
   // the group ends must be multiples of 128
   bool col_grouped;
@@ -92,6 +94,8 @@ struct GroupReduceArgs {
   float* group_amax;
   const float* noop;
   int expand;
+  const int64_t* pad_ends;  // optional: also require this padded layout of the groups
+  int64_t pad_rows;
 };
 cudaError_t launch_group_reduce(const GroupReduceArgs& a, const DeviceInfo& dev,
                                 cudaStream_t stream);

@@ -156,6 +156,8 @@ struct AmaxKernelArgs {
   const float* noop;
   const int64_t* ends;
   int G;
+  const int64_t* pad_ends;  // with ends: also require this padded layout (pad_rows rows)
+  int64_t pad_rows;
   int64_t rows_per_item;  // multiple of 8 * kRowGroups
   int64_t keep_from_row;  // rows >= this are loaded with an L2 evict_last hint
   int num_col_items;
@@ -169,7 +171,10 @@ __global__ void __launch_bounds__(kThreads) k_amax_bf16(AmaxKernelArgs a) {
   __shared__ float col_red[kRowGroups][CW];
   __shared__ float red[kThreads / 32];
   if (noop_set(a.noop)) return;
-  if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) return;
+  if (a.ends != nullptr && (!groups_valid(a.ends, a.G, a.M) ||
+                            (a.pad_ends != nullptr &&
+                             !pad_layout_valid(a.ends, a.pad_ends, a.G, a.M, a.pad_rows))))
+    return;
   const uint16_t* x = static_cast<const uint16_t*>(a.x);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int cw = w % kColWarps, rg = w / kColWarps;
@@ -258,7 +263,10 @@ __global__ void __launch_bounds__(kThreads) k_amax_f32(AmaxKernelArgs a) {
   __shared__ float col_red[kRowGroups][CW];
   __shared__ float red[kThreads / 32];
   if (noop_set(a.noop)) return;
-  if (a.ends != nullptr && !groups_valid(a.ends, a.G, a.M)) return;
+  if (a.ends != nullptr && (!groups_valid(a.ends, a.G, a.M) ||
+                            (a.pad_ends != nullptr &&
+                             !pad_layout_valid(a.ends, a.pad_ends, a.G, a.M, a.pad_rows))))
+    return;
   const float* x = static_cast<const float*>(a.x);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int cw = w % kColWarps, rg = w / kColWarps;
@@ -370,6 +378,8 @@ struct AmaxTmaArgs {
   const float* noop;
   const int64_t* ends;
   int G;
+  const int64_t* pad_ends;  // with ends: also require this padded layout (pad_rows rows)
+  int64_t pad_rows;
   int keep_tiles;  // the last keep_tiles tiles of a chunk are loaded with evict_last
   int* status;
   // grouped columns: col_amax is [G][K], the column maxima of each group's rows (the
@@ -407,7 +417,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
                                              ~uintptr_t(1023));
   if (noop_set(a.noop)) return;
   if (a.ends != nullptr && (!groups_valid(a.ends, a.G, a.M) ||
-                            (a.col_grouped && !ends_aligned(a.ends, a.G, kTileRows))))
+                            (a.col_grouped && !ends_aligned(a.ends, a.G, kTileRows)) ||
+                            (a.pad_ends != nullptr &&
+                             !pad_layout_valid(a.ends, a.pad_ends, a.G, a.M, a.pad_rows))))
     return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int begin, end;
@@ -805,6 +817,9 @@ __global__ void __launch_bounds__(kThreads) k_group_reduce(GroupReduceArgs a) {
   __shared__ float s_m;
   if (noop_set(a.noop)) return;
   if (!load_group_ends(a.group_ends, a.num_groups, a.M, s_ends)) return;
+  if (a.pad_ends != nullptr &&
+      !pad_layout_valid(a.group_ends, a.pad_ends, a.num_groups, a.M, a.pad_rows))
+    return;
   const int tid = threadIdx.x;
   for (int g = blockIdx.x; g < a.num_groups; g += gridDim.x) {
     const int64_t r0 = g ? s_ends[g - 1] : 0, r1 = s_ends[g];
@@ -891,6 +906,8 @@ cudaError_t launch_amax(const AmaxArgs& a, const DeviceInfo& dev, cudaStream_t s
       k.noop = a.noop;
       k.ends = a.group_ends;
       k.G = a.num_groups;
+      k.pad_ends = a.pad_ends;
+      k.pad_rows = a.pad_rows;
       k.status = dev.status;
       k.col_grouped = a.col_grouped ? 1 : 0;
       const int grid = pipe_grid_size(k.grid.num_tiles, dev.num_sms);
@@ -930,6 +947,8 @@ cudaError_t launch_amax(const AmaxArgs& a, const DeviceInfo& dev, cudaStream_t s
   k.noop = a.noop;
   k.ends = a.group_ends;
   k.G = a.num_groups;
+  k.pad_ends = a.pad_ends;
+  k.pad_rows = a.pad_rows;
   k.num_col_items = (int)((a.K + CW - 1) / CW);
   k.rows_per_item = pick_rows_per_item(a.M, k.num_col_items, dev.num_sms);
   // keep the last ~80 MB of x in L2 for the encode pass, which walks x backwards

@@ -321,15 +321,15 @@ def test_grouped_invalid_ends_write_nothing_and_set_status():
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("fos,bound", [(True, 256.0), (False, 448.0)])
 @pytest.mark.parametrize("counts,cols", [
-    ([100, 156, 0, 300, 212], 640),   # ends 100, 256, 256, 556, 768: groups merged into chunks
-    ([77, 300, 135], 300),            # no end on a tile boundary but the last: one chunk
-    ([256] * 40, 1024),               # 40 chunks, 1280 items: several per CTA
-    ([128, 0, 0, 128], 128),          # empty groups between chunks
+    ([100, 156, 0, 300, 212], 640),   # ends 100, 256, 256, 556, 768
+    ([77, 300, 135], 300),            # no end on a tile boundary but the last
+    ([256] * 40, 1024),               # 40 groups, several tiles per CTA
+    ([128, 0, 0, 128], 128),          # empty groups
 ])
 def test_grouped_quantize_per_group_amax_any_ends(dtype, fos, bound, counts, cols):
-    """Per-group amax, rowwise, with rows a multiple of 128 and group ends anywhere: the
-    amax and the encode of each chunk of groups run in one kernel (chunks end at the
-    group ends that fall on 128-row boundaries)."""
+    """Per-group amax, rowwise, with rows a multiple of 128 and group ends anywhere
+    (inside tiles, on tile boundaries, empty groups, many groups): the row maxima,
+    each group's maximum over its rows and the encode with each row's group amax."""
     x, ends = _groups(counts, cols, 1, seed=14)
     x = x.to(dtype)
     rows = x.shape[0]
