@@ -409,6 +409,9 @@ SUPPLEMENTARY = {
     "rht": "random Hadamard transform of the wgrad operand dY 16384x28672 BF16 (per column, "
            "16-row blocks, (1/4) H16 diag(s), sign mask 0x6D2B) fused into its row-scaled "
            "columnwise quantize (per-column amax of the transform, bound 448)",
+    "rht-both": "dY 16384x28672 BF16, row-scaled, both directions in one encode pass: rowwise "
+                "as it is, columnwise after the random Hadamard transform (sign mask 0x6D2B); "
+                "row amax of dY, column amax of the transform, bound 448",
     "outliers": "X 4096x4096 BF16 N(0,1), 0.1 % of the entries x50: per-tensor then "
                 "row-scaled NVFP4 quantize, both directions, 1x16, bound 448 (each call: "
                 "prep, amax pass, encode; X fits in L2, so its second read comes from L2)",
@@ -475,6 +478,22 @@ def supplementary_oracle_sample(w: str, strip_rows: int, min_seconds: float = 10
         nbytes = threads * (2 * strip_rows * cols + strip_rows * cols // 2
                             + strip_rows * cols // 16 + 4 * cols)
         what = f"{threads} strip(s) of {strip_rows} rows (tokens) of a 28672-column dY"
+    elif w == "rht-both":
+        g = workloads.generator(workloads.SEEDS["linear"], "cpu")
+        xb, _ = bits(workloads.row_lognormal(n, 28672, g, "cpu"))
+        cols = 28672
+        for i in range(threads):
+            part = xb[i * strip_rows:(i + 1) * strip_rows]
+            jobs.append(lambda p=part: (
+                oracle.quantize(p, "bf16", mode=oracle.ROW_SCALED, bound=448.0,
+                                columnwise=False),
+                oracle.quantize_columnwise_rht(p, "bf16", RHT_SIGN_MASK, mode=oracle.ROW_SCALED,
+                                               bound=448.0)))
+        nbytes = threads * (2 * strip_rows * cols + 2 * (strip_rows * cols // 2
+                                                          + strip_rows * cols // 16)
+                            + 4 * (cols + strip_rows))
+        what = (f"{threads} strip(s) of {strip_rows} rows (tokens) of a 28672-column dY, "
+                f"both directions")
     elif w == "weights16x16":
         xb, _ = bits(workloads.edge_normal(n, 8192, torch.bfloat16, "cpu", std=0.02))
         cols = 8192
@@ -651,6 +670,23 @@ def run_supplementary(args):
         # fused: the amax pass and the encode pass each read x and transform it
         bmin = bio + 2 * M * K
         kern, kbytes, launches = "whole step (prep, transformed column amax, encode)", bmin, 3
+        dtype, elems = "bf16", M * K
+    elif w == "rht-both":
+        x = workloads.linear(dev)[1]
+        M, K = x.shape
+        cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+        row = nv.alloc_out(M, K, M, dev)
+        col = nv.alloc_out(K, M, K, dev)
+
+        def step(ev):
+            ev[0].record(stream)
+            nv.nvfp4_quantize_both_rht(x, RHT_SIGN_MASK, cfg, row, col, stream=stream)
+        bio = 2 * M * K + 2 * (M * K // 2 + M * K // 16) + 4 * (M + K)
+        # the floor reads x twice (both maxima in one pass, then the encode); these
+        # kernels read it three times (the row amax and the transform's amax apart)
+        bmin = bio + 2 * M * K
+        kern, kbytes, launches = ("whole step (prep, transformed column amax, row amax, "
+                                  "encode)"), bmin, 4
         dtype, elems = "bf16", M * K
     elif w in ("outliers", "edge", "tiny"):
         if w == "outliers":

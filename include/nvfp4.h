@@ -276,6 +276,25 @@ NVFP4_API nvfp4_status nvfp4_quantize_columnwise_rht(const void *x, int32_t in_d
                                                      nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_both_rht -- both directions in one encode pass, the transform on the
+ * transposed side only ([TE-3206]: the fprop operand as it is, the wgrad operand
+ * rotated): row = nvfp4_quantize_rowwise(x, cfg), col =
+ * nvfp4_quantize_columnwise_rht(x, sign_mask, cfg), byte for byte.
+ *   cfg: 1x16 blocks only (block_2d == 1: NVFP4_ERR_UNSUPPORTED); both modes;
+ *   four-over-six allowed.  With NVFP4_PER_TENSOR each direction has its own tensor
+ *   amax (of x, of the transform).  row->amax_in / col->amax_in, if given, are taken
+ *   as the amax of x / of the transform.
+ *   rows a multiple of 16; x rows 16-byte aligned (cols * element size a multiple of
+ *   16, x 16-byte aligned), else NVFP4_ERR_UNSUPPORTED.  Nothing is enqueued when a
+ *   check fails.  noop as for every call.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_both_rht(const void *x, int32_t in_dtype, int64_t rows,
+                                               int64_t cols, uint32_t sign_mask,
+                                               const nvfp4_config *cfg, const nvfp4_out *row,
+                                               const nvfp4_out *col, const float *noop,
+                                               nvfp4_stream_t stream);
+
+/*
  * One operand of nvfp4_gemm: an NVFP4 tensor in K-major layout -- a rowwise output
  * (lines = rows of x) or a columnwise output (lines = columns of x, the operand
  * that enters the GEMM transposed).

@@ -473,6 +473,94 @@ nvfp4_status nvfp4_quantize_columnwise_rht(const void* x, int32_t in_dtype, int6
   return quantize_impl(workspace, NVFP4_IN_FP32, rows, cols, cfg, nullptr, col, noop, stream);
 }
 
+nvfp4_status nvfp4_quantize_both_rht(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                     uint32_t sign_mask, const nvfp4_config* cfg,
+                                     const nvfp4_out* row, const nvfp4_out* col,
+                                     const float* noop, nvfp4_stream_t stream) {
+  // every argument is checked before the first launch, so a rejected call enqueues nothing
+  nvfp4_status st = check_rht(x, in_dtype, rows, cols, sign_mask);
+  if (st != NVFP4_OK) return st;
+  if ((st = check_config(cfg)) != NVFP4_OK) return st;
+  if (cfg->block_2d)
+    return fail(NVFP4_ERR_UNSUPPORTED, "the two-direction transform quantize uses 1x16 blocks");
+  if (row == nullptr || col == nullptr) return fail(NVFP4_ERR_INVALID, "row and col must be non-NULL");
+  const bool rs = cfg->mode == NVFP4_ROW_SCALED;
+  const int64_t n_r = rs ? rows : 1, n_c = rs ? cols : 1;
+  if ((st = check_out(row, "row", rows, cols, n_r)) != NVFP4_OK) return st;
+  if ((st = check_out(col, "col", cols, rows, n_c)) != NVFP4_OK) return st;
+  const int elem = in_dtype == NVFP4_IN_FP32 ? 4 : 2;
+  if (rows * cols > 0 &&
+      ((cols * elem) % 16 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0))
+    return fail(NVFP4_ERR_UNSUPPORTED, "x rows must be 16-byte aligned");
+  DeviceInfo dev{};
+  if ((st = current_device(&dev)) != NVFP4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const InType in = in_dtype == NVFP4_IN_BF16 ? InType::BF16 : InType::FP32;
+  const bool need_r = row->amax_in == nullptr, need_c = col->amax_in == nullptr;
+  // 1. clear the amax outputs (or copy the given ones), after the noop check
+  PrepArgs prep{};
+  int nz = 0, nc = 0;
+  if (need_r) {
+    prep.zero_ptr[nz] = row->amax;
+    prep.zero_n[nz++] = n_r;
+  } else if (row->amax != row->amax_in) {
+    prep.copy_dst[nc] = row->amax;
+    prep.copy_src[nc] = row->amax_in;
+    prep.copy_n[nc++] = n_r;
+  }
+  if (need_c) {
+    prep.zero_ptr[nz] = col->amax;
+    prep.zero_n[nz++] = n_c;
+  } else if (col->amax != col->amax_in) {
+    prep.copy_dst[nc] = col->amax;
+    prep.copy_src[nc] = col->amax_in;
+    prep.copy_n[nc++] = n_c;
+  }
+  prep.noop = noop;
+  cudaError_t e;
+  if (nz + nc > 0 && (e = launch_prep(prep, dev, s)) != cudaSuccess)
+    return cuda_fail(e, "prep launch");
+  // 2. the transposed side's amax is the transform's; the rowwise side's is x's
+  if (need_c) {
+    RhtAmaxArgs ra{x, in == InType::BF16, rows, cols, sign_mask, rs ? col->amax : nullptr,
+                   rs ? nullptr : col->amax, noop};
+    if ((e = launch_rht16_amax(ra, dev, s)) != cudaSuccess)
+      return cuda_fail(e, "transform amax launch");
+  }
+  if (need_r) {
+    AmaxArgs am{};
+    am.x = x;
+    am.in = in;
+    am.M = rows;
+    am.K = cols;
+    am.row_amax = rs ? row->amax : nullptr;
+    am.tensor_amax = rs ? nullptr : row->amax;
+    am.noop = noop;
+    if ((e = launch_amax(am, dev, s)) != cudaSuccess) return cuda_fail(e, "amax launch");
+  }
+  // 3. one encode pass: rows as they are, columns transformed block by block
+  QuantArgs q{};
+  q.x = x;
+  q.in = in;
+  q.M = rows;
+  q.K = cols;
+  q.row_scaled = rs;
+  q.four_over_six = cfg->four_over_six != 0;
+  q.block_2d = false;
+  q.bound = cfg->bound;
+  q.noop = noop;
+  q.rht = true;
+  q.rht_mask = sign_mask;
+  q.row_codes = row->codes;
+  q.row_scales = row->scales;
+  q.row_amax = row->amax;
+  q.col_codes = col->codes;
+  q.col_scales = col->scales;
+  q.col_amax = col->amax;
+  if ((e = launch_quantize(q, dev, s)) != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const float* amax,
                               int32_t mode, int64_t rows, int64_t cols, float bound, void* out,
                               int32_t out_dtype, nvfp4_stream_t stream) {

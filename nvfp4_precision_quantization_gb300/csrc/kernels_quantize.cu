@@ -805,8 +805,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   // Columnwise scale bytes of the first three tile rows of a column's 32-byte
   // scale sector, per tile of the super-strip row and column, held until the CTA
   // reaches the fourth (4 tiles apart in its walk): [tile][column][visit][row half].
-  __shared__ uint32_t csb[SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? TileGrid::kGroup : 1]
-                         [SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? 128 : 1][3][2];
+  __shared__ uint32_t csb[SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D && !RHT
+                              ? TileGrid::kGroup : 1]
+                         [SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D && !RHT ? 128 : 1]
+                         [3][2];
   __shared__ volatile int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1015,7 +1017,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   // in the order i ^ 4, which puts the two halves on disjoint shared-memory
   // banks; their code words are put back in row order afterwards.  Otherwise
   // consecutive threads take consecutive column pairs.
-  constexpr bool PAIRED = SECT && BOTH && sizeof(T) == 2 && !FOS && !B2D;
+  // (With the transform, each thread needs its 16-row blocks in natural row order.)
+  constexpr bool PAIRED = SECT && BOTH && sizeof(T) == 2 && !FOS && !B2D && !RHT;
   // CPAIR (sector stores, columnwise only, BF16, 1x16): a thread holds 32 rows of a
   // column pair, and neighbouring lanes hold the two 32-row halves of the same 64-row
   // run, so that after one exchange each lane stores one column's 32 code bytes (a
@@ -1236,7 +1239,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     } else if (COL) {
       uint32_t w0[RG / 8], w1[RG / 8];
       uint32_t sc0, sc1;
-      colwise_compute<T, RG, FOS, B2D, ROW && COL, RHT>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1,
+      colwise_compute<T, RG, FOS, B2D, ROW && COL && !RHT, RHT>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1,
                                                    sc0, sc1);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -1386,6 +1389,18 @@ EncodeFn pick_rht(bool fos, bool tma, int outm) {
              : k_encode<T, false, true, false, false, false, kOutDirect, true>;
 }
 
+// Both directions, 1x16 blocks, the columnwise blocks transformed first (TMA loads).
+template <typename T>
+EncodeFn pick_rht_both(bool fos, int outm) {
+  if constexpr (sizeof(T) == 2) {
+    if (outm == kOutSector)
+      return fos ? k_encode<T, true, true, true, false, true, kOutSector, true>
+                 : k_encode<T, true, true, false, false, true, kOutSector, true>;
+  }
+  return fos ? k_encode<T, true, true, true, false, true, kOutDirect, true>
+             : k_encode<T, true, true, false, false, true, kOutDirect, true>;
+}
+
 template <typename T>
 EncodeFn pick_dir(bool row, bool col, bool fos, bool b2d, bool tma, int outm) {
   if (row && col) return pick_mode<T, true, true>(fos, b2d, tma, outm);
@@ -1443,8 +1458,8 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.in_rows = q.pad_ends != nullptr ? q.in_rows : q.M;
   a.rht_mask = q.rht_mask;
   if (a.grid.num_tiles == 0) return cudaSuccess;
-  if (q.rht && (row || q.block_2d || q.col_grouped || q.pad_ends != nullptr))
-    return cudaErrorInvalidValue;  // the transform is built for the plain columnwise path
+  if (q.rht && (q.block_2d || q.col_grouped || q.pad_ends != nullptr))
+    return cudaErrorInvalidValue;  // the transform is built for the plain 1x16 paths
 
   CUtensorMap map, map_rc, map_cc;
   memset(&map_rc, 0, sizeof(map_rc));
@@ -1463,6 +1478,9 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
              make_byte_map(&map_cc, q.col_codes, q.K, a.col_cpitch, 32, 64))
       outm = kOutTma;
   }
+  // the transform with both directions: sector or direct stores only
+  if (q.rht && both && outm == kOutTma) outm = kOutDirect;
+  if (q.rht && both && !tma) return cudaErrorInvalidValue;  // rows of x not TMA-aligned
   // columnwise only (BF16, 1x16): whole-sector code stores from lane pairs
   if (bf16 && tma && col && !row && !q.block_2d && a.col_cpitch % 32 == 0 &&
       aligned(q.col_codes, 32) && a.col_spitch % 4 == 0 && aligned(q.col_scales, 4))
@@ -1494,8 +1512,10 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.row_scale_groups = (tout && both && bf16 && a.row_spitch % 32 == 0 &&
                         aligned(q.row_scales, 32)) ? 1 : 0;
 
-  EncodeFn fn = q.rht ? (bf16 ? pick_rht<uint16_t>(q.four_over_six, tma, outm)
-                              : pick_rht<float>(q.four_over_six, tma, outm))
+  EncodeFn fn = q.rht ? (both ? (bf16 ? pick_rht_both<uint16_t>(q.four_over_six, outm)
+                                     : pick_rht_both<float>(q.four_over_six, outm))
+                              : bf16 ? pick_rht<uint16_t>(q.four_over_six, tma, outm)
+                                     : pick_rht<float>(q.four_over_six, tma, outm))
                : bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, outm)
                       : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, outm);
   const int smem = outm == kOutTma ? EncodeSmem<kOutTma>::kBytes

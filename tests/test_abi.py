@@ -149,6 +149,37 @@ def test_rht_host_validation_without_gpu(lib_path):
     assert st == nv.NVFP4_ERR_UNSUPPORTED
 
 
+def test_both_rht_host_validation_without_gpu(lib_path):
+    """The two-direction transform quantize rejects what it does not cover before any
+    CUDA call: 16x16 blocks, rows not a multiple of 16, x rows not 16-byte aligned, a
+    missing direction."""
+    import nvfp4_precision_quantization_gb300 as nv
+    L = nv.load_library()
+    R = ctypes.byref
+    cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
+    row = nv._COut(1024, 2048, 4096, None)
+    col = nv._COut(8192, 16384, 32768, None)
+    st = L.nvfp4_quantize_both_rht(256, nv.NVFP4_IN_BF16, 40, 64, 0, R(cfg), R(row), R(col),
+                                   None, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "multiple of 16" in nv.nvfp4_last_error()
+    tiles = nv.Config(nv.NVFP4_PER_TENSOR, 448.0, 0, 1)
+    st = L.nvfp4_quantize_both_rht(256, nv.NVFP4_IN_BF16, 32, 64, 0, R(tiles), R(row), R(col),
+                                   None, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "1x16" in nv.nvfp4_last_error()
+    st = L.nvfp4_quantize_both_rht(256, nv.NVFP4_IN_BF16, 32, 64, 0, R(cfg), None, R(col),
+                                   None, None)
+    assert st == nv.NVFP4_ERR_INVALID
+    st = L.nvfp4_quantize_both_rht(256, nv.NVFP4_IN_BF16, 32, 36, 0, R(cfg), R(row), R(col),
+                                   None, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "16-byte" in nv.nvfp4_last_error()
+    st = L.nvfp4_quantize_both_rht(264, nv.NVFP4_IN_FP32, 32, 64, 0, R(cfg), R(row), R(col),
+                                   None, None)
+    assert st == nv.NVFP4_ERR_UNSUPPORTED and "16-byte" in nv.nvfp4_last_error()
+    st = L.nvfp4_quantize_both_rht(256, nv.NVFP4_IN_BF16, 32, 64, 0x10000, R(cfg), R(row),
+                                   R(col), None, None)
+    assert st == nv.NVFP4_ERR_INVALID and "sign_mask" in nv.nvfp4_last_error()
+
+
 def test_overlap_and_selftest_validation_without_gpu(lib_path):
     """Overlapping buffers of the transform and the self-test's limits are rejected on
     the host, before any CUDA call."""

@@ -197,3 +197,99 @@ def test_wgrad_gemm_on_transformed_operands():
     assert np.all(np.abs(got - exact) <= _bound(tokens, dabs, exact, False))
     ref = dy_t.float().cpu().numpy().astype(np.float64).T @ x_t.float().cpu().numpy().astype(np.float64)
     assert np.linalg.norm(got - ref) < 0.2 * np.linalg.norm(ref)
+
+
+# ---------------------------------------------------------------- both directions
+
+def _both_expected(x, mask, conf, parallel=False):
+    """Rowwise quantization of x and columnwise quantization of its transform, each
+    from the oracle on its own."""
+    xb, tag = host_bits(x)
+    kw = dict(mode=conf[0], bound=conf[1], four_over_six=conf[2])
+    if parallel:
+        row = oracle.quantize_parallel(xb, tag, columnwise=False, **kw)["row"]
+        col = oracle.quantize_parallel(oracle.rht16(xb, tag, mask), "fp32", rowwise=False,
+                                       **kw)["col"]
+    else:
+        row = oracle.quantize(xb, tag, columnwise=False, **kw)["row"]
+        col = oracle.quantize_columnwise_rht(xb, tag, mask, **kw)
+    return row, col
+
+
+def _both_gpu(x, mask, conf, noop=None, fill=None, amax_in=(None, None)):
+    rows, cols = x.shape
+    rs = conf[0] == nv.NVFP4_ROW_SCALED
+    row = nv.alloc_out(rows, cols, rows if rs else 1, DEV, fill)
+    col = nv.alloc_out(cols, rows, cols if rs else 1, DEV, fill)
+    row.amax_in, col.amax_in = amax_in
+    nv.nvfp4_quantize_both_rht(x, mask, cfg(*conf), row, col, noop=noop)
+    torch.cuda.synchronize()
+    return row, col
+
+
+BOTH_CONFIGS = [c for c in CONFIGS if not c[3]]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+# (512, 1024), (256, 256): code pitches multiples of 32 bytes (BF16: sector stores);
+# (2048, 384): 16 but not 32 (direct stores); (272, 40): a last tile of 16 rows;
+# (16, 8): one block
+@pytest.mark.parametrize("shape", [(512, 1024), (256, 256), (2048, 384), (272, 40), (16, 8),
+                                   (1024, 96)])
+@pytest.mark.parametrize("conf", BOTH_CONFIGS)
+def test_quantize_both_rht_matches_oracle(dtype, shape, conf):
+    """Both directions in one encode pass, the transform on the columnwise side only
+    ("NVFP4: enable row-scaled transpose quantization for backward", TE PR #3206,
+    description: rowwise for fprop, the transposed operand for wgrad)."""
+    rows, cols = shape
+    x = _input(rows, cols, dtype, seed=31 + rows + cols)
+    mask = 0x5A3C
+    row, col = _both_gpu(x, mask, conf)
+    er, ec = _both_expected(x, mask, conf)
+    assert_same(row, er, f"both-rht row {shape} {conf}")
+    assert_same(col, ec, f"both-rht col {shape} {conf}")
+
+
+@pytest.mark.parametrize("conf", BOTH_CONFIGS)
+def test_quantize_both_rht_multitile(conf):
+    """4096 x 4096 BF16 (1024 tiles, several per CTA, sector stores) and 2048 x 3000
+    FP32 (direct stores), compared in full with the oracle run in host threads."""
+    for x in (workloads.outliers(DEV), _input(2048, 3000, torch.float32, seed=41)):
+        row, col = _both_gpu(x, 0x6D2B, conf)
+        er, ec = _both_expected(x, 0x6D2B, conf, parallel=True)
+        assert_same(row, er, f"both-rht row {tuple(x.shape)} {conf}")
+        assert_same(col, ec, f"both-rht col {tuple(x.shape)} {conf}")
+
+
+def test_quantize_both_rht_equals_the_two_calls():
+    """The one-pass call gives the bytes of the rowwise quantize of x and the fused
+    columnwise quantize of its transform, called separately."""
+    x = _input(2048, 3584, torch.bfloat16, seed=42)
+    for conf in BOTH_CONFIGS:
+        c = cfg(*conf)
+        rs = conf[0] == nv.NVFP4_ROW_SCALED
+        row, col = _both_gpu(x, 0x0F0F, conf)
+        r2 = nv.alloc_out(2048, 3584, 2048 if rs else 1, DEV)
+        nv.nvfp4_quantize_rowwise(x, c, r2)
+        c2 = nv.alloc_out(3584, 2048, 3584 if rs else 1, DEV)
+        nv.nvfp4_quantize_columnwise_rht(x, 0x0F0F, c, c2)
+        torch.cuda.synchronize()
+        for a, b in ((row, r2), (col, c2)):
+            assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+            assert torch.equal(a.amax, b.amax)
+
+
+def test_quantize_both_rht_given_amax_and_noop():
+    x = _input(512, 256, torch.bfloat16, seed=43)
+    conf = (nv.NVFP4_PER_TENSOR, 448.0, False, False)
+    ref_r, ref_c = _both_gpu(x, 0x2468, conf)
+    # given maxima: the row one is x's, the column one the transform's
+    row, col = _both_gpu(x, 0x2468, conf, amax_in=(ref_r.amax.clone(), ref_c.amax.clone()))
+    for a, b in ((row, ref_r), (col, ref_c)):
+        assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+        assert torch.equal(a.amax, b.amax)
+    assert not torch.equal(ref_r.amax, ref_c.amax)  # two different tensors
+    noop = torch.ones(1, dtype=torch.float32, device=DEV)
+    row, col = _both_gpu(x, 0x2468, conf, noop=noop, fill=0xA5)
+    for o in (row, col):
+        assert bool((o.codes == 0xA5).all()) and bool((o.scales == 0xA5).all())
