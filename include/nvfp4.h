@@ -276,6 +276,23 @@ NVFP4_API nvfp4_status nvfp4_quantize_columnwise_rht(const void *x, int32_t in_d
                                                      nvfp4_stream_t stream);
 
 /*
+ * nvfp4_grouped_quantize_columnwise_rht -- nvfp4_grouped_quantize_columnwise of the
+ * transform nvfp4_rht16(x, sign_mask): each group's rows rotated block by block and
+ * quantized columnwise with that group's amax of the transform (the wgrad operands
+ * of the per-expert GEMMs with their 16-token blocks rotated).  Every rule of
+ * nvfp4_grouped_quantize_columnwise applies (group ends multiples of 128, 1x16
+ * blocks, 16-byte aligned rows of x); sign_mask < 2^16.  col->amax_in, if given, is
+ * taken as the groups' amax of the transform.
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_quantize_columnwise_rht(const void *x, int32_t in_dtype,
+                                                   int64_t rows, int64_t cols,
+                                                   const int64_t *group_ends,
+                                                   int32_t num_groups, uint32_t sign_mask,
+                                                   const nvfp4_config *cfg,
+                                                   const nvfp4_out *col, const float *noop,
+                                                   nvfp4_stream_t stream);
+
+/*
  * nvfp4_quantize_both_rht -- both directions in one encode pass, the transform on the
  * transposed side only ([TE-3206]: the fprop operand as it is, the wgrad operand
  * rotated): row = nvfp4_quantize_rowwise(x, cfg), col =

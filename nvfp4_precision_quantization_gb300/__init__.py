@@ -31,6 +31,7 @@ __all__ = [
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
     "NVFP4_GEMM_STATIC_WS_BYTES", "alloc_out", "EXPORTED_SYMBOLS", "nvfp4_rht16",
     "nvfp4_quantize_columnwise_rht", "nvfp4_quantize_both_rht",
+    "nvfp4_grouped_quantize_columnwise_rht",
 ]
 
 NVFP4_OK = 0
@@ -57,6 +58,7 @@ EXPORTED_SYMBOLS = (
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_static_ws",
     "nvfp4_grouped_gemm_workspace_size", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_wgrad",
     "nvfp4_rht16", "nvfp4_quantize_columnwise_rht", "nvfp4_quantize_both_rht",
+    "nvfp4_grouped_quantize_columnwise_rht",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -140,6 +142,8 @@ def load_library():
         "nvfp4_quantize_columnwise_rht": [vp, i32, i64, i64, C.c_uint32, vp, vp, vp, C.c_uint64,
                                           vp, vp],
         "nvfp4_quantize_both_rht": [vp, i32, i64, i64, C.c_uint32, vp, vp, vp, vp, vp],
+        "nvfp4_grouped_quantize_columnwise_rht": [vp, i32, i64, i64, vp, i32, C.c_uint32, vp, vp,
+                                                  vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -236,6 +240,17 @@ def nvfp4_quantize_columnwise_rht(x: torch.Tensor, sign_mask: int, cfg: Config, 
     _check(load_library().nvfp4_quantize_columnwise_rht(
         _ptr(x), _in_dtype(x), rows, cols, sign_mask, C.byref(cfg), C.byref(c), _ptr(workspace),
         nbytes, _ptr(noop), _stream(stream)))
+
+
+def nvfp4_grouped_quantize_columnwise_rht(x: torch.Tensor, group_ends: torch.Tensor,
+                                          sign_mask: int, cfg: Config, col: Out, noop=None,
+                                          stream=None) -> None:
+    """Grouped columnwise quantization of the transformed x (each group's amax)."""
+    rows, cols = _matrix(x)
+    c = col._c()
+    _check(load_library().nvfp4_grouped_quantize_columnwise_rht(
+        _ptr(x), _in_dtype(x), rows, cols, _ptr(group_ends), group_ends.numel(), sign_mask,
+        C.byref(cfg), C.byref(c), _ptr(noop), _stream(stream)))
 
 
 def nvfp4_quantize_both_rht(x: torch.Tensor, sign_mask: int, cfg: Config, row: Out, col: Out,

@@ -934,12 +934,15 @@ nvfp4_status nvfp4_grouped_quantize_rowwise_padded(
   return NVFP4_OK;
 }
 
-nvfp4_status nvfp4_grouped_quantize_columnwise(const void* x, int32_t in_dtype, int64_t rows,
-                                               int64_t cols, const int64_t* group_ends,
-                                               int32_t num_groups, const nvfp4_config* cfg,
-                                               const nvfp4_out* col, const float* noop,
-                                               nvfp4_stream_t stream) {
+namespace {
+// The grouped columnwise quantize, of x or (rht) of its transform.
+nvfp4_status grouped_columnwise_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                     const int64_t* group_ends, int32_t num_groups,
+                                     const nvfp4_config* cfg, const nvfp4_out* col,
+                                     const float* noop, nvfp4_stream_t stream, bool rht,
+                                     uint32_t sign_mask) {
   nvfp4_status st;
+  if (rht && (st = check_rht(x, in_dtype, rows, cols, sign_mask)) != NVFP4_OK) return st;
   if (!valid_in_dtype(in_dtype)) return fail(NVFP4_ERR_INVALID, "unknown in_dtype");
   if ((st = check_sizes(rows, cols)) != NVFP4_OK) return st;
   if ((st = check_config(cfg)) != NVFP4_OK) return st;
@@ -977,7 +980,15 @@ nvfp4_status nvfp4_grouped_quantize_columnwise(const void* x, int32_t in_dtype, 
   }
   cudaError_t e = launch_group_check(g, dev, stream, false);
   if (e != cudaSuccess) return cuda_fail(e, "group check launch");
-  if (col->amax_in == nullptr) {
+  if (col->amax_in == nullptr && rht) {
+    // each group's column maxima (or maximum) of the transform, read-only
+    RhtAmaxArgs ra{x, in == InType::BF16, rows, cols, sign_mask, rs ? col->amax : nullptr,
+                   rs ? nullptr : col->amax, noop};
+    ra.group_ends = group_ends;
+    ra.num_groups = num_groups;
+    if ((e = launch_rht16_amax(ra, dev, stream)) != cudaSuccess)
+      return cuda_fail(e, "transform amax launch");
+  } else if (col->amax_in == nullptr) {
     if (rs) {
       // each group's column maxima: the TMA amax pass publishing per group
       AmaxArgs am{};
@@ -1024,8 +1035,29 @@ nvfp4_status nvfp4_grouped_quantize_columnwise(const void* x, int32_t in_dtype, 
   q.num_groups = num_groups;
   q.col_grouped = true;
   q.col_grouped_per_tensor = !rs;
+  q.rht = rht;
+  q.rht_mask = sign_mask;
   if ((e = launch_quantize(q, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize");
   return NVFP4_OK;
+}
+}  // namespace
+
+nvfp4_status nvfp4_grouped_quantize_columnwise(const void* x, int32_t in_dtype, int64_t rows,
+                                               int64_t cols, const int64_t* group_ends,
+                                               int32_t num_groups, const nvfp4_config* cfg,
+                                               const nvfp4_out* col, const float* noop,
+                                               nvfp4_stream_t stream) {
+  return grouped_columnwise_impl(x, in_dtype, rows, cols, group_ends, num_groups, cfg, col, noop,
+                                 stream, false, 0);
+}
+
+nvfp4_status nvfp4_grouped_quantize_columnwise_rht(const void* x, int32_t in_dtype, int64_t rows,
+                                                   int64_t cols, const int64_t* group_ends,
+                                                   int32_t num_groups, uint32_t sign_mask,
+                                                   const nvfp4_config* cfg, const nvfp4_out* col,
+                                                   const float* noop, nvfp4_stream_t stream) {
+  return grouped_columnwise_impl(x, in_dtype, rows, cols, group_ends, num_groups, cfg, col, noop,
+                                 stream, true, sign_mask);
 }
 
 const char* nvfp4_last_error(void) { return g_last_error.c_str(); }

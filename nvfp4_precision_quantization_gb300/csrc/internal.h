@@ -181,6 +181,9 @@ struct RhtAmaxArgs {
   float* col_amax;
   float* tensor_amax;
   const float* noop;
+  // optional grouped rows (ends multiples of 128): col_amax [G][cols] or tensor_amax [G]
+  const int64_t* group_ends = nullptr;
+  int num_groups = 0;
 };
 cudaError_t launch_rht16_amax(const RhtAmaxArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 

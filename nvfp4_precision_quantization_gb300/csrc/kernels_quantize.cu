@@ -1458,8 +1458,8 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.in_rows = q.pad_ends != nullptr ? q.in_rows : q.M;
   a.rht_mask = q.rht_mask;
   if (a.grid.num_tiles == 0) return cudaSuccess;
-  if (q.rht && (q.block_2d || q.col_grouped || q.pad_ends != nullptr))
-    return cudaErrorInvalidValue;  // the transform is built for the plain 1x16 paths
+  if (q.rht && (q.block_2d || q.pad_ends != nullptr || (q.col_grouped && row)))
+    return cudaErrorInvalidValue;  // the transform is built for the 1x16 paths
 
   CUtensorMap map, map_rc, map_cc;
   memset(&map_rc, 0, sizeof(map_rc));

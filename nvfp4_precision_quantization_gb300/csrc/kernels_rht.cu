@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16(RhtKernelArgs a) {
 // patterns, so the atomic works on the bits; the result is the exact max whatever
 // the order.
 constexpr int kAmaxBlocks = 16;
+constexpr int kMaxRhtGroups = 4096;
 
 struct RhtAmaxKernelArgs {
   const void* x;
@@ -111,11 +112,25 @@ struct RhtAmaxKernelArgs {
   float* col_amax;
   float* tensor_amax;
   const float* noop;
+  // grouped rows (group ends multiples of 128): col_amax is [G][cols] (each group's
+  // column maxima) or tensor_amax is [G] (each group's maximum)
+  const int64_t* ends;
+  int G;
 };
 
 template <bool BF16, int V>
 __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax(RhtAmaxKernelArgs a) {
+  __shared__ float s_gmax[kMaxRhtGroups];  // grouped per-group maxima of this CTA
   if (a.noop != nullptr && *a.noop == 1.0f) return;
+  const bool grouped = a.ends != nullptr;
+  const bool group_tensor = grouped && a.tensor_amax != nullptr;
+  if (grouped) {
+    if (!groups_valid(a.ends, a.G, a.rows) || !ends_aligned(a.ends, a.G, 128)) return;
+    if (group_tensor) {
+      for (int g = threadIdx.x; g < a.G; g += kRhtThreads) s_gmax[g] = 0.0f;
+      __syncthreads();
+    }
+  }
   const int64_t stride = (int64_t)gridDim.x * kRhtThreads;
   const int64_t row_blocks = a.rows / 16;
   float tmax = 0.0f;  // per-tensor: this thread's max over all its items
@@ -127,7 +142,44 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax(RhtAmaxKernelArgs a)
     float cmax[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) cmax[k] = 0.0f;
+    // grouped: the group of the current row block, and where it ends
+    int g = 0;
+    int64_t g_end = a.rows;
+    if (grouped) {
+      const int64_t r0 = ch * kAmaxBlocks * 16;
+      int lo = 0, hi = a.G;  // first group whose end is > r0
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a.ends + mid) <= r0) lo = mid + 1;
+        else hi = mid;
+      }
+      g = lo;
+      g_end = __ldg(a.ends + g);
+    }
+    // publish the maxima of group g's rows seen so far
+    auto flush = [&]() {
+      if (group_tensor) {
+        float m = cmax[0];
+#pragma unroll
+        for (int k = 1; k < V; ++k) m = fmaxf(m, cmax[k]);
+        if (m > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(s_gmax + g), __float_as_uint(m));
+      } else {
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+          if (cmax[k] > 0.0f)
+            atomicMax(reinterpret_cast<unsigned int*>(a.col_amax + (int64_t)g * a.cols + c0 + k),
+                      __float_as_uint(cmax[k]));
+      }
+#pragma unroll
+      for (int k = 0; k < V; ++k) cmax[k] = 0.0f;
+    };
     for (int64_t rb = ch * kAmaxBlocks; rb < rb1; ++rb) {
+      if (grouped && rb * 16 >= g_end) {
+        flush();
+        do {
+          g_end = __ldg(a.ends + ++g);
+        } while (rb * 16 >= g_end);
+      }
       const int64_t base = rb * 16 * a.cols + c0;
       float v[V][16];
 #pragma unroll
@@ -160,6 +212,10 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax(RhtAmaxKernelArgs a)
         for (int r = 0; r < 16; ++r) cmax[k] = fmaxf(cmax[k], fabsf(v[k][r]));
       }
     }
+    if (grouped) {
+      flush();
+      continue;
+    }
     if (a.col_amax != nullptr) {
 #pragma unroll
       for (int k = 0; k < V; ++k)
@@ -168,6 +224,14 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax(RhtAmaxKernelArgs a)
 #pragma unroll
     for (int k = 0; k < V; ++k) tmax = fmaxf(tmax, cmax[k]);
   }
+  if (group_tensor) {
+    __syncthreads();
+    for (int gg = threadIdx.x; gg < a.G; gg += kRhtThreads)
+      if (s_gmax[gg] > 0.0f)
+        atomicMax(reinterpret_cast<unsigned int*>(a.tensor_amax + gg), __float_as_uint(s_gmax[gg]));
+    return;
+  }
+  if (grouped) return;
   if (a.tensor_amax != nullptr) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
@@ -198,6 +262,9 @@ cudaError_t launch_rht16_amax(const RhtAmaxArgs& q, const DeviceInfo& dev, cudaS
   a.col_amax = q.col_amax;
   a.tensor_amax = q.tensor_amax;
   a.noop = q.noop;
+  a.ends = q.group_ends;
+  a.G = q.num_groups;
+  if (a.ends != nullptr && (a.G < 1 || a.G > kMaxRhtGroups)) return cudaErrorInvalidValue;
   const int64_t blocks =
       std::min<int64_t>((a.items + kRhtThreads - 1) / kRhtThreads, 8LL * dev.num_sms);
   void (*fn)(RhtAmaxKernelArgs);

@@ -18,9 +18,12 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _expected(x, ends, c):
-    """Oracle, one group at a time, concatenated along the token axis."""
+def _expected(x, ends, c, mask=None):
+    """Oracle, one group at a time, concatenated along the token axis (mask: of the
+    transform of x instead of x)."""
     xb, tag = host_bits(x)
+    if mask is not None:
+        xb, tag = oracle.rht16(xb, tag, mask), "fp32"
     rows, cols = xb.shape
     codes = np.zeros((cols, rows // 2), np.uint8)
     scales = np.zeros((cols, rows // 16), np.uint8)
@@ -38,7 +41,7 @@ def _expected(x, ends, c):
     return codes, scales, amax
 
 
-def _run(x, ends, c, amax_in=None, fill=None):
+def _run(x, ends, c, amax_in=None, fill=None, mask=None, noop=None):
     rows, cols = x.shape
     G = len(ends)
     rs = c.mode == nv.NVFP4_ROW_SCALED
@@ -46,8 +49,11 @@ def _run(x, ends, c, amax_in=None, fill=None):
     if fill is not None:
         col.amax.fill_(-1.0)
     col.amax_in = amax_in
-    nv.nvfp4_grouped_quantize_columnwise(x, torch.from_numpy(np.asarray(ends, np.int64)).to(DEV),
-                                         c, col)
+    e = torch.from_numpy(np.asarray(ends, np.int64)).to(DEV)
+    if mask is None:
+        nv.nvfp4_grouped_quantize_columnwise(x, e, c, col, noop=noop)
+    else:
+        nv.nvfp4_grouped_quantize_columnwise_rht(x, e, mask, c, col, noop=noop)
     torch.cuda.synchronize()
     return col
 
@@ -106,3 +112,63 @@ def test_unaligned_ends_write_nothing():
     assert nv.nvfp4_device_status(reset=True) & nv.NVFP4_DEVICE_BAD_GROUPS
     assert bool((col.codes == 0xA5).all()) and bool((col.scales == 0xA5).all())
     assert bool((col.amax == -1.0).all())
+
+
+# ---------------------------------------------------------------- with the transform
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("mode", [nv.NVFP4_ROW_SCALED, nv.NVFP4_PER_TENSOR])
+@pytest.mark.parametrize("fos,bound", [(False, 448.0), (True, 256.0)])
+@pytest.mark.parametrize("cols", [256, 96])
+def test_grouped_columnwise_rht_matches_oracle(dtype, mode, fos, bound, cols):
+    """Each group's rows transformed block by block (16 tokens per block, groups of
+    whole 128-row tiles) and quantized with the group's amax of the transform."""
+    ends = np.cumsum([128, 0, 256, 384, 128])
+    x = workloads.seeded_normal(int(ends[-1]), cols, seed=34, dtype=dtype, device=DEV,
+                                row_scale_decades=1.0)
+    c = cfg(mode, bound, fos)
+    _check(_run(x, ends, c, mask=0xC3A5), _expected(x, ends, c, mask=0xC3A5),
+           "grouped columnwise rht")
+
+
+def test_grouped_columnwise_rht_equals_transform_then_quantize():
+    """The fused call gives the bytes of the transform into a buffer followed by the
+    plain grouped columnwise quantize of that buffer, on the MoE tokens."""
+    xp, ends, _, _ = workloads.moe(DEV)
+    xp = xp[:int(ends[7])]  # the first 8 groups
+    e = ends[:8].contiguous()
+    for c in (cfg(nv.NVFP4_ROW_SCALED, 448.0, False), cfg(nv.NVFP4_PER_TENSOR, 256.0, True)):
+        fused = _run(xp, e.cpu().numpy(), c, mask=0x6D2B)
+        y = torch.empty(xp.shape, dtype=torch.float32, device=DEV)
+        nv.nvfp4_rht16(xp, 0x6D2B, y)
+        two = _run(y, e.cpu().numpy(), c)
+        assert torch.equal(fused.codes, two.codes) and torch.equal(fused.scales, two.scales)
+        assert torch.equal(fused.amax, two.amax)
+
+
+def test_grouped_columnwise_rht_moe_groups_match_oracle():
+    xp, ends, _, _ = workloads.moe(DEV)
+    c = cfg(nv.NVFP4_ROW_SCALED, 448.0, False)
+    ends_np = ends.cpu().numpy()
+    col = _run(xp, ends_np, c, mask=0x6D2B)
+    for g in (0, len(ends_np) - 1):
+        s, e = (int(ends_np[g - 1]) if g else 0), int(ends_np[g])
+        xb, tag = host_bits(xp[s:e])
+        o = oracle.quantize_columnwise_rht(xb, tag, 0x6D2B, mode=c.mode, bound=c.bound)
+        assert np.array_equal(col.codes[:, s // 2:e // 2].cpu().numpy(), o[0]), g
+        assert np.array_equal(col.scales[:, s // 16:e // 16].cpu().numpy(), o[1]), g
+        assert np.array_equal(col.amax.view(len(ends_np), -1)[g].cpu().numpy(), o[2]), g
+
+
+def test_grouped_columnwise_rht_unaligned_ends_and_noop_write_nothing():
+    x = workloads.seeded_normal(256, 128, seed=35, device=DEV)
+    nv.nvfp4_device_status(reset=True)
+    col = _run(x, np.array([100, 256], np.int64), cfg(nv.NVFP4_ROW_SCALED, 448.0, False),
+               fill=0xA5, mask=0x1)
+    assert nv.nvfp4_device_status(reset=True) & nv.NVFP4_DEVICE_BAD_GROUPS
+    assert bool((col.codes == 0xA5).all()) and bool((col.scales == 0xA5).all())
+    assert bool((col.amax == -1.0).all())
+    noop = torch.ones(1, dtype=torch.float32, device=DEV)
+    col = _run(x, np.array([128, 256], np.int64), cfg(nv.NVFP4_PER_TENSOR, 448.0, False),
+               fill=0xA5, mask=0x1, noop=noop)
+    assert bool((col.codes == 0xA5).all()) and bool((col.amax == -1.0).all())
