@@ -5,7 +5,21 @@
 // TransformerEngine PR #3454, description: both directions in one kernel; amax
 // is an exact max, so the result is byte-identical to separate reductions).
 //
-// Layout of the work: a CTA owns an item of RB rows x CW columns.  Each thread
+// Kernels:
+//   k_amax_tma      the pass for x whose rows TMA can describe: persistent, a ring of
+//                   128-row x 256-byte tiles in the encode kernel's tile order
+//                   (tile_pipeline.cuh), walked the other way so the encode pass
+//                   finds the tail in L2; row, column (per tensor or per row group)
+//                   and tensor maxima.
+//   k_amax_bf16 / k_amax_f32
+//                   the same maxima for any x with plain 128-bit loads (below).
+//   k_grouped_amax  per-group maxima with plain loads (no per-row output to use).
+//   k_group_reduce  per-group maxima from per-row maxima, written back to the rows.
+//   k_group_check   validates group ends and clears or copies the outputs.
+//   k_prep          clears or copies the outputs after the noop check.
+// Every kernel checks the noop flag first.
+//
+// k_amax_bf16 / k_amax_f32: a CTA owns an item of RB rows x CW columns.  Each thread
 // owns 16 bytes of columns (8 BF16 or 4 FP32) and walks down its rows with 8
 // independent 128-bit loads in flight; its column maxima stay in registers for
 // the whole item.  Row maxima are reduced across the warp with a transposing

@@ -17,13 +17,23 @@
 // thread = one row, 128 bytes of each box) and warps 4-7 encode columns (a thread
 // = a column pair over 64 rows).  Each consumer warp releases a stage through an
 // "empty" mbarrier, so warps never wait for each other.  Shared-memory reads are
-// bank-conflict free under the swizzle.  Codes leave as whole 32-byte sectors:
-// one 256-bit store per thread (a row's 64 code bytes of a tile are two sectors,
-// so are a column's), or, when the code pitches are only 16-byte aligned,
-// through per-warp shared-memory staging and TMA tensor stores.  A rowwise
-// thread keeps its row's scale bytes for the 4 tiles of a super-strip row and
-// writes the 32-byte sector once; columnwise scale bytes are written per tile
-// with an L2 evict_last hint so the sector completes in L2.
+// bank-conflict free under the swizzle.  Output paths (OutMode):
+//   sector  code pitches multiples of 32 bytes: whole 32-byte sectors, one 256-bit
+//           store per thread; with both directions (no four-over-six) the two
+//           halves of a row's or a column's run sit in neighbouring lanes (PAIRED),
+//           columnwise only the two 32-row halves of a column's run do (CPAIR).
+//           A rowwise thread keeps its row's scale bytes for the 4 tiles of a
+//           super-strip row and writes the 32-byte sector once; columnwise scale
+//           bytes are collected per 4 tile rows or written per tile with an L2
+//           evict_last hint so the sector completes in L2.
+//   TMA     code pitches multiples of 16 bytes: per-warp shared-memory staging and
+//           TMA tensor stores.
+//   direct  any pitch: the widest stores the pitch and base allow on interior
+//           tiles (both directions, no four-over-six: rowwise rows staged per warp
+//           and written back row by row), bytes on edge tiles.
+// Four-over-six with both directions encodes one column block and one row box at a
+// time (instruction cache, registers).  RHT: the columnwise warps transform each
+// 16-row block in registers before encoding it.
 #include <algorithm>
 #include <cstring>
 
