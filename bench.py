@@ -682,11 +682,11 @@ def run_supplementary(args):
             ev[0].record(stream)
             nv.nvfp4_quantize_both_rht(x, RHT_SIGN_MASK, cfg, row, col, stream=stream)
         bio = 2 * M * K + 2 * (M * K // 2 + M * K // 16) + 4 * (M + K)
-        # the floor reads x twice (both maxima in one pass, then the encode); these
-        # kernels read it three times (the row amax and the transform's amax apart)
+        # x is read twice: one pass for x's row maxima and the transform's column
+        # maxima, then the encode
         bmin = bio + 2 * M * K
-        kern, kbytes, launches = ("whole step (prep, transformed column amax, row amax, "
-                                  "encode)"), bmin, 4
+        kern, kbytes, launches = ("whole step (prep, row and transformed column amax, "
+                                  "encode)"), bmin, 3
         dtype, elems = "bf16", M * K
     elif w in ("outliers", "edge", "tiny"):
         if w == "outliers":

@@ -520,23 +520,32 @@ nvfp4_status nvfp4_quantize_both_rht(const void* x, int32_t in_dtype, int64_t ro
   cudaError_t e;
   if (nz + nc > 0 && (e = launch_prep(prep, dev, s)) != cudaSuccess)
     return cuda_fail(e, "prep launch");
-  // 2. the transposed side's amax is the transform's; the rowwise side's is x's
-  if (need_c) {
+  // 2. the transposed side's amax is the transform's; the rowwise side's is x's --
+  //    both from one read of x where the column count allows
+  if (need_c && need_r && rht16_amax_rows_supported(x, in == InType::BF16, cols)) {
     RhtAmaxArgs ra{x, in == InType::BF16, rows, cols, sign_mask, rs ? col->amax : nullptr,
                    rs ? nullptr : col->amax, noop};
-    if ((e = launch_rht16_amax(ra, dev, s)) != cudaSuccess)
-      return cuda_fail(e, "transform amax launch");
-  }
-  if (need_r) {
-    AmaxArgs am{};
-    am.x = x;
-    am.in = in;
-    am.M = rows;
-    am.K = cols;
-    am.row_amax = rs ? row->amax : nullptr;
-    am.tensor_amax = rs ? nullptr : row->amax;
-    am.noop = noop;
-    if ((e = launch_amax(am, dev, s)) != cudaSuccess) return cuda_fail(e, "amax launch");
+    if ((e = launch_rht16_amax_rows(ra, rs ? row->amax : nullptr, rs ? nullptr : row->amax, dev,
+                                    s)) != cudaSuccess)
+      return cuda_fail(e, "transform and row amax launch");
+  } else {
+    if (need_c) {
+      RhtAmaxArgs ra{x, in == InType::BF16, rows, cols, sign_mask, rs ? col->amax : nullptr,
+                     rs ? nullptr : col->amax, noop};
+      if ((e = launch_rht16_amax(ra, dev, s)) != cudaSuccess)
+        return cuda_fail(e, "transform amax launch");
+    }
+    if (need_r) {
+      AmaxArgs am{};
+      am.x = x;
+      am.in = in;
+      am.M = rows;
+      am.K = cols;
+      am.row_amax = rs ? row->amax : nullptr;
+      am.tensor_amax = rs ? nullptr : row->amax;
+      am.noop = noop;
+      if ((e = launch_amax(am, dev, s)) != cudaSuccess) return cuda_fail(e, "amax launch");
+    }
   }
   // 3. one encode pass: rows as they are, columns transformed block by block
   QuantArgs q{};

@@ -186,6 +186,12 @@ struct RhtAmaxArgs {
   int num_groups = 0;
 };
 cudaError_t launch_rht16_amax(const RhtAmaxArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+// The transform's column maxima (a.col_amax / a.tensor_amax) and x's row maxima
+// (row_max [rows] or row_tensor [1]) in one read of x; for column counts whose
+// thread groups fill whole CTAs (rht16_amax_rows_supported), no group ends.
+bool rht16_amax_rows_supported(const void* x, bool bf16, int64_t cols);
+cudaError_t launch_rht16_amax_rows(const RhtAmaxArgs& a, float* row_max, float* row_tensor,
+                                   const DeviceInfo& dev, cudaStream_t stream);
 
 struct GemmArgs {
   const uint8_t* a_codes;

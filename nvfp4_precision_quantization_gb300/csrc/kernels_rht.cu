@@ -240,6 +240,135 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax(RhtAmaxKernelArgs a)
   }
 }
 
+// The transform's column maxima and, in the same read of x, x's own row maxima
+// (the two-direction transform quantize: rows as they are, columns transformed).
+// The CTA's 256 threads take 256 adjacent column groups of one run of kAmaxBlocks row
+// blocks (the launcher requires column groups a multiple of 256), so the loop is
+// uniform over the CTA.  Per row block a warp reduces its 16 rows' |x| maxima over
+// its 32 lanes with a transposing shuffle reduction (16 shuffles, each row ending in
+// a lane pair), the 8 warps combine theirs with shared-memory atomics, and after the
+// run one global atomic per row (row_max [rows]) or one per CTA and run
+// (row_tensor [1]) publishes them.
+struct RhtAmaxRowsArgs {
+  RhtAmaxKernelArgs k;
+  float* row_max;     // [rows] or NULL
+  float* row_tensor;  // [1] or NULL
+};
+
+template <bool BF16, int V>
+__global__ void __launch_bounds__(kRhtThreads) k_rht16_amax_rows(RhtAmaxRowsArgs ra) {
+  const RhtAmaxKernelArgs& a = ra.k;
+  constexpr int kRunRows = kAmaxBlocks * 16;
+  __shared__ float s_rmax[kRunRows];
+  __shared__ float s_red[kRhtThreads / 32];
+  if (a.noop != nullptr && *a.noop == 1.0f) return;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t stride = (int64_t)gridDim.x * kRhtThreads;
+  const int64_t row_blocks = a.rows / 16;
+  // this lane pair's row of a 16-row block after the transposing reduction
+  const int my_row = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                     ((lane >> 1) & 1);
+  float tmax = 0.0f;
+  for (int64_t base = (int64_t)blockIdx.x * kRhtThreads; base < a.items; base += stride) {
+    const int64_t it = base + tid;  // items is a multiple of kRhtThreads
+    const int64_t ch = it / a.groups;
+    const int64_t c0 = (it - ch * a.groups) * V;
+    const int64_t rb0 = ch * kAmaxBlocks, rb1 = min(row_blocks, rb0 + kAmaxBlocks);
+    s_rmax[tid] = 0.0f;  // kRunRows == kRhtThreads
+    __syncthreads();
+    float cmax[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) cmax[k] = 0.0f;
+    for (int64_t rb = rb0; rb < rb1; ++rb) {
+      const int64_t rowbase = rb * 16 * a.cols + c0;
+      float v[V][16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int64_t e = rowbase + r * a.cols;
+        if constexpr (BF16) {
+          const uint16_t* xb = static_cast<const uint16_t*>(a.x);
+          if constexpr (V == 2) {
+            const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(xb + e));
+            v[0][r] = __uint_as_float(w << 16);
+            v[1][r] = __uint_as_float(w & 0xffff0000u);
+          } else {
+            v[0][r] = __uint_as_float((uint32_t)__ldg(xb + e) << 16);
+          }
+        } else {
+          const float* xf = static_cast<const float*>(a.x);
+          if constexpr (V == 2) {
+            const float2 t = __ldg(reinterpret_cast<const float2*>(xf + e));
+            v[0][r] = t.x;
+            v[1][r] = t.y;
+          } else {
+            v[0][r] = __ldg(xf + e);
+          }
+        }
+      }
+      // x's row maxima over this warp's columns: halve the rows held per lane
+      // with each shuffle step (16 -> 8 -> 4 -> 2 -> 1), then the lane pair
+      float m[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        m[r] = fabsf(v[0][r]);
+#pragma unroll
+        for (int k = 1; k < V; ++k) m[r] = fmaxf(m[r], fabsf(v[k][r]));
+      }
+#pragma unroll
+      for (int h = 8; h >= 1; h >>= 1) {
+        const bool up = lane & (2 * h);  // this lane keeps the upper half of its rows
+#pragma unroll
+        for (int j = 0; j < h; ++j) {
+          const float send = up ? m[j] : m[j + h];
+          const float keep = up ? m[j + h] : m[j];
+          m[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2 * h));
+        }
+      }
+      m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
+      if ((lane & 1) == 0 && m[0] > 0.0f)
+        atomicMax(reinterpret_cast<unsigned int*>(s_rmax + 16 * (rb - rb0) + my_row),
+                  __float_as_uint(m[0]));
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        rht16_block(v[k], a.mask);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) cmax[k] = fmaxf(cmax[k], fabsf(v[k][r]));
+      }
+    }
+    if (a.col_amax != nullptr) {
+#pragma unroll
+      for (int k = 0; k < V; ++k)
+        atomicMax(reinterpret_cast<unsigned int*>(a.col_amax + c0 + k), __float_as_uint(cmax[k]));
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) tmax = fmaxf(tmax, cmax[k]);
+    __syncthreads();  // every warp's row maxima of this run are in s_rmax
+    const int64_t r = rb0 * 16 + tid;
+    const float rv = s_rmax[tid];
+    if (ra.row_max != nullptr && r < a.rows && rv > 0.0f)
+      atomicMax(reinterpret_cast<unsigned int*>(ra.row_max + r), __float_as_uint(rv));
+    if (ra.row_tensor != nullptr) {
+      float w = rv;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
+      if (lane == 0) s_red[tid >> 5] = w;
+      __syncthreads();
+      if (tid == 0) {
+        float t = 0.0f;
+        for (int i = 0; i < kRhtThreads / 32; ++i) t = fmaxf(t, s_red[i]);
+        if (t > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(ra.row_tensor), __float_as_uint(t));
+      }
+    }
+    __syncthreads();  // s_rmax and s_red are reused by the next run
+  }
+  if (a.tensor_amax != nullptr) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(a.tensor_amax), __float_as_uint(tmax));
+  }
+}
+static_assert(kAmaxBlocks * 16 == kRhtThreads, "one row of a run per thread");
+
 bool pair_ok(const void* x, bool bf16, int64_t cols, const void* y) {
   const int elem = bf16 ? 2 : 4;
   return cols % 2 == 0 && reinterpret_cast<uintptr_t>(x) % (2 * elem) == 0 &&
@@ -247,6 +376,39 @@ bool pair_ok(const void* x, bool bf16, int64_t cols, const void* y) {
 }
 
 }  // namespace
+
+bool rht16_amax_rows_supported(const void* x, bool bf16, int64_t cols) {
+  const int64_t groups = pair_ok(x, bf16, cols, nullptr) ? cols / 2 : cols;
+  return groups % kRhtThreads == 0;
+}
+
+cudaError_t launch_rht16_amax_rows(const RhtAmaxArgs& q, float* row_max, float* row_tensor,
+                                   const DeviceInfo& dev, cudaStream_t stream) {
+  if (q.rows == 0 || q.cols == 0) return cudaSuccess;
+  if (!rht16_amax_rows_supported(q.x, q.bf16, q.cols) || q.group_ends != nullptr)
+    return cudaErrorInvalidValue;
+  const bool pair = pair_ok(q.x, q.bf16, q.cols, nullptr);
+  RhtAmaxRowsArgs ra{};
+  RhtAmaxKernelArgs& a = ra.k;
+  a.x = q.x;
+  a.rows = q.rows;
+  a.cols = q.cols;
+  a.groups = pair ? q.cols / 2 : q.cols;
+  a.chunks = (q.rows / 16 + kAmaxBlocks - 1) / kAmaxBlocks;
+  a.items = a.chunks * a.groups;
+  a.mask = q.sign_mask;
+  a.col_amax = q.col_amax;
+  a.tensor_amax = q.tensor_amax;
+  a.noop = q.noop;
+  ra.row_max = row_max;
+  ra.row_tensor = row_tensor;
+  const int64_t blocks = std::min<int64_t>(a.items / kRhtThreads, 8LL * dev.num_sms);
+  void (*fn)(RhtAmaxRowsArgs);
+  if (q.bf16) fn = pair ? k_rht16_amax_rows<true, 2> : k_rht16_amax_rows<true, 1>;
+  else fn = pair ? k_rht16_amax_rows<false, 2> : k_rht16_amax_rows<false, 1>;
+  fn<<<(unsigned)blocks, kRhtThreads, 0, stream>>>(ra);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rht16_amax(const RhtAmaxArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
   if (q.rows == 0 || q.cols == 0) return cudaSuccess;

@@ -233,9 +233,11 @@ BOTH_CONFIGS = [c for c in CONFIGS if not c[3]]
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 # (512, 1024), (256, 256): code pitches multiples of 32 bytes (BF16: sector stores);
 # (2048, 384): 16 but not 32 (direct stores); (272, 40): a last tile of 16 rows;
-# (16, 8): one block
+# (16, 8): one block.  Where the column pairs fill whole CTAs (512, 1024, 3584 BF16
+# columns...) one read of x gives both maxima: (512, 1024), (272, 512) and (400, 1024)
+# take that path, the last two with a partial last run of row blocks.
 @pytest.mark.parametrize("shape", [(512, 1024), (256, 256), (2048, 384), (272, 40), (16, 8),
-                                   (1024, 96)])
+                                   (1024, 96), (272, 512), (400, 1024)])
 @pytest.mark.parametrize("conf", BOTH_CONFIGS)
 def test_quantize_both_rht_matches_oracle(dtype, shape, conf):
     """Both directions in one encode pass, the transform on the columnwise side only
