@@ -328,6 +328,44 @@ __device__ __forceinline__ float sse16_signed(float err, const float* x, uint32_
   return err;
 }
 
+// The same transform of two blocks at once (two adjacent columns), every add,
+// subtract and product formed as a packed pair: each half of add.rn.f32x2 /
+// sub.rn.f32x2 / mul.rn.f32x2 is the IEEE operation of the scalar steps, so a and b
+// come out bit for bit as rht16_block would make them.
+__device__ __forceinline__ void rht16_block2(float (&a)[16], float (&b)[16], uint32_t mask) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t sb = ((mask >> j) & 1u) << 31;
+    a[j] = __uint_as_float(__float_as_uint(a[j]) ^ sb);
+    b[j] = __uint_as_float(__float_as_uint(b[j]) ^ sb);
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h *= 2) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      float s0, s1, d0, d1;
+      asm("{\n\t.reg .b64 u, w, s, d;\n\t"
+          "mov.b64 u, {%4, %5};\n\tmov.b64 w, {%6, %7};\n\t"
+          "add.rn.f32x2 s, u, w;\n\tsub.rn.f32x2 d, u, w;\n\t"
+          "mov.b64 {%0, %1}, s;\n\tmov.b64 {%2, %3}, d;\n\t}"
+          : "=f"(s0), "=f"(s1), "=f"(d0), "=f"(d1)
+          : "f"(a[i]), "f"(b[i]), "f"(a[i + h]), "f"(b[i + h]));
+      a[i] = s0, b[i] = s1, a[i + h] = d0, b[i + h] = d1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float p0, p1;
+    asm("{\n\t.reg .b64 u, q, d;\n\t"
+        "mov.b64 u, {%2, %3};\n\tmov.b64 q, {%4, %4};\n\t"
+        "mul.rn.f32x2 d, u, q;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(p0), "=f"(p1)
+        : "f"(a[j]), "f"(b[j]), "f"(0.25f));
+    a[j] = p0, b[j] = p1;
+  }
+}
+
 // Random Hadamard transform of one 16-value block, in place: v = (1/4) H16 diag(s) v
 // with H16 the Sylvester Hadamard matrix and s_j = -1 where bit j of mask is set.
 // FP32 steps in this order: the signs (exact), the four natural-order butterfly

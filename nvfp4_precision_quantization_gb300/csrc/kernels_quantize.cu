@@ -488,8 +488,10 @@ __device__ __forceinline__ void rowwise_store_scales(const EncodeArgs& a, int r,
 // ---------------------------------------------------------------- columnwise
 
 // Codes and scales of column pair (cl, cl + 1) over rows [rb0, rb0 + RG).
+// RHT_PAIR: the two columns' transforms as packed pairs (fewer instructions, more
+// registers: used where the register budget allows, the columnwise-only kernels).
 template <typename T, int RG, bool FOS, bool B2D, bool LOOP = false, bool RHT = false,
-          typename M>
+          bool RHT_PAIR = false, typename M>
 __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m,
                                                 const EncodeArgs& a, int cl, int rb0,
                                                 const int32_t (&coff)[8], float S_t, float A_t,
@@ -592,8 +594,12 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
     }
     if constexpr (RHT) {
       // the block of each column replaced by its transform; its max from the result
-      rht16_block(x0, a.rht_mask);
-      rht16_block(x1, a.rht_mask);
+      if constexpr (RHT_PAIR) {
+        rht16_block2(x0, x1, a.rht_mask);
+      } else {
+        rht16_block(x0, a.rht_mask);
+        rht16_block(x1, a.rht_mask);
+      }
       b0 = absmax16_f32(x0);
       b1 = absmax16_f32(x1);
     }
@@ -1249,7 +1255,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     } else if (COL) {
       uint32_t w0[RG / 8], w1[RG / 8];
       uint32_t sc0, sc1;
-      colwise_compute<T, RG, FOS, B2D, ROW && COL && !RHT, RHT>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1,
+      colwise_compute<T, RG, FOS, B2D, ROW && COL && !RHT, RHT, RHT && !ROW>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1,
                                                    sc0, sc1);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);

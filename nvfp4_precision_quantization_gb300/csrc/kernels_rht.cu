@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16(RhtKernelArgs a) {
       }
     }
 #pragma unroll
-    for (int k = 0; k < V; ++k) rht16_block(v[k], a.mask);
+    if constexpr (V == 2) rht16_block2(v[0], v[1], a.mask);
+    else rht16_block(v[0], a.mask);
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       float* yp = a.y + base + r * a.cols;
@@ -205,9 +206,10 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax(RhtAmaxKernelArgs a)
           }
         }
       }
+      if constexpr (V == 2) rht16_block2(v[0], v[1], a.mask);
+      else rht16_block(v[0], a.mask);
 #pragma unroll
       for (int k = 0; k < V; ++k) {
-        rht16_block(v[k], a.mask);
 #pragma unroll
         for (int r = 0; r < 16; ++r) cmax[k] = fmaxf(cmax[k], fabsf(v[k][r]));
       }
@@ -328,9 +330,10 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax_rows(RhtAmaxRowsArgs
       if ((lane & 1) == 0 && m[0] > 0.0f)
         atomicMax(reinterpret_cast<unsigned int*>(s_rmax + 16 * (rb - rb0) + my_row),
                   __float_as_uint(m[0]));
+      if constexpr (V == 2) rht16_block2(v[0], v[1], a.mask);
+      else rht16_block(v[0], a.mask);
 #pragma unroll
       for (int k = 0; k < V; ++k) {
-        rht16_block(v[k], a.mask);
 #pragma unroll
         for (int r = 0; r < 16; ++r) cmax[k] = fmaxf(cmax[k], fabsf(v[k][r]));
       }
