@@ -49,7 +49,11 @@ __device__ __forceinline__ void atomic_max_nonneg(float* p, float v) {
 
 // ---------------------------------------------------------------- prep
 
+// The next kernel (the amax pass, launched for programmatic dependent launch) may
+// start its prologue and its loads of x at once: it waits for this grid before it
+// touches the outputs cleared here.
 __global__ void k_prep(PrepArgs a) {
+  pdl_launch_dependents();
   if (noop_set(a.noop)) return;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
@@ -855,6 +859,7 @@ __global__ void __launch_bounds__(kThreads) k_group_reduce(GroupReduceArgs a) {
 
 __global__ void k_group_check(GroupCheckArgs a, int* status, bool expand_pass) {
   __shared__ int64_t s_ends[kMaxGroups];
+  pdl_launch_dependents();  // as k_prep: the next kernel waits before it reads our outputs
   if (noop_set(a.noop)) return;
   const bool ok = load_group_ends(a.group_ends, a.num_groups, a.M, s_ends);
   // padded layout: group_ends are the padded ends (M output rows), rag_ends the
