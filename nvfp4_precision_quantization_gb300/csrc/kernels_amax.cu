@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
   const int count = end - begin;
   const bool fwd = (blockIdx.x & 1) == 0;  // the encode kernel walks this chunk the other way
+  if (warp == kConsumerWarps && lane == 0) prefetch_tmap(&tmap);  // while the barriers are set up
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -462,7 +463,6 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
 
   if (warp == kConsumerWarps) {
     if (lane != 0) return;
-    prefetch_tmap(&tmap);
     const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
     TileCursor cur;
     cur.seek(a.grid, a.grid.walk(begin, end, 0, fwd));

@@ -846,6 +846,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
   const int count = end - begin;
   const bool fwd = (blockIdx.x & 1) != 0;  // the amax kernel walks this chunk the other way
+  if (TMA && warp == kConsumerWarps && lane == 0) prefetch_tmap(&tmap);  // while barriers are set up
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 2);  // producer: TMA arrival (with bytes) + staged-meta arrival
@@ -861,7 +862,6 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   if (warp == kConsumerWarps) {
     // ---------------- producer warp
     const uint64_t policy = policy_evict_first();
-    if (TMA && lane == 0) prefetch_tmap(&tmap);
     // tiles are issued in order k = 0, 1, ...: one cursor steps along with them
     TileCursor ci;
     ci.seek(a.grid, a.grid.walk(begin, end, 0, fwd));

@@ -303,6 +303,25 @@ def test_grouped_amax_matches_oracle():
     assert np.array_equal(ga.cpu().numpy(), g) and np.array_equal(ex.cpu().numpy(), e)
 
 
+@pytest.mark.parametrize("with_rows", [True, False])
+def test_grouped_amax_many_groups(with_rows):
+    """1000 groups (empty ones included), more than the reduction's CTAs: each CTA
+    takes several groups.  With the per-row output the maxima come from the tiled row
+    pass and the per-group reduction, without it from the grouped kernel."""
+    rng = np.random.default_rng(15)
+    counts = rng.integers(0, 24, 1000).tolist()
+    counts[3] = 0
+    x, ends = _groups(counts, 200, 1, seed=16)
+    ga = torch.full((len(ends),), -1.0, device=DEV)
+    ex = torch.full((x.shape[0],), -1.0, device=DEV) if with_rows else None
+    nv.nvfp4_grouped_amax(x, torch.from_numpy(ends).to(DEV), ga, ex)
+    xb, tag = host_bits(x)
+    g, e = oracle.grouped_amax(xb, tag, ends)
+    assert np.array_equal(ga.cpu().numpy(), g)
+    if with_rows:
+        assert np.array_equal(ex.cpu().numpy(), e)
+
+
 def test_grouped_invalid_ends_write_nothing_and_set_status():
     x, _ = _groups([64, 64], 256, 1, seed=13)
     nv.nvfp4_device_status(reset=True)
