@@ -292,6 +292,17 @@ def test_quantize_both_rht_given_amax_and_noop():
         assert torch.equal(a.amax, b.amax)
     assert not torch.equal(ref_r.amax, ref_c.amax)  # two different tensors
     noop = torch.ones(1, dtype=torch.float32, device=DEV)
-    row, col = _both_gpu(x, 0x2468, conf, noop=noop, fill=0xA5)
-    for o in (row, col):
-        assert bool((o.codes == 0xA5).all()) and bool((o.scales == 0xA5).all())
+    # (256, 1024): the one-read amax of both maxima; (512, 256): the two passes
+    for xx in (x, _input(256, 1024, torch.bfloat16, seed=44)):
+        for cf in (conf, (nv.NVFP4_ROW_SCALED, 448.0, False, False)):
+            row, col = _both_gpu(xx, 0x2468, cf, noop=noop, fill=0xA5)
+            for o in (row, col):
+                assert bool((o.codes == 0xA5).all()) and bool((o.scales == 0xA5).all())
+    # only one maximum given: the other is computed on its own
+    x2 = _input(256, 1024, torch.bfloat16, seed=45)
+    ref_r, ref_c = _both_gpu(x2, 0x1357, conf)
+    for given in ((ref_r.amax.clone(), None), (None, ref_c.amax.clone())):
+        row, col = _both_gpu(x2, 0x1357, conf, amax_in=given)
+        for a, b in ((row, ref_r), (col, ref_c)):
+            assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+            assert torch.equal(a.amax, b.amax)
