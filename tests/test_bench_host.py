@@ -31,7 +31,7 @@ def test_quant_bytes_by_dtype_and_mode():
     assert bench.quant_bytes(32, 48, 2, False) == bench.bytes_io(32, 48) - 4 * 80 + 8
 
 
-@pytest.mark.parametrize("w", ["rht", "dequant", "moe-col", "weights16x16", "moe", "outliers",
+@pytest.mark.parametrize("w", ["rht", "rht-both", "dequant", "moe-col", "weights16x16", "moe", "outliers",
                                "edge", "tiny"])
 @pytest.mark.parametrize("threads", [1, 2])
 def test_supplementary_oracle_samples_repeat_to_the_minimum_time(w, threads):
