@@ -658,7 +658,7 @@ def run_supplementary(args):
                                    "encode)"), bio, 5
         dtype, elems = "bf16", M * K
     elif w == "rht":
-        x = workloads.linear(dev)[1]
+        x = workloads.linear(dev, rows=args.rows)[1]
         M, K = x.shape
         cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
         col = nv.alloc_out(K, M, K, dev)
@@ -672,7 +672,7 @@ def run_supplementary(args):
         kern, kbytes, launches = "whole step (prep, transformed column amax, encode)", bmin, 3
         dtype, elems = "bf16", M * K
     elif w == "rht-both":
-        x = workloads.linear(dev)[1]
+        x = workloads.linear(dev, rows=args.rows)[1]
         M, K = x.shape
         cfg = nv.Config(nv.NVFP4_ROW_SCALED, 448.0, 0, 0)
         row = nv.alloc_out(M, K, M, dev)
