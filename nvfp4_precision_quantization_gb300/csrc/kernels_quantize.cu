@@ -821,10 +821,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   // Columnwise scale bytes of the first three tile rows of a column's 32-byte
   // scale sector, per tile of the super-strip row and column, held until the CTA
   // reaches the fourth (4 tiles apart in its walk): [tile][column][visit][row half].
-  __shared__ uint32_t csb[SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D && !RHT
-                              ? TileGrid::kGroup : 1]
-                         [SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D && !RHT ? 128 : 1]
-                         [3][2];
+  __shared__ uint32_t csb[SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? TileGrid::kGroup : 1]
+                         [SECT && ROW && COL && sizeof(T) == 2 && !FOS && !B2D ? 128 : 1][3][2];
   __shared__ volatile int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1033,8 +1031,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   // in the order i ^ 4, which puts the two halves on disjoint shared-memory
   // banks; their code words are put back in row order afterwards.  Otherwise
   // consecutive threads take consecutive column pairs.
-  // (With the transform, each thread needs its 16-row blocks in natural row order.)
-  constexpr bool PAIRED = SECT && BOTH && sizeof(T) == 2 && !FOS && !B2D && !RHT;
+  // With the transform each thread needs its 16-row blocks in natural row order: the
+  // odd lanes then read them in that order too (PERM off) and take the 2-way bank
+  // conflict between the two halves.
+  constexpr bool PAIRED = SECT && BOTH && sizeof(T) == 2 && !FOS && !B2D;
+  constexpr bool PERM = PAIRED && !RHT;
   // CPAIR (sector stores, columnwise only, BF16, 1x16): a thread holds 32 rows of a
   // column pair, and neighbouring lanes hold the two 32-row halves of the same 64-row
   // run, so that after one exchange each lane stores one column's 32 code bytes (a
@@ -1054,7 +1055,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     const int box = cl / G::BOXC, byte = (cl % G::BOXC) * (int)sizeof(T);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int kk = k ^ (PAIRED ? 4 * hh : 0);  // the row actually read, mod 8
+      const int kk = k ^ (PERM ? 4 * hh : 0);  // the row actually read, mod 8
       coff[k] = box * kBoxBytes + ((((byte >> 4) ^ kk)) << 4) + (byte & 15) + (kk - k) * 128;
     }
   }
@@ -1259,7 +1260,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
                                                    sc0, sc1);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if constexpr (PAIRED) {
+      if constexpr (PERM) {
 #pragma unroll
         for (int q = 0; q < RG / 8; ++q) {
           w0[q] = __byte_perm(w0[q], 0, word_sel);
