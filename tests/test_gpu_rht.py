@@ -298,6 +298,11 @@ def test_quantize_both_rht_given_amax_and_noop():
             row, col = _both_gpu(xx, 0x2468, cf, noop=noop, fill=0xA5)
             for o in (row, col):
                 assert bool((o.codes == 0xA5).all()) and bool((o.scales == 0xA5).all())
+    # empty shapes: no rows (each column's amax is 0), no columns
+    for rows, cols in ((0, 64), (32, 0)):
+        e = torch.empty(rows, cols, dtype=torch.bfloat16, device=DEV)
+        r0, c0 = _both_gpu(e, 0x1, (nv.NVFP4_ROW_SCALED, 448.0, False, False))
+        assert bool((r0.amax == 0).all()) and bool((c0.amax == 0).all())
     # only one maximum given: the other is computed on its own
     x2 = _input(256, 1024, torch.bfloat16, seed=45)
     ref_r, ref_c = _both_gpu(x2, 0x1357, conf)
