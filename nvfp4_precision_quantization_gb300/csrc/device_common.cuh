@@ -12,7 +12,9 @@
 // __fsub_rn), packed pairs whose products cannot be contracted (mul2_fma), and two
 // divisions replaced by FMA sequences proven to return the correctly rounded
 // quotient (div6_short, div_by_scale).  The conversions use the sm_100-family cvt
-// instructions (RNE, satfinite).
+// instructions (RNE, satfinite).  The four-over-six choice is first tried on an
+// estimate of the two errors with a proven bound (fos_bounded_pick); the exact
+// sums decide whenever the bound does not.
 #pragma once
 
 #include <cuda.h>
@@ -283,13 +285,13 @@ __device__ __forceinline__ void e2m1_magnitudes4(uint32_t m, float (&v)[4]) {
 // err = fl(err + fl(d_i * d_i)) with d_i = fl(x_i - fl(v_i * D)), v_i the value of
 // code i (c0: values 0..7, c1: 8..15) and D the candidate's dequantize factor.
 // Two ways of decoding, so that the two candidates load different pipes:
-//   sse16_magnitudes: from |x| (ax) and the codes' magnitudes (table lookup).  The
+//   sse16_magnitudes: from |x| and the codes' magnitudes (table lookup).  The
 //     sign of a nonzero code is the sign of its x, so |x_i| - |v_i D| is d_i up to
 //     its sign, and d_i * d_i is the same.
 //   sse16_signed: from x and the signed values (hardware E2M1 -> FP16 conversion).
 // The dequantized values, the differences and the squares are formed two at a time
 // (packed); the additions stay one at a time, in order.
-__device__ __forceinline__ float sse16_magnitudes(float err, const float* ax, uint32_t c0,
+__device__ __forceinline__ float sse16_magnitudes(float err, const float* x, uint32_t c0,
                                                   uint32_t c1, float D, float negz) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -298,8 +300,8 @@ __device__ __forceinline__ float sse16_magnitudes(float err, const float* ax, ui
     e2m1_magnitudes4(((q & 1) ? (w >> 16) : w) & 0x7777u, v);
     mul2_fma(v[0], v[1], D, D, negz, g[0], g[1]);
     mul2_fma(v[2], v[3], D, D, negz, g[2], g[3]);
-    sub2_rn(ax[4 * q], ax[4 * q + 1], g[0], g[1], d[0], d[1]);
-    sub2_rn(ax[4 * q + 2], ax[4 * q + 3], g[2], g[3], d[2], d[3]);
+    sub2_rn(fabsf(x[4 * q]), fabsf(x[4 * q + 1]), g[0], g[1], d[0], d[1]);
+    sub2_rn(fabsf(x[4 * q + 2]), fabsf(x[4 * q + 3]), g[2], g[3], d[2], d[3]);
     mul2_fma(d[0], d[1], d[0], d[1], negz, p[0], p[1]);
     mul2_fma(d[2], d[3], d[2], d[3], negz, p[2], p[3]);
 #pragma unroll
@@ -326,6 +328,85 @@ __device__ __forceinline__ float sse16_signed(float err, const float* x, uint32_
     for (int k = 0; k < 4; ++k) err = __fadd_rn(err, p[k]);
   }
   return err;
+}
+
+// (sa, sb) = (fl(r0 r0 + sa), fl(r1 r1 + sb)): one packed FMA.
+__device__ __forceinline__ void sq2_acc(float r0, float r1, float& sa, float& sb) {
+  asm("{\n\t.reg .b64 r, s;\n\t"
+      "mov.b64 r, {%2, %3};\n\tmov.b64 s, {%0, %1};\n\t"
+      "fma.rn.f32x2 s, r, r, s;\n\tmov.b64 {%0, %1}, s;\n\t}"
+      : "+f"(sa), "+f"(sb)
+      : "f"(r0), "f"(r1));
+}
+
+// Codes of x[0..7] scaled by e (as codes8), and the squared residuals of the scaled
+// values added into (sa, sb), even i into sa and odd i into sb: r_i = fl(v_i - y_i)
+// with y_i = fl(x_i e) and v_i the value of code i (its FP16 form from the hardware
+// conversion, subtracted from y_i in one mixed-precision instruction), then
+// fl(r_i r_i + s) as packed FMAs.  The sum only estimates the candidate's error;
+// fos_bounded_pick bounds how far the estimate can be from the exact sum.
+__device__ __forceinline__ uint32_t codes8_residual(const float* x, float e, float& sa,
+                                                    float& sb) {
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) mul2_rn(x[2 * i], x[2 * i + 1], e, y[2 * i], y[2 * i + 1]);
+  uint32_t w, h[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %8, %7;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %10, %9;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %12, %11;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %4, b3;\n\t}"
+      : "=r"(w), "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]),
+        "f"(y[7]));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float r0, r1;  // v - y: FP16 value minus FP32 value, one rounding each
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "sub.rn.f32.f16 %0, a, %3;\n\tsub.rn.f32.f16 %1, b, %4;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "r"(h[k]), "f"(y[2 * k]), "f"(y[2 * k + 1]));
+    sq2_acc(r0, r1, sa, sb);
+  }
+  return w;
+}
+
+// Four-over-six without the exact error sums, where a bound settles the choice.
+// Per candidate T, with D its dequantize factor and A = sum (y_i - v_i)^2 from
+// codes8_residual, E' = fl(fl(D D) A) estimates the exact error err (the
+// definition's FP32 sum of fl(x_i - fl(v_i D))^2 in element order).  Both are
+// within a few rounding errors of the real sum of t_i^2, t_i = x_i - v_i D:
+//   * e D = 1 + phi with |phi| <= 5u (u = 2^-24: the roundings of S = F/a, e = S/sd,
+//     fl(1/F), fl(sd a) and D), so D y_i = x_i (1 + theta_i), |theta_i| <= 6u;
+//   * fl(b e) <= 6.5 bounds every |y_i| by 6.5 and every |y_i - v_i| by 1 (half the
+//     E2M1 spacing, or the distance to 6 past it), so |t_i| <= D (1 + 40u) and
+//     b <= 6.5001 D;
+//   * forward error analysis of the 16 terms then gives |err - sum t_i^2| <= 528.1 u D^2
+//     (the products, differences and squares, and the in-order sum of 16 non-negative
+//     terms) and |E' - sum t_i^2| <= 1568.3 u D^2 (the x_i theta_i terms, the rounding
+//     of each r_i, the two 8-term FMA chains and their sum, the final product), plus
+//     underflow terms below 100 * 2^-150 (D^2 + 1) that D in [2^-62, 2^61] makes
+//     negligible against 2^-12 D^2.
+// So |err - E'| <= 2096.4 u D^2 < 2^-12 D^2 / 1.9, and err4 < err6 holds whenever
+// E'4 - E'6 < -2^-12 (D4^2 + D6^2) (after the roundings of that comparison), and fails
+// whenever the difference exceeds +2^-12 (D4^2 + D6^2).  Returns 1 (T = 4), 0 (T = 6)
+// or -1: the estimates are too close, or the block is outside the ranges above (inf,
+// NaN and saturated blocks included), and the exact sums decide.
+__device__ __forceinline__ int fos_bounded_pick(float b, float e6, float e4, float D6, float D4,
+                                                float A6, float A4) {
+  const float y6 = __fmul_rn(b, e6), y4 = __fmul_rn(b, e4);
+  const bool in_range = y6 <= 6.5f && y4 <= 6.5f && D6 >= 0x1p-62f && D6 <= 0x1p61f &&
+                        D4 >= 0x1p-62f && D4 <= 0x1p61f;
+  if (!in_range) return -1;
+  const float q6 = __fmul_rn(D6, D6), q4 = __fmul_rn(D4, D4);
+  const float diff = __fsub_rn(__fmul_rn(q4, A4), __fmul_rn(q6, A6));
+  const float tol = __fmul_rn(0x1p-12f, __fadd_rn(q4, q6));
+  return diff < -tol ? 1 : (diff > tol ? 0 : -1);
 }
 
 // The same transform of two blocks at once (two adjacent columns), every add,
@@ -389,31 +470,56 @@ __device__ __forceinline__ void rht16_block(float (&v)[16], uint32_t mask) {
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
 }
 
+// The exact four-over-six choice of one block: 1 when the T = 4 error (codes d0, d1,
+// factor D4) is below the T = 6 error (codes c0, c1, factor D6).  Out of line: it
+// runs only for the blocks that fos_bounded_pick leaves open, and its code is then
+// not repeated in every unrolled block of the encode loops.
+static __device__ __noinline__ int fos_exact_pick(float4 xa, float4 xb, float4 xc,
+                                                  float4 xd, uint32_t c0, uint32_t c1,
+                                                  uint32_t d0, uint32_t d1, float D6, float D4,
+                                                  float negz) {
+  const float x[16] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w,
+                       xc.x, xc.y, xc.z, xc.w, xd.x, xd.y, xd.z, xd.w};
+  const float err4 = sse16_signed(0.0f, x, d0, d1, D4, negz);
+  const float err6 = sse16_magnitudes(0.0f, x, c0, c1, D6, negz);
+  return err4 < err6;
+}
+
 // Quantize 16 FP32 values of one block whose max |x| is b: writes the two code
 // words (value k in nibble k) and returns the scale byte.  FOS: four-over-six
 // (needs the line amax a and F_inv for the error of each candidate, and negz =
-// -0.0 at run time, see mul2_fma).
+// -0.0 at run time, see mul2_fma).  The choice is that of the exact in-order error
+// sums: the bounded estimate settles it where it provably agrees with them, the
+// exact sums (out of line) elsewhere.
 template <bool FOS, bool SHORT = false>
 __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S, float a,
                                                float F_inv, float negz, uint32_t& c0,
                                                uint32_t& c1) {
   BlockEnc e6 = block_encode<6, SHORT>(b, S);
-  c0 = codes8(x, e6.e);
-  c1 = codes8(x + 8, e6.e);
   if constexpr (!FOS) {
+    c0 = codes8(x, e6.e);
+    c1 = codes8(x + 8, e6.e);
     return e6.s8;
   } else {
     BlockEnc e4 = block_encode<4>(b, S);
-    const uint32_t d0 = codes8(x, e4.e);
-    const uint32_t d1 = codes8(x + 8, e4.e);
+    float s6a = 0.0f, s6b = 0.0f, s4a = 0.0f, s4b = 0.0f;
+    c0 = codes8_residual(x, e6.e, s6a, s6b);
+    c1 = codes8_residual(x + 8, e6.e, s6a, s6b);
+    const uint32_t d0 = codes8_residual(x, e4.e, s4a, s4b);
+    const uint32_t d1 = codes8_residual(x + 8, e4.e, s4a, s4b);
     const float D6 = dequant_factor(e6.sd, a, F_inv);
     const float D4 = dequant_factor(e4.sd, a, F_inv);
-    float ax[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ax[i] = fabsf(x[i]);
-    const float err6 = sse16_magnitudes(0.0f, ax, c0, c1, D6, negz);
-    const float err4 = sse16_signed(0.0f, x, d0, d1, D4, negz);
-    if (err4 < err6) {
+    // one scale byte: the same codes and errors, and a tie keeps T = 6
+    int pick = e4.s8 == e6.s8 ? 0
+                              : fos_bounded_pick(b, e6.e, e4.e, D6, D4, __fadd_rn(s6a, s6b),
+                                                 __fadd_rn(s4a, s4b));
+    if (pick < 0)  // the exact sums
+      pick = fos_exact_pick(make_float4(x[0], x[1], x[2], x[3]),
+                            make_float4(x[4], x[5], x[6], x[7]),
+                            make_float4(x[8], x[9], x[10], x[11]),
+                            make_float4(x[12], x[13], x[14], x[15]), c0, c1, d0, d1, D6, D4,
+                            negz);
+    if (pick) {
       c0 = d0;
       c1 = d1;
       return e4.s8;

@@ -706,10 +706,7 @@ __device__ __forceinline__ void subtile_scales(const uint8_t* stage, M& m, float
       uint32_t c0, c1, d0, d1;
       codes16(x, e6.e, c0, c1);
       codes16(x, e4.e, d0, d1);
-      float ax[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) ax[k] = fabsf(x[k]);
-      err6 = sse16_magnitudes(err6, ax, c0, c1, D6, negz);
+      err6 = sse16_magnitudes(err6, x, c0, c1, D6, negz);
       err4 = sse16_signed(err4, x, d0, d1, D4, negz);
     }
     if (err4 < err6) e6 = e4;
