@@ -63,7 +63,7 @@ def encode_bytes(rows, cols):
 # the X and dY launches, from one ncu capture of a full step (dram__bytes_read.sum +
 # dram__bytes_write.sum, L2 left as the step leaves it).  To be taken again whenever
 # the encode kernel changes.
-ENCODE_TRAFFIC_BYTES = (324.6e6 + 1353.6e6) / 2
+ENCODE_TRAFFIC_BYTES = (361.4e6 + 1383.6e6) / 2
 
 
 def measured_peaks():

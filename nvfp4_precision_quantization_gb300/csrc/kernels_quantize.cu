@@ -856,7 +856,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp
-    const uint64_t policy = policy_evict_first();
+    // x's tiles at the normal L2 priority: the evict-first output lines then leave L2
+    // (written back) first, during this pass, and fewer dirty lines are left to the
+    // next kernel
+    const uint64_t policy = policy_evict_normal();
     // tiles are issued in order k = 0, 1, ...: one cursor steps along with them
     TileCursor ci;
     ci.seek(a.grid, a.grid.walk(begin, end, 0, fwd));
