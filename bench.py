@@ -6,9 +6,9 @@ pass followed by the encode pass that writes rowwise and columnwise E2M1 codes
 and E4M3 scales (row-scaled: rows use the row amax, columns the column amax).
 
 The step is issued as nvfp4_amax + nvfp4_quantize_both(amax_in = that amax) per
-operand -- the same three kernels nvfp4_quantize_both launches on its own --
-so that CUDA events on the launching stream can time the encode kernel alone
-for the roofline figure.
+operand -- the same kernels nvfp4_quantize_both launches on its own (prep, amax,
+encode; with four-over-six one encode pass per direction) -- so that CUDA events
+on the launching stream can time the encode pass alone for the roofline figure.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -377,7 +377,9 @@ def run_ours(args):
                          "algorithmic_bytes": enc_bytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 6 * K,
+            # prep + amax + encode per operand; four-over-six encodes each direction
+            # in its own pass
+            "gpu_launches": (8 if fos else 6) * K,
             "clocks": clocks,
         }
         print(json.dumps(line))

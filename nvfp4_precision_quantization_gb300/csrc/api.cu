@@ -265,18 +265,7 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
   } else if (am.row_amax || am.col_amax || am.tensor_amax) {
     if ((e = launch_amax(am, dev, stream)) != cudaSuccess) return cuda_fail(e, "amax launch");
   }
-  if (q.block_2d && row && col && q.row_amax != q.col_amax) {
-    // 16x16 tiles share one scale per tile; with two different per-tensor amax
-    // sources the directions are encoded by two launches
-    QuantArgs qr = q, qc = q;
-    qr.col_codes = nullptr;
-    qc.row_codes = nullptr;
-    qc.copy_dst = nullptr;
-    if ((e = launch_quantize(qr, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize");
-    if ((e = launch_quantize(qc, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize");
-  } else if ((e = launch_quantize(q, dev, stream)) != cudaSuccess) {
-    return cuda_fail(e, "quantize launch");
-  }
+  if ((e = launch_quantize(q, dev, stream)) != cudaSuccess) return cuda_fail(e, "quantize launch");
   return NVFP4_OK;
 }
 

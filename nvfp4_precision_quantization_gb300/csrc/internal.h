@@ -136,6 +136,9 @@ struct QuantArgs {
   // replaced by its random Hadamard transform with this sign mask before encoding
   bool rht;
   uint32_t rht_mask;
+  // walk each CTA's tiles the other way (a second pass over x then starts on the tiles
+  // that the first one read last, still in L2)
+  bool reverse_walk;
 };
 cudaError_t launch_quantize(const QuantArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 

@@ -31,9 +31,9 @@
 //   direct  any pitch: the widest stores the pitch and base allow on interior
 //           tiles (both directions, no four-over-six: rowwise rows staged per warp
 //           and written back row by row), bytes on edge tiles.
-// Four-over-six with both directions encodes one column block and one row box at a
-// time (instruction cache, registers).  RHT: the columnwise warps transform each
-// 16-row block in registers before encoding it.
+// Four-over-six with 1x16 blocks and both directions is launched as two
+// single-direction passes (see launch_quantize).  RHT: the columnwise warps
+// transform each 16-row block in registers before encoding it.
 #include <algorithm>
 #include <cstring>
 
@@ -83,6 +83,7 @@ struct EncodeArgs {
   int row_scale_groups;  // rowwise scales of a super-strip row go out as one 32-byte sector
   int col_scale_sectors;  // columnwise scales of four tile rows go out as one 32-byte sector
   float neg_zero;         // -0.0, the addend of the four-over-six products (see mul2_fma)
+  int reverse_walk;       // walk each chunk the other way (a second pass over x)
 };
 
 // Per-stage values staged by the producer: the tile's per-row and per-column
@@ -183,7 +184,7 @@ __device__ __forceinline__ uint32_t encode_block(const float* x, float b, float 
 // Rows / columns outside x were zero-filled by the load, so they encode to 0;
 // the caller decides what is stored.  rot = 4 (BF16) makes step j read block
 // j ^ 2 of the box row (its results land in the slots of block j).
-template <typename T, int NBOX, bool FOS, bool B2D, bool LOOP = false, typename M>
+template <typename T, int NBOX, bool FOS, bool B2D, typename M>
 __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m,
                                                 const EncodeArgs& a, int r, int b0, float S_t,
                                                 float A_t,
@@ -194,60 +195,6 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m
   const float S = a.row_scaled ? m.rowS[r] : S_t;
   const float A = a.row_scaled ? m.rowA(r) : A_t;
   const int sw = (r & 7) ^ rot;
-  if constexpr (FOS && !B2D && LOOP) {
-    // Four-over-six in the kernels that encode both directions: the block routine
-    // is large, so the blocks run in a loop -- one copy of its code per call site
-    // instead of one per block keeps the kernel in the instruction cache (measured:
-    // +37 % on the two-direction path; the rowwise-only kernel, small enough
-    // already, is faster unrolled).  Each block's code words rotate into place and its
-    // scale byte shifts in from the top, so nothing is indexed at run time.
-    constexpr int NT = NBOX * NB;
-    uint32_t flat[2 * NT];
-    uint64_t sc_all = 0;
-#pragma unroll 1
-    for (int t = 0; t < NT; ++t) {
-      const int bi = t / NB, j = t % NB;
-      const uint8_t* rowp = stage + (b0 + bi) * kBoxBytes + r * 128;
-      float x[16];
-      float b;
-      if constexpr (sizeof(T) == 2) {
-        const uint4 v0 = lds128(rowp + (((2 * j) ^ sw) << 4));
-        const uint4 v1 = lds128(rowp + (((2 * j + 1) ^ sw) << 4));
-        const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[2 * i] = bf16_lo(u[i]);
-          x[2 * i + 1] = bf16_hi(u[i]);
-        }
-        b = absmax8_bf16(v0, v1);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v = lds128(rowp + (((4 * j + k) ^ sw) << 4));
-          x[4 * k] = __uint_as_float(v.x);
-          x[4 * k + 1] = __uint_as_float(v.y);
-          x[4 * k + 2] = __uint_as_float(v.z);
-          x[4 * k + 3] = __uint_as_float(v.w);
-        }
-        b = absmax16_f32(x);
-      }
-      uint32_t c0, c1;
-      const uint32_t s8 =
-          quantize16<true, sizeof(T) == 2>(x, b, S, A, a.F_inv, a.neg_zero, c0, c1);
-#pragma unroll
-      for (int k = 0; k < 2 * NT - 2; ++k) flat[k] = flat[k + 2];
-      flat[2 * NT - 2] = c0;
-      flat[2 * NT - 1] = c1;
-      sc_all = (sc_all >> 8) | ((uint64_t)s8 << (8 * (NT - 1)));
-    }
-#pragma unroll
-    for (int bi = 0; bi < NBOX; ++bi) {
-#pragma unroll
-      for (int k = 0; k < 2 * NB; ++k) w[bi][k] = flat[2 * NB * bi + k];
-      sc[bi] = (uint32_t)(sc_all >> (8 * NB * bi)) & (uint32_t)((1ull << (8 * NB)) - 1);
-    }
-    return;
-  }
 #pragma unroll
   for (int bi = 0; bi < NBOX; ++bi) {
     const int box = b0 + bi;
@@ -490,8 +437,8 @@ __device__ __forceinline__ void rowwise_store_scales(const EncodeArgs& a, int r,
 // Codes and scales of column pair (cl, cl + 1) over rows [rb0, rb0 + RG).
 // RHT_PAIR: the two columns' transforms as packed pairs (fewer instructions, more
 // registers: used where the register budget allows, the columnwise-only kernels).
-template <typename T, int RG, bool FOS, bool B2D, bool LOOP = false, bool RHT = false,
-          bool RHT_PAIR = false, typename M>
+template <typename T, int RG, bool FOS, bool B2D, bool RHT = false, bool RHT_PAIR = false,
+          typename M>
 __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m,
                                                 const EncodeArgs& a, int cl, int rb0,
                                                 const int32_t (&coff)[8], float S_t, float A_t,
@@ -504,56 +451,6 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
   const float A0 = a.row_scaled ? m.colA(cl) : A_t;
   const float A1 = a.row_scaled ? m.colA(cl + 1) : A_t;
   sc0 = sc1 = 0;
-  if constexpr (FOS && !B2D && LOOP && sizeof(T) == 2 && NB == 4) {
-    // Four-over-six with both directions: one column block per iteration (t = 2 jb +
-    // column), one copy of the block routine, and only one column's 16 values
-    // unpacked at a time (the packed pairs are loaded again for the second column),
-    // which keeps the loop inside the register budget of two CTAs per SM.  Each
-    // iteration's two code words and scale byte shift into place, so nothing is
-    // indexed at run time.
-    uint32_t flat[4 * NB];
-    uint64_t sc_all = 0;
-#pragma unroll 1
-    for (int t = 0; t < 2 * NB; ++t) {
-      const int jb = t >> 1, c = t & 1;
-      const uint8_t* base = stage + (rb0 + 16 * jb) * 128;
-      uint32_t v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        v[i] = *reinterpret_cast<const uint32_t*>(base + i * 128 + coff[i & 7]);
-      uint32_t t8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) t8[i] = absmax_bf16x2(v[2 * i], v[2 * i + 1]);
-      const uint32_t mm =
-          absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(t8[0], t8[1]), absmax_bf16x2(t8[2], t8[3])),
-                        absmax_bf16x2(absmax_bf16x2(t8[4], t8[5]), absmax_bf16x2(t8[6], t8[7])));
-      // this column's half of each pair, moved to the top 16 bits (the FP32 value)
-      const uint32_t sel = c ? 0x3244u : 0x1044u;
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(byte_perm(v[i], 0u, sel));
-      const float b = __uint_as_float(byte_perm(mm & 0x7fff7fffu, 0u, sel));
-      uint32_t q0, q1;
-      const uint32_t s8 = quantize16<true, true>(x, b, c ? S1 : S0, c ? A1 : A0, a.F_inv,
-                                                 a.neg_zero, q0, q1);
-#pragma unroll
-      for (int k = 0; k < 4 * NB - 2; ++k) flat[k] = flat[k + 2];
-      flat[4 * NB - 2] = q0;
-      flat[4 * NB - 1] = q1;
-      sc_all = (sc_all >> 8) | ((uint64_t)s8 << (8 * (2 * NB - 1)));
-    }
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      w0[2 * j] = flat[4 * j];
-      w0[2 * j + 1] = flat[4 * j + 1];
-      w1[2 * j] = flat[4 * j + 2];
-      w1[2 * j + 1] = flat[4 * j + 3];
-    }
-    const uint32_t lo = (uint32_t)sc_all, hi = (uint32_t)(sc_all >> 32);
-    sc0 = byte_perm(lo, hi, 0x6420u);
-    sc1 = byte_perm(lo, hi, 0x7531u);
-    return;
-  }
 #pragma unroll
   for (int jb = 0; jb < NB; ++jb) {
     const uint8_t* base = stage + (rb0 + 16 * jb) * 128;
@@ -840,7 +737,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
   int begin, end;
   a.grid.chunk(blockIdx.x, gridDim.x, begin, end);
   const int count = end - begin;
-  const bool fwd = (blockIdx.x & 1) != 0;  // the amax kernel walks this chunk the other way
+  // the amax kernel walks this chunk the other way (a second encode pass: the same way)
+  const bool fwd = ((blockIdx.x & 1) != 0) != (a.reverse_walk != 0);
   if (TMA && warp == kConsumerWarps && lane == 0) prefetch_tmap(&tmap);  // while barriers are set up
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -1101,8 +999,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         // (each row on its own keeps 8 code words live instead of 16)
         auto row_codes = [&](int rr, uint32_t (&sx)[1]) {
           uint32_t wx[1][8];
-          rowwise_compute<T, 1, FOS, B2D, ROW && COL>(stage, m, a, rr, hb, S_r, A_r, wx, sx,
-                                                      4 * hb);
+          rowwise_compute<T, 1, FOS, B2D>(stage, m, a, rr, hb, S_r, A_r, wx, sx, 4 * hb);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t lo = wx[0][q], hi = wx[0][q + 4];
@@ -1155,25 +1052,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     } else if (is_row) {
       uint32_t w[NBOX][G::BOXC / 8];
       uint32_t sc[NBOX];
-      // Four-over-six with both directions and sector stores: one box at a time, its
-      // 32 code bytes stored as soon as they are computed (8 code words live instead
-      // of 16, which keeps the loop inside the register budget)
-      constexpr bool BOXWISE = FOS && !B2D && BOTH && SECT && sizeof(T) == 2;
-      if constexpr (BOXWISE) {
-        uint8_t* cp = a.row_codes + ((int64_t)tm * kTileRows + r) * a.row_cpitch +
-                      (int64_t)tn * (G::TILEC / 2);
-#pragma unroll 1
-        for (int bi = 0; bi < NBOX; ++bi) {
-          uint32_t wb[1][G::BOXC / 8], sb[1];
-          rowwise_compute<T, 1, FOS, B2D, true>(stage, m, a, r, b0 + bi, S_r, A_r, wb, sb);
-          if (bi == 0) sc[0] = sb[0];
-          else sc[NBOX - 1] = sb[0];
-          if (fast) stg_v8_cs(cp + (b0 + bi) * 32, wb[0]);
-          else rowwise_store<T, 1>(a, r, b0 + bi, tm, tn, wb, sb, false);
-        }
-      } else {
-        rowwise_compute<T, NBOX, FOS, B2D, ROW && COL>(stage, m, a, r, b0, S_r, A_r, w, sc);
-      }
+      rowwise_compute<T, NBOX, FOS, B2D>(stage, m, a, r, b0, S_r, A_r, w, sc);
       if (ROW && !COL && a.pad_ends != nullptr && r >= m.nrows) {
         // a padding row: zero codes and scales (what a zero row encodes to)
 #pragma unroll
@@ -1234,14 +1113,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         store_row_scales();
       } else if constexpr (SECT) {
         if (fast) {
-          if constexpr (!BOXWISE) {
-            uint8_t* cp = a.row_codes + ((int64_t)tm * kTileRows + r) * a.row_cpitch +
-                          (int64_t)tn * (G::TILEC / 2);
+          uint8_t* cp = a.row_codes + ((int64_t)tm * kTileRows + r) * a.row_cpitch +
+                        (int64_t)tn * (G::TILEC / 2);
 #pragma unroll
-            for (int bi = 0; bi < NBOX; ++bi) stg_v8_cs(cp + bi * 32 + b0 * 32, w[bi]);
-          }
+          for (int bi = 0; bi < NBOX; ++bi) stg_v8_cs(cp + bi * 32 + b0 * 32, w[bi]);
           store_row_scales();
-        } else if constexpr (!BOXWISE) {
+        } else {
           rowwise_store<T, NBOX>(a, r, b0, tm, tn, w, sc, false);
         }
       } else if (STAGED_ROWS && interior && a.rc_g >= 4) {
@@ -1256,8 +1133,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     } else if (COL) {
       uint32_t w0[RG / 8], w1[RG / 8];
       uint32_t sc0, sc1;
-      colwise_compute<T, RG, FOS, B2D, ROW && COL && !RHT, RHT, RHT && !ROW>(stage, m, a, cl, rb0, coff, S_c, A_c, w0, w1,
-                                                   sc0, sc1);
+      colwise_compute<T, RG, FOS, B2D, RHT, RHT && !ROW>(stage, m, a, cl, rb0, coff, S_c, A_c,
+                                                         w0, w1, sc0, sc1);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if constexpr (PERM) {
@@ -1388,7 +1265,13 @@ template <typename T, bool ROW, bool COL>
 EncodeFn pick_mode(bool fos, bool b2d, bool tma, int outm) {
   if (b2d)
     return fos ? pick_io<T, ROW, COL, true, true>(tma, outm) : pick_io<T, ROW, COL, false, true>(tma, outm);
-  return fos ? pick_io<T, ROW, COL, true, false>(tma, outm) : pick_io<T, ROW, COL, false, false>(tma, outm);
+  if constexpr (ROW && COL) {
+    // four-over-six with 1x16 blocks and both directions runs as two passes
+    return fos ? nullptr : pick_io<T, ROW, COL, false, false>(tma, outm);
+  } else {
+    return fos ? pick_io<T, ROW, COL, true, false>(tma, outm)
+               : pick_io<T, ROW, COL, false, false>(tma, outm);
+  }
 }
 
 // Columnwise only, 1x16 blocks, each block transformed first.
@@ -1409,13 +1292,11 @@ EncodeFn pick_rht(bool fos, bool tma, int outm) {
 // Both directions, 1x16 blocks, the columnwise blocks transformed first (TMA loads).
 template <typename T>
 EncodeFn pick_rht_both(bool fos, int outm) {
+  if (fos) return nullptr;  // four-over-six: two single-direction passes
   if constexpr (sizeof(T) == 2) {
-    if (outm == kOutSector)
-      return fos ? k_encode<T, true, true, true, false, true, kOutSector, true>
-                 : k_encode<T, true, true, false, false, true, kOutSector, true>;
+    if (outm == kOutSector) return k_encode<T, true, true, false, false, true, kOutSector, true>;
   }
-  return fos ? k_encode<T, true, true, true, false, true, kOutDirect, true>
-             : k_encode<T, true, true, false, false, true, kOutDirect, true>;
+  return k_encode<T, true, true, false, false, true, kOutDirect, true>;
 }
 
 template <typename T>
@@ -1436,6 +1317,23 @@ int pipe_grid_size(int64_t num_tiles, int num_sms) {
 cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStream_t stream) {
   const bool row = q.row_codes != nullptr, col = q.col_codes != nullptr;
   if (!row && !col) return cudaSuccess;
+  if (row && col && (q.block_2d ? q.row_amax != q.col_amax : q.four_over_six)) {
+    // Both directions as two single-direction passes: rows, then columns walked the
+    // other way (starting on the tiles the first pass left in L2).  16x16 tiles share
+    // one scale per tile, so two different per-tensor amax need two passes; and
+    // four-over-six with 1x16 blocks is faster so: a two-direction kernel would hold
+    // both directions' block routines and spill at the 96 registers that two CTAs per
+    // SM allow (measured with given amax, BF16: X 16384 x 8192 215.7 -> 194.2 us, dY
+    // 16384 x 28672 725.7 -> 625.2 us, although x is read twice).
+    QuantArgs qr = q, qc = q;
+    qr.col_codes = nullptr;
+    qr.rht = false;  // the transform belongs to the columnwise side
+    qc.row_codes = nullptr;
+    qc.copy_dst = nullptr;
+    qc.reverse_walk = !q.reverse_walk;
+    const cudaError_t e = launch_quantize(qr, dev, stream);
+    return e != cudaSuccess ? e : launch_quantize(qc, dev, stream);
+  }
   const bool bf16 = q.in == InType::BF16;
   const int box_cols = bf16 ? TileGeo<uint16_t>::BOXC : TileGeo<float>::BOXC;
   const int tile_cols = 2 * box_cols;
@@ -1474,6 +1372,7 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
   a.col_grouped_pt = q.col_grouped_per_tensor ? 1 : 0;
   a.in_rows = q.pad_ends != nullptr ? q.in_rows : q.M;
   a.rht_mask = q.rht_mask;
+  a.reverse_walk = q.reverse_walk ? 1 : 0;
   if (a.grid.num_tiles == 0) return cudaSuccess;
   if (q.rht && (q.block_2d || q.pad_ends != nullptr || (q.col_grouped && row)))
     return cudaErrorInvalidValue;  // the transform is built for the 1x16 paths
@@ -1535,6 +1434,7 @@ cudaError_t launch_quantize(const QuantArgs& q, const DeviceInfo& dev, cudaStrea
                                      : pick_rht<float>(q.four_over_six, tma, outm))
                : bf16 ? pick_dir<uint16_t>(row, col, q.four_over_six, q.block_2d, tma, outm)
                       : pick_dir<float>(row, col, q.four_over_six, q.block_2d, tma, outm);
+  if (fn == nullptr) return cudaErrorInvalidValue;  // split into two passes above
   const int smem = outm == kOutTma ? EncodeSmem<kOutTma>::kBytes
                    : outm == kOutSector ? EncodeSmem<kOutSector>::kBytes
                                         : EncodeSmem<kOutDirect>::kBytes;
