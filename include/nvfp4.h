@@ -135,7 +135,9 @@ NVFP4_API nvfp4_status nvfp4_amax(const void *x, int32_t in_dtype, int64_t rows,
  *   cfg: see nvfp4_config.  row / col: the output direction(s); amax length is
  *   rows / cols for ROW_SCALED and 1 for PER_TENSOR.  The _both variant reads x
  *   for the amax pass and once more for the encode pass (a global amax must be
- *   known before the first code), in one stream-ordered sequence of kernels.
+ *   known before the first code), in one stream-ordered sequence of kernels; with
+ *   four-over-six and 1x16 blocks the encode runs as one pass per direction (x is
+ *   read once more; faster than one pass holding both directions' block routines).
  */
 NVFP4_API nvfp4_status nvfp4_quantize_rowwise(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
                                     const nvfp4_config *cfg, const nvfp4_out *row,
@@ -293,7 +295,8 @@ NVFP4_API nvfp4_status nvfp4_grouped_quantize_columnwise_rht(const void *x, int3
                                                    nvfp4_stream_t stream);
 
 /*
- * nvfp4_quantize_both_rht -- both directions in one encode pass, the transform on the
+ * nvfp4_quantize_both_rht -- both directions in one call (one encode pass; two, one per
+ * direction, with four-over-six), the transform on the
  * transposed side only ([TE-3206]: the fprop operand as it is, the wgrad operand
  * rotated): row = nvfp4_quantize_rowwise(x, cfg), col =
  * nvfp4_quantize_columnwise_rht(x, sign_mask, cfg), byte for byte.

@@ -240,7 +240,8 @@ BOTH_CONFIGS = [c for c in CONFIGS if not c[3]]
                                    (1024, 96), (272, 512), (400, 1024)])
 @pytest.mark.parametrize("conf", BOTH_CONFIGS)
 def test_quantize_both_rht_matches_oracle(dtype, shape, conf):
-    """Both directions in one encode pass, the transform on the columnwise side only
+    """Both directions in one call (one encode pass, or one per direction with
+    four-over-six), the transform on the columnwise side only
     ("NVFP4: enable row-scaled transpose quantization for backward", TE PR #3206,
     description: rowwise for fprop, the transposed operand for wgrad)."""
     rows, cols = shape
