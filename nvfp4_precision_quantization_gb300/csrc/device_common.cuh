@@ -227,6 +227,34 @@ __device__ __forceinline__ void mul2_rn(float a, float b, float e, float& ra, fl
       : "f"(a), "f"(b), "f"(e));
 }
 
+// The two four-over-six candidates of a block at once: the steps of block_encode<6>
+// and block_encode<4> (and of dequant_factor for each), with the products paired in
+// packed multiplies and the two scale bytes converted, and decoded, by one
+// instruction each (cvt ...e4m3x2: the second source lands in the low byte, which
+// decodes into the low half).  Every value is rounded as in the separate steps.
+template <bool SHORT>
+__device__ __forceinline__ void block_encode_pair(float b, float S, float a, float F_inv,
+                                                  BlockEnc& e6, BlockEnc& e4, float& D6,
+                                                  float& D4) {
+  const float q6 = SHORT ? div6_short(b) : __fdiv_rn(b, 6.0f);
+  const float q4 = __fmul_rn(b, 0.25f);  // b/4 == b*0.25 exactly
+  float s6, s4;
+  mul2_rn(q6, q4, S, s6, s4);
+  uint16_t pr;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pr) : "f"(s4), "f"(s6));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));
+  e6.s8 = pr & 0xffu;
+  e4.s8 = (uint32_t)pr >> 8;
+  e6.sd = f16_bits_to_f32(h2);
+  e4.sd = f16_bits_to_f32(h2 >> 16);
+  e6.e = (e6.sd == 0.0f) ? 0.0f : div_by_scale(S, e6.sd);
+  e4.e = (e4.sd == 0.0f) ? 0.0f : div_by_scale(S, e4.sd);
+  float t6, t4;
+  mul2_rn(e6.sd, e4.sd, a, t6, t4);
+  mul2_rn(t6, t4, F_inv, D6, D4);
+}
+
 // Eight codes of x[0..7] scaled by e (products via packed multiplies).
 __device__ __forceinline__ uint32_t codes8(const float* x, float e) {
   float y[8];
@@ -495,20 +523,20 @@ template <bool FOS, bool SHORT = false>
 __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S, float a,
                                                float F_inv, float negz, uint32_t& c0,
                                                uint32_t& c1) {
-  BlockEnc e6 = block_encode<6, SHORT>(b, S);
   if constexpr (!FOS) {
+    const BlockEnc e6 = block_encode<6, SHORT>(b, S);
     c0 = codes8(x, e6.e);
     c1 = codes8(x + 8, e6.e);
     return e6.s8;
   } else {
-    BlockEnc e4 = block_encode<4>(b, S);
+    BlockEnc e6, e4;
+    float D6, D4;
+    block_encode_pair<SHORT>(b, S, a, F_inv, e6, e4, D6, D4);
     float s6a = 0.0f, s6b = 0.0f, s4a = 0.0f, s4b = 0.0f;
     c0 = codes8_residual(x, e6.e, s6a, s6b);
     c1 = codes8_residual(x + 8, e6.e, s6a, s6b);
     const uint32_t d0 = codes8_residual(x, e4.e, s4a, s4b);
     const uint32_t d1 = codes8_residual(x + 8, e4.e, s4a, s4b);
-    const float D6 = dequant_factor(e6.sd, a, F_inv);
-    const float D4 = dequant_factor(e4.sd, a, F_inv);
     // one scale byte: the same codes and errors, and a tie keeps T = 6
     int pick = e4.s8 == e6.s8 ? 0
                               : fos_bounded_pick(b, e6.e, e4.e, D6, D4, __fadd_rn(s6a, s6b),
