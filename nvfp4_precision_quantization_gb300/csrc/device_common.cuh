@@ -227,6 +227,19 @@ __device__ __forceinline__ void mul2_rn(float a, float b, float e, float& ra, fl
       : "f"(a), "f"(b), "f"(e));
 }
 
+// (ra, rb) = (fl(a0 * b0), fl(a1 * b1)): one packed multiply of two pairs.  The
+// compiler may contract a packed multiply into an addition that uses it (mul2_fma is
+// the form that cannot be), so this is for products where one rounding fewer is
+// harmless.
+__device__ __forceinline__ void mul2_pair(float a0, float a1, float b0, float b1, float& ra,
+                                          float& rb) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(ra), "=f"(rb)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // The two four-over-six candidates of a block at once: the steps of block_encode<6>
 // and block_encode<4> (and of dequant_factor for each), with the products paired in
 // packed multiplies and the two scale bytes converted, and decoded, by one
@@ -424,15 +437,19 @@ __device__ __forceinline__ uint32_t codes8_residual(const float* x, float e, flo
 // E'4 - E'6 < -2^-12 (D4^2 + D6^2) (after the roundings of that comparison), and fails
 // whenever the difference exceeds +2^-12 (D4^2 + D6^2).  Returns 1 (T = 4), 0 (T = 6)
 // or -1: the estimates are too close, or the block is outside the ranges above (inf,
-// NaN and saturated blocks included), and the exact sums decide.
-__device__ __forceinline__ int fos_bounded_pick(float b, float e6, float e4, float D6, float D4,
-                                                float A6, float A4) {
-  const float y6 = __fmul_rn(b, e6), y4 = __fmul_rn(b, e4);
-  const bool in_range = y6 <= 6.5f && y4 <= 6.5f && D6 >= 0x1p-62f && D6 <= 0x1p61f &&
-                        D4 >= 0x1p-62f && D4 <= 0x1p61f;
-  if (!in_range) return -1;
-  const float q6 = __fmul_rn(D6, D6), q4 = __fmul_rn(D4, D4);
-  const float diff = __fsub_rn(__fmul_rn(q4, A4), __fmul_rn(q6, A6));
+// NaN and saturated blocks included), and the exact sums decide.  The ranges take
+// three comparisons: fl(b/4) >= fl(b/6) and every rounding step is monotonic, so the
+// T = 4 scale is at least the T = 6 one, hence D4 >= D6 and fl(b e4) <= fl(b e6).
+// The paired products round as the scalar ones (a contraction into the difference or
+// the sum that follows would only drop a rounding, which the margin covers).
+__device__ __forceinline__ int fos_bounded_pick(float b, float e6, float D6, float D4, float A6,
+                                                float A4) {
+  const float y6 = __fmul_rn(b, e6);
+  if (!(y6 <= 6.5f && D6 >= 0x1p-62f && D4 <= 0x1p61f)) return -1;
+  float q6, q4, E6, E4;
+  mul2_pair(D6, D4, D6, D4, q6, q4);
+  mul2_pair(q6, q4, A6, A4, E6, E4);
+  const float diff = __fsub_rn(E4, E6);
   const float tol = __fmul_rn(0x1p-12f, __fadd_rn(q4, q6));
   return diff < -tol ? 1 : (diff > tol ? 0 : -1);
 }
@@ -539,7 +556,7 @@ __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S,
     const uint32_t d1 = codes8_residual(x + 8, e4.e, s4a, s4b);
     // one scale byte: the same codes and errors, and a tie keeps T = 6
     int pick = e4.s8 == e6.s8 ? 0
-                              : fos_bounded_pick(b, e6.e, e4.e, D6, D4, __fadd_rn(s6a, s6b),
+                              : fos_bounded_pick(b, e6.e, D6, D4, __fadd_rn(s6a, s6b),
                                                  __fadd_rn(s4a, s4b));
     if (pick < 0)  // the exact sums
       pick = fos_exact_pick(make_float4(x[0], x[1], x[2], x[3]),

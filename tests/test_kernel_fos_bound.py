@@ -66,11 +66,16 @@ def candidate_errors(x: np.ndarray, a: np.ndarray, bound: float):
 
 
 def decide(c):
-    """The kernel's decision: 1 (T = 4), 0 (T = 6) or -1 (exact sums)."""
+    """The kernel's decision: 1 (T = 4), 0 (T = 6) or -1 (exact sums).  The kernel
+    checks fl(b e6) <= 6.5, D6 >= 2^-62 and D4 <= 2^61 only: the T = 4 scale is never
+    below the T = 6 one, so the same bounds then hold for the other candidate (checked
+    here on every block)."""
     c6, c4 = c[6], c[4]
-    ok = (c6["ymax"] <= 6.5) & (c4["ymax"] <= 6.5)
+    full = (c6["ymax"] <= 6.5) & (c4["ymax"] <= 6.5)
     for D in (c6["D"], c4["D"]):
-        ok &= (D >= 2.0 ** -62) & (D <= 2.0 ** 61)
+        full &= (D >= 2.0 ** -62) & (D <= 2.0 ** 61)
+    ok = (c6["ymax"] <= 6.5) & (c6["D"] >= 2.0 ** -62) & (c4["D"] <= 2.0 ** 61)
+    assert np.array_equal(ok, full)
     q6 = (c6["D"] * c6["D"]).astype(f32)
     q4 = (c4["D"] * c4["D"]).astype(f32)
     diff = (c4["est"] - c6["est"]).astype(f32)
