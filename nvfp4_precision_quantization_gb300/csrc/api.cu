@@ -54,6 +54,7 @@ bool bytes_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
 struct DevCacheEntry {
   bool ready = false;
   int num_sms = 0;
+  int64_t l2_bytes = 0;
   int* status = nullptr;
   uint8_t* gemm_static_ws = nullptr;  // device address of g_gemm_static_ws
 };
@@ -69,8 +70,10 @@ nvfp4_status current_device(DeviceInfo* out) {
   std::lock_guard<std::mutex> lock(g_mu);
   DevCacheEntry& c = g_dev[dev];
   if (!c.ready) {
-    int sms = 0;
+    int sms = 0, l2 = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_status_word);
@@ -79,12 +82,14 @@ nvfp4_status current_device(DeviceInfo* out) {
     e = cudaGetSymbolAddress(&ws, g_gemm_static_ws);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static GEMM workspace)");
     c.num_sms = sms;
+    c.l2_bytes = l2;
     c.status = static_cast<int*>(p);
     c.gemm_static_ws = static_cast<uint8_t*>(ws);
     c.ready = true;
   }
   out->device = dev;
   out->num_sms = c.num_sms;
+  out->l2_bytes = c.l2_bytes;
   out->status = c.status;
   out->gemm_static_ws = c.gemm_static_ws;
   return NVFP4_OK;

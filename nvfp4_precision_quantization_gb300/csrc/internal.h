@@ -13,6 +13,7 @@ enum class InType : int { BF16 = 0, FP32 = 1 };
 struct DeviceInfo {
   int device;
   int num_sms;
+  int64_t l2_bytes;  // the device's L2 size
   int* status;  // device address of the library status word
   uint8_t* gemm_static_ws;  // device address of the static GEMM workspace
 };
