@@ -1,22 +1,22 @@
-"""Four-over-six in the two-direction encode at sizes where every persistent CTA
-walks several tiles, compared byte for byte with the oracle.
+"""Four-over-six with both directions at sizes where every persistent CTA walks
+several tiles, compared byte for byte with the oracle.
 
 The encode kernel runs min(tiles, 2 x SMs) CTAs, each over a contiguous chunk of
 the tile order, so the small parity shapes give every CTA one tile at most.  These
 shapes give each CTA two to eight tiles.  That exercises the ring wrap, the tile
-cursor's walk and the super-strip scale sectors with the four-over-six block choice
-("Add NVFP4 four-over-six grouped GEMM for MoE training", torchao PR #9,
-description: the block scaled to 4 or to 6 by the lower squared error, bound 448 or
-256) on each of the kernel's three output paths for BF16 input with both
-directions ("NVFP4: enable row-scaled transpose quantization for backward",
-TransformerEngine PR #3206, description):
+cursor's walk (the columnwise pass walks each chunk the other way) and the scale
+stores with the four-over-six block choice ("Add NVFP4 four-over-six grouped GEMM
+for MoE training", torchao PR #9, description: the block scaled to 4 or to 6 by the
+lower squared error, bound 448 or 256) with both directions ("NVFP4: enable
+row-scaled transpose quantization for backward", TransformerEngine PR #3206,
+description).  With 1x16 blocks each direction is its own encode pass; the
+shapes cover its output paths:
 
-* 4096 x 4096 (the outliers workload): code pitches multiples of 32 bytes, one
-  32-byte sector store per thread; 1024 tiles.
-* 3232 x 9184: code pitches multiples of 16 but not of 32 bytes, per-warp staging
-  and TMA tensor stores; 936 tiles.
-* 4000 x 5000: pitches that allow neither, 16-byte or byte stores; 640 tiles
-  (BF16) and 2528 (FP32).
+* 4096 x 4096 (the outliers workload): columnwise code pitch a multiple of 32
+  bytes, one 32-byte sector store per lane pair; 1024 tiles.
+* 3232 x 9184 and 4000 x 5000: pitches multiples of 16 but not of 32 bytes, or
+  neither: direct 16-byte, 4-byte or byte stores; 936 and 640 tiles (BF16), 2528
+  (4000 x 5000 FP32).  The rowwise pass stores directly on every shape.
 
 The oracle runs in host threads over strips of lines (oracle.quantize_parallel, held
 equal to the whole-tensor oracle by tests/test_oracle_parallel.py).
@@ -37,23 +37,20 @@ DEV = "cuda"
 
 CASES = {
     "sector_4096x4096": lambda: workloads.outliers(DEV),
-    "tma_out_3232x9184": lambda: workloads.seeded_normal(3232, 9184, seed=31, device=DEV,
-                                                         row_scale_decades=2.0),
+    "direct_3232x9184": lambda: workloads.seeded_normal(3232, 9184, seed=31, device=DEV,
+                                                        row_scale_decades=2.0),
     "direct_4000x5000_bf16": lambda: workloads.edge_normal(4000, 5000, torch.bfloat16, DEV),
     "direct_4000x5000_fp32": lambda: workloads.edge_normal(4000, 5000, torch.float32, DEV),
 }
 
 
 def _output_path(rows, cols, dtype):
-    """Which store path the launcher picks for these pitches (BF16, both directions)."""
+    """The columnwise pass's store path for these pitches (the rowwise pass of
+    four-over-six stores directly): whole sectors when the BF16 code pitch is a
+    multiple of 32 bytes."""
     if dtype != torch.bfloat16:
         return "direct"
-    rp, cp = (cols + 1) // 2, (rows + 1) // 2
-    if rp % 32 == 0 and cp % 32 == 0:
-        return "sector"
-    if rp % 16 == 0 and cp % 16 == 0:
-        return "tma_out"
-    return "direct"
+    return "sector" if ((rows + 1) // 2) % 32 == 0 else "direct"
 
 
 @pytest.fixture(scope="module", params=list(CASES))
