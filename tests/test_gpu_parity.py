@@ -146,21 +146,23 @@ def test_quantize_with_given_amax():
     ra, ca, _ = oracle.amax(xb, tag)
     ra = ra * np.float32(1.5)   # any positive amax is allowed
     ca = ca * np.float32(0.75)
-    c = cfg(nv.NVFP4_ROW_SCALED)
-    g = gpu_quantize(x, c, row_amax_in=torch.from_numpy(ra).to(DEV),
-                     col_amax_in=torch.from_numpy(ca).to(DEV))
-    o = oracle_quantize(x, c, row_amax_in=ra, col_amax_in=ca)
-    assert_same(g["row"], o["row"], "row")
-    assert_same(g["col"], o["col"], "col")
+    # four-over-six too: both directions then run as one pass per direction
+    for fos in (False, True):
+        c = cfg(nv.NVFP4_ROW_SCALED, 448.0, fos)
+        g = gpu_quantize(x, c, row_amax_in=torch.from_numpy(ra).to(DEV),
+                         col_amax_in=torch.from_numpy(ca).to(DEV))
+        o = oracle_quantize(x, c, row_amax_in=ra, col_amax_in=ca)
+        assert_same(g["row"], o["row"], f"row fos={fos}")
+        assert_same(g["col"], o["col"], f"col fos={fos}")
     # per-tensor with different scalars per direction, 16x16 blocks too
-    for b2d in (False, True):
-        c = cfg(nv.NVFP4_PER_TENSOR, 448.0, False, b2d)
+    for b2d, fos in ((False, False), (True, False), (False, True), (True, True)):
+        c = cfg(nv.NVFP4_PER_TENSOR, 448.0, fos, b2d)
         g = gpu_quantize(x, c, row_amax_in=torch.tensor([7.0], device=DEV),
                          col_amax_in=torch.tensor([3.0], device=DEV))
         o = oracle_quantize(x, c, row_amax_in=np.array([7.0], np.float32),
                             col_amax_in=np.array([3.0], np.float32))
-        assert_same(g["row"], o["row"], "row")
-        assert_same(g["col"], o["col"], "col")
+        assert_same(g["row"], o["row"], f"row b2d={b2d} fos={fos}")
+        assert_same(g["col"], o["col"], f"col b2d={b2d} fos={fos}")
 
 
 def test_zero_rows_and_zero_tensor():
@@ -180,15 +182,16 @@ def test_noop_preserves_everything():
     x = _x((300, 260), torch.bfloat16, seed=7)
     flag = torch.ones(1, device=DEV)
     for mode in (nv.NVFP4_ROW_SCALED, nv.NVFP4_PER_TENSOR):
-        g = gpu_quantize(x, cfg(mode), noop=flag, fill=0xA5,
-                         outs={"row": nv.alloc_out(300, 260, 300 if mode else 1, DEV, 0xA5),
-                               "col": nv.alloc_out(260, 300, 260 if mode else 1, DEV, 0xA5)})
-        for d in ("row", "col"):
-            g[d].amax.fill_(-1.0)
-        g = gpu_quantize(x, cfg(mode), noop=flag, outs=g)
-        for d in ("row", "col"):
-            assert torch.all(g[d].codes == 0xA5) and torch.all(g[d].scales == 0xA5)
-            assert torch.all(g[d].amax == -1.0)
+        for fos in (False, True):  # four-over-six: one encode pass per direction
+            g = gpu_quantize(x, cfg(mode, 448.0, fos), noop=flag, fill=0xA5,
+                             outs={"row": nv.alloc_out(300, 260, 300 if mode else 1, DEV, 0xA5),
+                                   "col": nv.alloc_out(260, 300, 260 if mode else 1, DEV, 0xA5)})
+            for d in ("row", "col"):
+                g[d].amax.fill_(-1.0)
+            g = gpu_quantize(x, cfg(mode, 448.0, fos), noop=flag, outs=g)
+            for d in ("row", "col"):
+                assert torch.all(g[d].codes == 0xA5) and torch.all(g[d].scales == 0xA5)
+                assert torch.all(g[d].amax == -1.0)
     # amax entry point and grouped entry points too
     r = torch.full((300,), -1.0, device=DEV)
     nv.nvfp4_amax(x, row_amax=r, noop=flag)
