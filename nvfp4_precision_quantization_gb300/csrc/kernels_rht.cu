@@ -289,7 +289,13 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax_rows(RhtAmaxRowsArgs
         const int64_t e = rowbase + r * a.cols;
         if constexpr (BF16) {
           const uint16_t* xb = static_cast<const uint16_t*>(a.x);
-          if constexpr (V == 2) {
+          if constexpr (V == 4) {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(xb + e));
+            v[0][r] = __uint_as_float(w.x << 16);
+            v[1][r] = __uint_as_float(w.x & 0xffff0000u);
+            v[2][r] = __uint_as_float(w.y << 16);
+            v[3][r] = __uint_as_float(w.y & 0xffff0000u);
+          } else if constexpr (V == 2) {
             const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(xb + e));
             v[0][r] = __uint_as_float(w << 16);
             v[1][r] = __uint_as_float(w & 0xffff0000u);
@@ -297,6 +303,7 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax_rows(RhtAmaxRowsArgs
             v[0][r] = __uint_as_float((uint32_t)__ldg(xb + e) << 16);
           }
         } else {
+          static_assert(V <= 2, "four columns per thread: BF16 only");
           const float* xf = static_cast<const float*>(a.x);
           if constexpr (V == 2) {
             const float2 t = __ldg(reinterpret_cast<const float2*>(xf + e));
@@ -330,8 +337,14 @@ __global__ void __launch_bounds__(kRhtThreads) k_rht16_amax_rows(RhtAmaxRowsArgs
       if ((lane & 1) == 0 && m[0] > 0.0f)
         atomicMax(reinterpret_cast<unsigned int*>(s_rmax + 16 * (rb - rb0) + my_row),
                   __float_as_uint(m[0]));
-      if constexpr (V == 2) rht16_block2(v[0], v[1], a.mask);
-      else rht16_block(v[0], a.mask);
+      if constexpr (V == 4) {
+        rht16_block2(v[0], v[1], a.mask);
+        rht16_block2(v[2], v[3], a.mask);
+      } else if constexpr (V == 2) {
+        rht16_block2(v[0], v[1], a.mask);
+      } else {
+        rht16_block(v[0], a.mask);
+      }
 #pragma unroll
       for (int k = 0; k < V; ++k) {
 #pragma unroll
@@ -380,9 +393,15 @@ bool pair_ok(const void* x, bool bf16, int64_t cols, const void* y) {
 
 }  // namespace
 
+// BF16 rows of 4 x 256-column multiples: four columns per thread (the row maxima's
+// shuffle reduction then serves twice the elements).
+bool quad_ok(const void* x, bool bf16, int64_t cols) {
+  return bf16 && cols % (4 * kRhtThreads) == 0 && reinterpret_cast<uintptr_t>(x) % 8 == 0;
+}
+
 bool rht16_amax_rows_supported(const void* x, bool bf16, int64_t cols) {
   const int64_t groups = pair_ok(x, bf16, cols, nullptr) ? cols / 2 : cols;
-  return groups % kRhtThreads == 0;
+  return quad_ok(x, bf16, cols) || groups % kRhtThreads == 0;
 }
 
 cudaError_t launch_rht16_amax_rows(const RhtAmaxArgs& q, float* row_max, float* row_tensor,
@@ -390,13 +409,14 @@ cudaError_t launch_rht16_amax_rows(const RhtAmaxArgs& q, float* row_max, float* 
   if (q.rows == 0 || q.cols == 0) return cudaSuccess;
   if (!rht16_amax_rows_supported(q.x, q.bf16, q.cols) || q.group_ends != nullptr)
     return cudaErrorInvalidValue;
+  const bool quad = quad_ok(q.x, q.bf16, q.cols);
   const bool pair = pair_ok(q.x, q.bf16, q.cols, nullptr);
   RhtAmaxRowsArgs ra{};
   RhtAmaxKernelArgs& a = ra.k;
   a.x = q.x;
   a.rows = q.rows;
   a.cols = q.cols;
-  a.groups = pair ? q.cols / 2 : q.cols;
+  a.groups = quad ? q.cols / 4 : pair ? q.cols / 2 : q.cols;
   a.chunks = (q.rows / 16 + kAmaxBlocks - 1) / kAmaxBlocks;
   a.items = a.chunks * a.groups;
   a.mask = q.sign_mask;
@@ -407,8 +427,11 @@ cudaError_t launch_rht16_amax_rows(const RhtAmaxArgs& q, float* row_max, float* 
   ra.row_tensor = row_tensor;
   const int64_t blocks = std::min<int64_t>(a.items / kRhtThreads, 8LL * dev.num_sms);
   void (*fn)(RhtAmaxRowsArgs);
-  if (q.bf16) fn = pair ? k_rht16_amax_rows<true, 2> : k_rht16_amax_rows<true, 1>;
-  else fn = pair ? k_rht16_amax_rows<false, 2> : k_rht16_amax_rows<false, 1>;
+  if (q.bf16)
+    fn = quad ? k_rht16_amax_rows<true, 4>
+              : pair ? k_rht16_amax_rows<true, 2> : k_rht16_amax_rows<true, 1>;
+  else
+    fn = pair ? k_rht16_amax_rows<false, 2> : k_rht16_amax_rows<false, 1>;
   fn<<<(unsigned)blocks, kRhtThreads, 0, stream>>>(ra);
   return cudaGetLastError();
 }
