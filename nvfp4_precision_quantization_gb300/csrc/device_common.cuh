@@ -530,6 +530,72 @@ static __device__ __noinline__ int fos_exact_pick(float4 xa, float4 xb, float4 x
   return err4 < err6;
 }
 
+// Both four-over-six candidates of a block, their codes, and the choice the bounded
+// estimate makes: pick 1 (T = 4), 0 (T = 6) or -1 (open: the exact sums decide).
+struct FosEstimate {
+  uint32_t c0, c1, d0, d1;  // T = 6 and T = 4 code words
+  uint32_t s6, s4;          // scale bytes
+  float D6, D4;             // dequantize factors
+  int pick;
+};
+template <bool SHORT>
+__device__ __forceinline__ FosEstimate fos_estimate(const float* x, float b, float S, float a,
+                                                    float F_inv) {
+  FosEstimate f;
+  BlockEnc e6, e4;
+  block_encode_pair<SHORT>(b, S, a, F_inv, e6, e4, f.D6, f.D4);
+  float s6a = 0.0f, s6b = 0.0f, s4a = 0.0f, s4b = 0.0f;
+  f.c0 = codes8_residual(x, e6.e, s6a, s6b);
+  f.c1 = codes8_residual(x + 8, e6.e, s6a, s6b);
+  f.d0 = codes8_residual(x, e4.e, s4a, s4b);
+  f.d1 = codes8_residual(x + 8, e4.e, s4a, s4b);
+  f.s6 = e6.s8;
+  f.s4 = e4.s8;
+  // one scale byte: the same codes and errors, and a tie keeps T = 6
+  f.pick = e4.s8 == e6.s8 ? 0
+                          : fos_bounded_pick(b, e6.e, f.D6, f.D4, __fadd_rn(s6a, s6b),
+                                             __fadd_rn(s4a, s4b));
+  return f;
+}
+
+// Four-over-six with the open blocks left to the caller: writes the chosen codes and
+// returns the scale byte; for an open block (open = true) those of T = 6, which the
+// caller replaces with the exact choice (quantize16_exact) before storing them.
+template <bool SHORT>
+__device__ __forceinline__ uint32_t quantize16_est(const float* x, float b, float S, float a,
+                                                   float F_inv, uint32_t& c0, uint32_t& c1,
+                                                   bool& open) {
+  const FosEstimate f = fos_estimate<SHORT>(x, b, S, a, F_inv);
+  open = f.pick < 0;
+  const bool four = f.pick > 0;
+  c0 = four ? f.d0 : f.c0;
+  c1 = four ? f.d1 : f.c1;
+  return four ? f.s4 : f.s6;
+}
+
+// The exact four-over-six choice of one block (the in-order error sums of both
+// candidates): writes the codes and returns the scale byte.
+template <bool SHORT>
+__device__ __forceinline__ uint32_t quantize16_exact(const float* x, float b, float S, float a,
+                                                     float F_inv, float negz, uint32_t& c0,
+                                                     uint32_t& c1) {
+  BlockEnc e6, e4;
+  float D6, D4;
+  block_encode_pair<SHORT>(b, S, a, F_inv, e6, e4, D6, D4);
+  c0 = codes8(x, e6.e);
+  c1 = codes8(x + 8, e6.e);
+  if (e4.s8 == e6.s8) return e6.s8;
+  const uint32_t d0 = codes8(x, e4.e), d1 = codes8(x + 8, e4.e);
+  const float err4 = sse16_signed(0.0f, x, d0, d1, D4, negz);
+  const float err6 = sse16_magnitudes(0.0f, x, c0, c1, D6, negz);
+  if (err4 < err6) {
+    c0 = d0;
+    c1 = d1;
+    return e4.s8;
+  }
+  return e6.s8;
+}
+
 // Quantize 16 FP32 values of one block whose max |x| is b: writes the two code
 // words (value k in nibble k) and returns the scale byte.  FOS: four-over-six
 // (needs the line amax a and F_inv for the error of each candidate, and negz =
@@ -546,30 +612,17 @@ __device__ __forceinline__ uint32_t quantize16(const float* x, float b, float S,
     c1 = codes8(x + 8, e6.e);
     return e6.s8;
   } else {
-    BlockEnc e6, e4;
-    float D6, D4;
-    block_encode_pair<SHORT>(b, S, a, F_inv, e6, e4, D6, D4);
-    float s6a = 0.0f, s6b = 0.0f, s4a = 0.0f, s4b = 0.0f;
-    c0 = codes8_residual(x, e6.e, s6a, s6b);
-    c1 = codes8_residual(x + 8, e6.e, s6a, s6b);
-    const uint32_t d0 = codes8_residual(x, e4.e, s4a, s4b);
-    const uint32_t d1 = codes8_residual(x + 8, e4.e, s4a, s4b);
-    // one scale byte: the same codes and errors, and a tie keeps T = 6
-    int pick = e4.s8 == e6.s8 ? 0
-                              : fos_bounded_pick(b, e6.e, D6, D4, __fadd_rn(s6a, s6b),
-                                                 __fadd_rn(s4a, s4b));
+    const FosEstimate f = fos_estimate<SHORT>(x, b, S, a, F_inv);
+    int pick = f.pick;
     if (pick < 0)  // the exact sums
       pick = fos_exact_pick(make_float4(x[0], x[1], x[2], x[3]),
                             make_float4(x[4], x[5], x[6], x[7]),
                             make_float4(x[8], x[9], x[10], x[11]),
-                            make_float4(x[12], x[13], x[14], x[15]), c0, c1, d0, d1, D6, D4,
-                            negz);
-    if (pick) {
-      c0 = d0;
-      c1 = d1;
-      return e4.s8;
-    }
-    return e6.s8;
+                            make_float4(x[12], x[13], x[14], x[15]), f.c0, f.c1, f.d0, f.d1,
+                            f.D6, f.D4, negz);
+    c0 = pick ? f.d0 : f.c0;
+    c1 = pick ? f.d1 : f.c1;
+    return pick ? f.s4 : f.s6;
   }
 }
 

@@ -181,10 +181,53 @@ __device__ __forceinline__ uint32_t encode_block(const float* x, float b, float 
 
 // ---------------------------------------------------------------- rowwise
 
+// Block j of a box row (row pointer rowp, swizzle sw) as 16 FP32 values; returns
+// the block max (MAX) or 0.
+template <typename T, bool MAX>
+__device__ __forceinline__ float load_row_block(const uint8_t* rowp, int j, int sw,
+                                                float (&x)[16]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint4 v0 = lds128(rowp + (((2 * j) ^ sw) << 4));
+    const uint4 v1 = lds128(rowp + (((2 * j + 1) ^ sw) << 4));
+    const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = bf16_lo(u[i]);
+      x[2 * i + 1] = bf16_hi(u[i]);
+    }
+    return MAX ? absmax8_bf16(v0, v1) : 0.0f;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = lds128(rowp + (((4 * j + k) ^ sw) << 4));
+      x[4 * k] = __uint_as_float(v.x);
+      x[4 * k + 1] = __uint_as_float(v.y);
+      x[4 * k + 2] = __uint_as_float(v.z);
+      x[4 * k + 3] = __uint_as_float(v.w);
+    }
+    return MAX ? absmax16_f32(x) : 0.0f;
+  }
+}
+
+// The exact four-over-six choice of block j of a box row, its values read again from
+// the stage: codes in x, y, scale byte in z.  For the blocks the bound left open;
+// out of line, so that its code stays out of the encode loop.
+template <typename T>
+__device__ __noinline__ uint3 row_block_exact(const uint8_t* rowp, int j, int sw, float S,
+                                              float A, float F_inv, float negz) {
+  float x[16];
+  const float b = load_row_block<T, true>(rowp, j, sw, x);
+  uint3 r;
+  r.z = quantize16_exact<sizeof(T) == 2>(x, b, S, A, F_inv, negz, r.x, r.y);
+  return r;
+}
+
 // Codes and scales of row r of boxes [b0, b0 + NBOX): w[box][word], sc[box].
 // Rows / columns outside x were zero-filled by the load, so they encode to 0;
 // the caller decides what is stored.  rot = 4 (BF16) makes step j read block
-// j ^ 2 of the box row (its results land in the slots of block j).
+// j ^ 2 of the box row (its results land in the slots of block j).  With
+// four-over-six the bound settles each block; the blocks it leaves open are redone
+// with the exact sums after the loop (one test per row instead of one per block).
 template <typename T, int NBOX, bool FOS, bool B2D, typename M>
 __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m,
                                                 const EncodeArgs& a, int r, int b0, float S_t,
@@ -193,9 +236,11 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m
                                                 uint32_t (&sc)[NBOX], int rot = 0) {
   using G = TileGeo<T>;
   constexpr int NB = G::BOXC / 16;  // blocks per box row
+  constexpr bool DEFER = FOS && !B2D;
   const float S = a.row_scaled ? m.rowS[r] : S_t;
   const float A = a.row_scaled ? m.rowA(r) : A_t;
   const int sw = (r & 7) ^ rot;
+  uint32_t open_mask = 0;
 #pragma unroll
   for (int bi = 0; bi < NBOX; ++bi) {
     const int box = b0 + bi;
@@ -204,38 +249,42 @@ __device__ __forceinline__ void rowwise_compute(const uint8_t* stage, const M& m
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       float x[16];
-      float b;
-      if constexpr (sizeof(T) == 2) {
-        const uint4 v0 = lds128(rowp + (((2 * j) ^ sw) << 4));
-        const uint4 v1 = lds128(rowp + (((2 * j + 1) ^ sw) << 4));
-        const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[2 * i] = bf16_lo(u[i]);
-          x[2 * i + 1] = bf16_hi(u[i]);
-        }
-        b = B2D ? 0.0f : absmax8_bf16(v0, v1);
+      const float b = load_row_block<T, !B2D>(rowp, j, sw, x);
+      if constexpr (DEFER) {
+        bool open;
+        sc[bi] |= quantize16_est<sizeof(T) == 2>(x, b, S, A, a.F_inv, w[bi][2 * j],
+                                                 w[bi][2 * j + 1], open)
+                  << (8 * j);
+        open_mask |= (uint32_t)open << (bi * NB + j);
       } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v = lds128(rowp + (((4 * j + k) ^ sw) << 4));
-          x[4 * k] = __uint_as_float(v.x);
-          x[4 * k + 1] = __uint_as_float(v.y);
-          x[4 * k + 2] = __uint_as_float(v.z);
-          x[4 * k + 3] = __uint_as_float(v.w);
+        uint32_t s2 = 0;
+        float e2 = 0.0f;
+        if constexpr (B2D) {
+          const int sub = (r >> 4) * (G::TILEC / 16) + box * NB + j;
+          s2 = m.s2d(sub);
+          e2 = m.e2d(sub);
         }
-        b = B2D ? 0.0f : absmax16_f32(x);
+        sc[bi] |= encode_block<FOS, B2D, sizeof(T) == 2>(x, b, S, A, a.F_inv, a.neg_zero, s2,
+                                                         e2, w[bi][2 * j], w[bi][2 * j + 1])
+                  << (8 * j);
       }
-      uint32_t s2 = 0;
-      float e2 = 0.0f;
-      if constexpr (B2D) {
-        const int sub = (r >> 4) * (G::TILEC / 16) + box * NB + j;
-        s2 = m.s2d(sub);
-        e2 = m.e2d(sub);
+    }
+  }
+  if constexpr (DEFER) {
+    if (open_mask != 0) {
+#pragma unroll
+      for (int bi = 0; bi < NBOX; ++bi) {
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          if (open_mask & (1u << (bi * NB + j))) {
+            const uint3 e = row_block_exact<T>(stage + (b0 + bi) * kBoxBytes + r * 128, j, sw,
+                                               S, A, a.F_inv, a.neg_zero);
+            w[bi][2 * j] = e.x;
+            w[bi][2 * j + 1] = e.y;
+            sc[bi] = (sc[bi] & ~(0xffu << (8 * j))) | (e.z << (8 * j));
+          }
+        }
       }
-      sc[bi] |= encode_block<FOS, B2D, sizeof(T) == 2>(x, b, S, A, a.F_inv, a.neg_zero, s2, e2,
-                                                       w[bi][2 * j], w[bi][2 * j + 1])
-                << (8 * j);
     }
   }
 }
