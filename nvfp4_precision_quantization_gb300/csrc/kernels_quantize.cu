@@ -487,6 +487,30 @@ __device__ __forceinline__ void rowwise_store_scales(const EncodeArgs& a, int r,
 // Codes and scales of column pair (cl, cl + 1) over rows [rb0, rb0 + RG).
 // RHT_PAIR: the two columns' transforms as packed pairs (fewer instructions, more
 // registers: used where the register budget allows, the columnwise-only kernels).
+// The exact four-over-six choice of one column's 16-row block (column c of the pair
+// at base, row i at base + i * 128 + coff[i & 7]), read again from the stage: codes in
+// x, y, scale byte in z.  For the blocks the bound left open; out of line.
+template <typename T>
+__device__ __noinline__ uint3 col_block_exact(const uint8_t* base, int4 ca, int4 cb, int c,
+                                              float S, float A, float F_inv, float negz) {
+  const int32_t coff[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(base + i * 128 + coff[i & 7]);
+      x[i] = c ? bf16_hi(v) : bf16_lo(v);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(base + i * 128 + coff[i & 7]);
+      x[i] = c ? v.y : v.x;
+    }
+  }
+  const float b = absmax16_f32(x);
+  uint3 r;
+  r.z = quantize16_exact<sizeof(T) == 2>(x, b, S, A, F_inv, negz, r.x, r.y);
+  return r;
+}
+
 template <typename T, int RG, bool FOS, bool B2D, bool RHT = false, bool RHT_PAIR = false,
           typename M>
 __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m,
@@ -500,6 +524,9 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
   const float S1 = a.row_scaled ? m.colS[cl + 1] : S_t;
   const float A0 = a.row_scaled ? m.colA(cl) : A_t;
   const float A1 = a.row_scaled ? m.colA(cl + 1) : A_t;
+  // four-over-six: the blocks the bound leaves open are redone after the loop
+  constexpr bool DEFER = FOS && !B2D && !RHT;
+  uint32_t open_mask = 0;
   sc0 = sc1 = 0;
 #pragma unroll
   for (int jb = 0; jb < NB; ++jb) {
@@ -559,12 +586,43 @@ __device__ __forceinline__ void colwise_compute(const uint8_t* stage, const M& m
     }
     // SHORT (the BF16 block-max division shortcut) holds only for BF16 block maxima
     constexpr bool SHORT = sizeof(T) == 2 && !RHT;
-    sc0 |= encode_block<FOS, B2D, SHORT>(x0, b0, S0, A0, a.F_inv, a.neg_zero, s2, e2, w0[2 * jb],
-                                         w0[2 * jb + 1])
-           << (8 * jb);
-    sc1 |= encode_block<FOS, B2D, SHORT>(x1, b1, S1, A1, a.F_inv, a.neg_zero, s2, e2, w1[2 * jb],
-                                         w1[2 * jb + 1])
-           << (8 * jb);
+    if constexpr (DEFER) {
+      bool o0, o1;
+      sc0 |= quantize16_est<SHORT>(x0, b0, S0, A0, a.F_inv, w0[2 * jb], w0[2 * jb + 1], o0)
+             << (8 * jb);
+      sc1 |= quantize16_est<SHORT>(x1, b1, S1, A1, a.F_inv, w1[2 * jb], w1[2 * jb + 1], o1)
+             << (8 * jb);
+      open_mask |= ((uint32_t)o0 | ((uint32_t)o1 << 1)) << (2 * jb);
+    } else {
+      sc0 |= encode_block<FOS, B2D, SHORT>(x0, b0, S0, A0, a.F_inv, a.neg_zero, s2, e2,
+                                           w0[2 * jb], w0[2 * jb + 1])
+             << (8 * jb);
+      sc1 |= encode_block<FOS, B2D, SHORT>(x1, b1, S1, A1, a.F_inv, a.neg_zero, s2, e2,
+                                           w1[2 * jb], w1[2 * jb + 1])
+             << (8 * jb);
+    }
+  }
+  if constexpr (DEFER) {
+    if (open_mask != 0) {
+      const int4 ca = make_int4(coff[0], coff[1], coff[2], coff[3]);
+      const int4 cb = make_int4(coff[4], coff[5], coff[6], coff[7]);
+#pragma unroll
+      for (int jb = 0; jb < NB; ++jb) {
+        const uint8_t* base = stage + (rb0 + 16 * jb) * 128;
+        if (open_mask & (1u << (2 * jb))) {
+          const uint3 e = col_block_exact<T>(base, ca, cb, 0, S0, A0, a.F_inv, a.neg_zero);
+          w0[2 * jb] = e.x;
+          w0[2 * jb + 1] = e.y;
+          sc0 = (sc0 & ~(0xffu << (8 * jb))) | (e.z << (8 * jb));
+        }
+        if (open_mask & (2u << (2 * jb))) {
+          const uint3 e = col_block_exact<T>(base, ca, cb, 1, S1, A1, a.F_inv, a.neg_zero);
+          w1[2 * jb] = e.x;
+          w1[2 * jb + 1] = e.y;
+          sc1 = (sc1 & ~(0xffu << (8 * jb))) | (e.z << (8 * jb));
+        }
+      }
+    }
   }
 }
 
